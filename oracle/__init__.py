@@ -1,0 +1,144 @@
+"""TEST INFRASTRUCTURE ONLY: ctypes front end of the plain C oracle.
+
+Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
+leg may import this package. The attention library never imports it, and this
+package never imports the library: the two share nothing but the seeded input
+generators, which hold none of the method's arithmetic.
+
+The oracle (``attn_oracle.c``) restates, single-threaded and in double
+precision, the attention forward O = softmax(Q K^T * scale [+ causal mask]) V
+of the kbench page ("kbench -- Transformer Attention Micro-benchmark Harness",
+section "Implementation details / The three GPU kernels") and the STREAM Triad
+a = b + s*c of the TileOPs "Hardware Microbenchmarks" README (section
+"HBM Bandwidth").
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(HERE, "attn_oracle.c")
+LIBRARY = os.path.join(HERE, "libkboracle.so")
+
+# Flags: plain -O2, no FMA contraction (x86_64 and aarch64 then agree bit for bit).
+CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math"]
+
+
+def build(source: str = SOURCE, out: str = LIBRARY, force: bool = False) -> str:
+    """Compile the oracle with gcc into a shared library; return its path."""
+    if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(source):
+        return out
+    tmp = out + f".tmp{os.getpid()}"
+    subprocess.run(["gcc", *CFLAGS, "-o", tmp, source, "-lm"], check=True)
+    os.replace(tmp, out)
+    return out
+
+
+_I64 = ctypes.c_int64
+_DP = ctypes.POINTER(ctypes.c_double)
+_FP = ctypes.POINTER(ctypes.c_float)
+_I64P = ctypes.POINTER(ctypes.c_int64)
+
+
+class Oracle:
+    """Handle on one compiled copy of the oracle (the tests also load mutants)."""
+
+    def __init__(self, path: str):
+        lib = ctypes.CDLL(path)
+        lib.kb_oracle_attn.argtypes = [_DP, _DP, _DP, _DP, _I64, _I64, _I64, _I64,
+                                       ctypes.c_int, ctypes.c_double]
+        lib.kb_oracle_attn.restype = ctypes.c_int
+        lib.kb_oracle_attn_rows.argtypes = [_DP, _DP, _DP, _DP, _I64, _I64, _I64,
+                                            ctypes.c_int, ctypes.c_double, _I64P, _I64P, _I64]
+        lib.kb_oracle_attn_rows.restype = ctypes.c_int
+        lib.kb_oracle_triad.argtypes = [_FP, _FP, _FP, ctypes.c_float, _I64]
+        lib.kb_oracle_triad.restype = ctypes.c_int
+        self.lib = lib
+        self.path = path
+
+    @staticmethod
+    def _f64(x) -> np.ndarray:
+        # Exact widening: fp32 and bf16 values are all representable in fp64.
+        if hasattr(x, "detach"):  # a torch tensor on the CPU
+            x = x.detach().to("cpu").double().numpy()
+        return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+    def attn(self, q, k, v, causal: bool, scale: float) -> np.ndarray:
+        """O for q, k, v of shape [B, H, S, d]; returns float64 [B, H, S, d]."""
+        q, k, v = self._f64(q), self._f64(k), self._f64(v)
+        if q.ndim != 4 or q.shape != k.shape or q.shape != v.shape:
+            raise ValueError(f"q, k, v must share one [B,H,S,d] shape, got {q.shape} {k.shape} {v.shape}")
+        B, H, S, d = q.shape
+        o = np.empty_like(q)
+        rc = self.lib.kb_oracle_attn(q.ctypes.data_as(_DP), k.ctypes.data_as(_DP),
+                                     v.ctypes.data_as(_DP), o.ctypes.data_as(_DP),
+                                     B, H, S, d, int(bool(causal)), float(scale))
+        if rc != 0:
+            raise ValueError(f"kb_oracle_attn returned {rc}")
+        return o
+
+    def attn_rows(self, q, k, v, causal: bool, scale: float, heads, rows) -> np.ndarray:
+        """Rows (heads[t], rows[t]) of O, each exactly as the full evaluation gives it.
+
+        q, k, v are [B, H, S, d] (or [N, S, d]); heads index the flattened
+        b*H + h axis. Returns float64 [count, d].
+        """
+        q, k, v = self._f64(q), self._f64(k), self._f64(v)
+        S, d = q.shape[-2], q.shape[-1]
+        N = int(np.prod(q.shape[:-2]))
+        heads = np.ascontiguousarray(np.asarray(heads, dtype=np.int64))
+        rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        if heads.shape != rows.shape or heads.ndim != 1:
+            raise ValueError("heads and rows must be 1-D and of equal length")
+        o = np.empty((heads.size, d), dtype=np.float64)
+        rc = self.lib.kb_oracle_attn_rows(q.ctypes.data_as(_DP), k.ctypes.data_as(_DP),
+                                          v.ctypes.data_as(_DP), o.ctypes.data_as(_DP),
+                                          N, S, d, int(bool(causal)), float(scale),
+                                          heads.ctypes.data_as(_I64P), rows.ctypes.data_as(_I64P),
+                                          heads.size)
+        if rc != 0:
+            raise ValueError(f"kb_oracle_attn_rows returned {rc}")
+        return o
+
+    def triad(self, b, c, s: float) -> np.ndarray:
+        """a = b + s*c in fp32, rounded once."""
+        b = np.ascontiguousarray(np.asarray(b, dtype=np.float32))
+        c = np.ascontiguousarray(np.asarray(c, dtype=np.float32))
+        if b.shape != c.shape:
+            raise ValueError("b and c must have the same shape")
+        a = np.empty_like(b)
+        rc = self.lib.kb_oracle_triad(a.ctypes.data_as(_FP), b.ctypes.data_as(_FP),
+                                      c.ctypes.data_as(_FP), ctypes.c_float(s), b.size)
+        if rc != 0:
+            raise ValueError(f"kb_oracle_triad returned {rc}")
+        return a
+
+
+_default: Oracle | None = None
+_lock = threading.Lock()
+
+
+def get() -> Oracle:
+    """The oracle built from this directory's source (compiled on first use)."""
+    global _default
+    with _lock:
+        if _default is None:
+            _default = Oracle(build())
+        return _default
+
+
+def attn(q, k, v, causal: bool, scale: float) -> np.ndarray:
+    return get().attn(q, k, v, causal, scale)
+
+
+def attn_rows(q, k, v, causal: bool, scale: float, heads, rows) -> np.ndarray:
+    return get().attn_rows(q, k, v, causal, scale, heads, rows)
+
+
+def triad(b, c, s: float) -> np.ndarray:
+    return get().triad(b, c, s)

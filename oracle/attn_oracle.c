@@ -1,0 +1,144 @@
+/*
+ * attn_oracle.c -- TEST INFRASTRUCTURE ONLY: the plain CPU oracle.
+ *
+ * This file is the slow, obviously-correct restatement of what the attention
+ * library computes. It is used only by the tests, by the smoke check and by
+ * the benchmark's CPU-baseline leg. No product code path links, loads or calls
+ * it, and it shares no code, header or table with the CUDA library.
+ *
+ * Everything is single-threaded, in double precision, written as straight
+ * loops that follow the mathematical definition with no blocking, fusion or
+ * reordering. It is built with -ffp-contract=off so that x86_64 and aarch64
+ * hosts produce the same bits.
+ *
+ * Sources (web pages):
+ *  - "kbench -- Transformer Attention Micro-benchmark Harness",
+ *    section "Implementation details / The three GPU kernels": every kernel
+ *    computes O = softmax(Q K^T / sqrt(d)) V over a flattened (batch*heads)
+ *    axis, laid out [head, seq, dim] row-major.
+ *  - same page, section "CPU reference + cache profiling": a golden reference
+ *    that every target is diffed against.
+ *  - same page, sequence diagram "One MCU measurement": the request carries a
+ *    causal flag next to seq and dim.
+ *  - TileOPs "Hardware Microbenchmarks" README, section "HBM Bandwidth" and
+ *    "Methodology": the STREAM Triad a[i] = b[i] + s*c[i].
+ *
+ * Readings where the pages are silent:
+ *  - causal: key j is visible to query i iff j <= i;
+ *  - the scale is a parameter; it multiplies the raw dot product before the
+ *    mask and before the row maximum (the pages fix it to 1/sqrt(d));
+ *  - the row maximum is subtracted before exp; this leaves the mathematical
+ *    result unchanged and keeps exp finite for large scores;
+ *  - Triad rounds b + s*c once (a fused multiply-add), which is what a CUDA
+ *    compiler emits for that expression by default.
+ *
+ * Parity status: pinned. The attention functions are pinned by a
+ * high-precision brute-force evaluation on tiny inputs and by closed-form
+ * invariants; the Triad is pinned by exact rational arithmetic and by the
+ * STREAM constant check.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+
+#define KB_ORACLE_OK 0
+#define KB_ORACLE_BAD_ARG 1
+#define KB_ORACLE_NO_MEMORY 4
+
+/*
+ * One query row of one head.
+ *   q, k, v : [N, S, d] row-major, N = B*H (head n = b*H + h)
+ *   o_row   : d outputs for query i of head n
+ *   p       : caller-provided scratch of S doubles
+ *
+ * Steps, each as written on the kbench page (one query row at a time):
+ *   1. score s_j = scale * sum_c q[n,i,c] * k[n,j,c]   for every key j
+ *   2. causal: keys j > i are left out (probability exactly 0)
+ *   3. m = max_j s_j over the visible keys
+ *   4. p_j = exp(s_j - m), l = sum_j p_j
+ *   5. o[c] = (sum_j p_j * v[n,j,c]) / l
+ */
+static void attn_one_row(const double* q, const double* k, const double* v,
+                         double* o_row, double* p, int64_t S, int64_t d,
+                         int causal, double scale, int64_t n, int64_t i) {
+  const double* qi = q + (n * S + i) * d;
+  const double* kh = k + n * S * d;
+  const double* vh = v + n * S * d;
+  int64_t last = causal ? i : S - 1; /* last visible key */
+
+  /* 1. scores */
+  for (int64_t j = 0; j <= last; ++j) {
+    double dot = 0.0;
+    for (int64_t c = 0; c < d; ++c) dot += qi[c] * kh[j * d + c];
+    p[j] = scale * dot;
+  }
+  /* 3. row maximum over the visible keys */
+  double m = p[0];
+  for (int64_t j = 1; j <= last; ++j)
+    if (p[j] > m) m = p[j];
+  /* 4. unnormalised probabilities and their sum */
+  double l = 0.0;
+  for (int64_t j = 0; j <= last; ++j) {
+    p[j] = exp(p[j] - m);
+    l += p[j];
+  }
+  /* 5. weighted sum of the value rows, divided by the sum */
+  for (int64_t c = 0; c < d; ++c) {
+    double acc = 0.0;
+    for (int64_t j = 0; j <= last; ++j) acc += p[j] * vh[j * d + c];
+    o_row[c] = acc / l;
+  }
+}
+
+static int attn_args_ok(const void* q, const void* k, const void* v, const void* o,
+                        int64_t S, int64_t d, double scale) {
+  if (!q || !k || !v || !o) return 0;
+  if (S < 1 || d < 1) return 0;
+  if (!(scale == scale) || isinf(scale)) return 0;
+  return 1;
+}
+
+/* Full attention forward: o[n,i,:] for every head n < B*H and query i < S. */
+int kb_oracle_attn(const double* q, const double* k, const double* v, double* o,
+                   int64_t B, int64_t H, int64_t S, int64_t d, int causal,
+                   double scale) {
+  if (B < 1 || H < 1 || !attn_args_ok(q, k, v, o, S, d, scale)) return KB_ORACLE_BAD_ARG;
+  double* p = (double*)malloc((size_t)S * sizeof(double));
+  if (!p) return KB_ORACLE_NO_MEMORY;
+  int64_t N = B * H;
+  for (int64_t n = 0; n < N; ++n)
+    for (int64_t i = 0; i < S; ++i)
+      attn_one_row(q, k, v, o + (n * S + i) * d, p, S, d, causal, scale, n, i);
+  free(p);
+  return KB_ORACLE_OK;
+}
+
+/*
+ * A listed subset of (head, query) rows, for workloads too large to evaluate
+ * in full. Rows are independent, so each listed row is exactly the row the
+ * full evaluation would give. o is [count, d].
+ */
+int kb_oracle_attn_rows(const double* q, const double* k, const double* v, double* o,
+                        int64_t N, int64_t S, int64_t d, int causal, double scale,
+                        const int64_t* heads, const int64_t* rows, int64_t count) {
+  if (N < 1 || count < 0 || !attn_args_ok(q, k, v, o, S, d, scale)) return KB_ORACLE_BAD_ARG;
+  if (count > 0 && (!heads || !rows)) return KB_ORACLE_BAD_ARG;
+  for (int64_t t = 0; t < count; ++t)
+    if (heads[t] < 0 || heads[t] >= N || rows[t] < 0 || rows[t] >= S) return KB_ORACLE_BAD_ARG;
+  double* p = (double*)malloc((size_t)S * sizeof(double));
+  if (!p) return KB_ORACLE_NO_MEMORY;
+  for (int64_t t = 0; t < count; ++t)
+    attn_one_row(q, k, v, o + t * d, p, S, d, causal, scale, heads[t], rows[t]);
+  free(p);
+  return KB_ORACLE_OK;
+}
+
+/*
+ * STREAM Triad, a[i] = b[i] + s*c[i], in fp32 with one rounding of the exact
+ * value (C99 fmaf is specified to round b + s*c once).
+ */
+int kb_oracle_triad(float* a, const float* b, const float* c, float s, int64_t n) {
+  if (n < 0 || (n > 0 && (!a || !b || !c))) return KB_ORACLE_BAD_ARG;
+  for (int64_t i = 0; i < n; ++i) a[i] = fmaf(s, c[i], b[i]);
+  return KB_ORACLE_OK;
+}

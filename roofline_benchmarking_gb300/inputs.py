@@ -1,0 +1,130 @@
+"""Seeded synthetic inputs shared by the tests, the benchmark and the oracle checks.
+
+This module holds no attention arithmetic: it only draws random numbers and
+rounds them to the storage dtype. Both the CUDA path and the oracle consume the
+exact bytes it produces.
+
+Draw recipe (one reading, fixed here): a CPU ``torch.Generator`` seeded with
+the workload's seed draws Q, then K, then V, each as a full fp32 [B, H, S, d]
+tensor. "uniform" is ``rand * 2 - 1`` (U[-1, 1]); "normal(0, sigma)" is
+``randn * sigma`` (sigma is the standard deviation). bf16 workloads then round
+each fp32 draw to bf16 with round-to-nearest-even (``Tensor.to(torch.bfloat16)``).
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import torch
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    H: int
+    S: int
+    d: int
+    causal: bool
+    dtype: str          # "f32", "bf16" or "f16"
+    seed: int
+    dist: str           # "uniform" or "normal"
+    sigma_qk: float = 1.0
+    sigma_v: float = 1.0
+
+    @property
+    def N(self) -> int:
+        return self.B * self.H
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    @property
+    def flops(self) -> float:
+        """4*B*H*S^2*d, halved when causal (the benchmark's FLOP convention)."""
+        f = 4.0 * self.B * self.H * self.S * self.S * self.d
+        return f / 2 if self.causal else f
+
+    @property
+    def elem_bytes(self) -> int:
+        return 4 if self.dtype == "f32" else 2
+
+    @property
+    def io_bytes(self) -> int:
+        """Q, K, V read once and O written once."""
+        return 4 * self.B * self.H * self.S * self.d * self.elem_bytes
+
+    def with_(self, **kw) -> "Workload":
+        return dataclasses.replace(self, **kw)
+
+
+# The pages' workloads, restated. Names say what each one is.
+SINGLE_HEAD_F32 = Workload("f32_b1h1s64d32", 1, 1, 64, 32, False, "f32", 0, "uniform")
+F32_S1024 = Workload("f32_b1h8s1024d64", 1, 8, 1024, 64, False, "f32", 1, "uniform")
+F32_S1024_CAUSAL = F32_S1024.with_(name="f32_b1h8s1024d64_causal", causal=True)
+BF16_CAUSAL_S4096 = Workload("bf16_causal_b4h16s4096d128", 4, 16, 4096, 128, True, "bf16", 2, "normal")
+BF16_S2048_D64 = Workload("bf16_b16h12s2048d64", 16, 12, 2048, 64, False, "bf16", 3, "normal")
+BF16_CAUSAL_S16384 = Workload("bf16_causal_b1h32s16384d128_sharp", 1, 32, 16384, 128, True, "bf16", 4,
+                              "normal", sigma_qk=3.0, sigma_v=1.0)
+
+WORKLOADS = {w.name: w for w in (SINGLE_HEAD_F32, F32_S1024, F32_S1024_CAUSAL,
+                                 BF16_CAUSAL_S4096, BF16_S2048_D64, BF16_CAUSAL_S16384)}
+
+# STREAM Triad working set: three fp32 arrays of 2 GiB each.
+TRIAD_ARRAY_BYTES = 2 << 30
+TRIAD_N = TRIAD_ARRAY_BYTES // 4
+
+_TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
+
+
+def torch_dtype(dtype: str) -> torch.dtype:
+    return _TORCH_DTYPE[dtype]
+
+
+def make_qkv(w: Workload):
+    """Q, K, V for workload ``w`` as CPU tensors of its storage dtype, [B, H, S, d]."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(w.seed)
+    shape = (w.B, w.H, w.S, w.d)
+    out = []
+    for which in ("q", "k", "v"):
+        if w.dist == "uniform":
+            x = torch.rand(shape, generator=g, dtype=torch.float32) * 2.0 - 1.0
+        elif w.dist == "normal":
+            sigma = w.sigma_v if which == "v" else w.sigma_qk
+            x = torch.randn(shape, generator=g, dtype=torch.float32) * sigma
+        else:
+            raise ValueError(f"unknown distribution {w.dist!r}")
+        out.append(x.to(torch_dtype(w.dtype)).contiguous())
+    return tuple(out)
+
+
+def sample_rows(w: Workload, per_head: int = 64, seed: int = 12345):
+    """A fixed seeded subset of (head, row) pairs: per head, rows 0 and S-1 plus
+    ``per_head - 2`` distinct others. Returns two int64 tensors (heads, rows)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    heads, rows = [], []
+    k = min(per_head, w.S)
+    for n in range(w.N):
+        chosen = {0, w.S - 1}
+        if k > len(chosen):
+            perm = torch.randperm(w.S, generator=g).tolist()
+            for r in perm:
+                if len(chosen) >= k:
+                    break
+                chosen.add(r)
+        for r in sorted(chosen):
+            heads.append(n)
+            rows.append(r)
+    return torch.tensor(heads, dtype=torch.int64), torch.tensor(rows, dtype=torch.int64)
+
+
+def make_triad_inputs(n: int, seed: int = 5):
+    """b and c for the Triad as fp32 CPU tensors: U[-1, 1] draws from ``seed``."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    b = torch.rand(n, generator=g, dtype=torch.float32) * 2.0 - 1.0
+    c = torch.rand(n, generator=g, dtype=torch.float32) * 2.0 - 1.0
+    return b, c
