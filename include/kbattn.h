@@ -1,0 +1,199 @@
+/*
+ * kbattn.h -- C ABI of libkbattn, scaled-dot-product attention forward and
+ * the STREAM Triad bandwidth ceiling on one GB300 (sm_103a).
+ *
+ * No CUDA or PyTorch type appears here: a stream is passed as `void*` (a
+ * cudaStream_t; NULL is the legacy default stream) and every tensor as a
+ * plain device pointer.
+ *
+ * The problem definition follows the kbench page ("kbench -- Transformer
+ * Attention Micro-benchmark Harness"):
+ *  - section "Implementation details / The three GPU kernels": all kernels
+ *    compute O = softmax(Q K^T / sqrt(d)) V over a flattened (batch*heads)
+ *    axis laid out [head, seq, dim] row-major; here the scale is a parameter;
+ *  - "Architecture" diagram: one shared problem definition behind a dispatch
+ *    call run_attention(kernel, cfg) with CUDA-event timing in the launch layer;
+ *  - sequence diagram "One MCU measurement": the request carries seq, dim and
+ *    a causal flag;
+ *  - section "Implementation details", the paragraph on gpu/src/launch.cu:
+ *    events around the kernel only, no host<->device copy in the window,
+ *    configurable warm-up, per-iteration times.
+ * The Triad follows the TileOPs "Hardware Microbenchmarks" README, section
+ * "HBM Bandwidth" and "Methodology": a[i] = b[i] + s*c[i], float4 vectorised,
+ * cudaEvent timing, block sizes 128/256/512.
+ *
+ * Conventions for every call:
+ *  - Layout: q, k, v, o are contiguous [B, H, S, d] row-major (head
+ *    n = b*H + h, then query/key row, then feature), i.e. [N, S, d].
+ *  - Causal: key j is visible to query i iff j <= i.
+ *  - Ownership: the caller owns every pointer. The library never frees,
+ *    retains or synchronises caller memory or streams, except where a call
+ *    says so (the *_bench calls synchronise on their own events).
+ *  - Alignment: device pointers must be 16-byte aligned.
+ *  - Errors: every call returns a kb_status; no exception or abort crosses the
+ *    ABI. Arguments are validated before any launch, so a rejected call has
+ *    no effect on the device. KB_ERR_CUDA leaves the CUDA error code in
+ *    kb_last_cuda_error() (per thread).
+ *  - Asynchrony: launches are asynchronous on `stream`; results are valid
+ *    once the stream reaches that point. Waits inside the kernels are
+ *    bounded; a wait that runs out sets a device error word that
+ *    kb_check_device_error() reports as KB_ERR_TIMEOUT.
+ */
+#ifndef KBATTN_H
+#define KBATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+/* Exported symbols (the library is built with hidden default visibility). */
+#if defined(__GNUC__)
+#define KB_API __attribute__((visibility("default")))
+#else
+#define KB_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  KB_OK = 0,
+  KB_ERR_INVALID_ARG = 1, /* null pointer, non-positive size, bad scale, overflow */
+  KB_ERR_UNSUPPORTED = 2, /* valid request this build has no kernel for */
+  KB_ERR_CUDA = 3,        /* a CUDA runtime call failed; see kb_last_cuda_error() */
+  KB_ERR_NO_MEMORY = 4,   /* workspace too small or allocation failed */
+  KB_ERR_TIMEOUT = 5,     /* a bounded device-side wait ran out */
+  KB_ERR_NO_DEVICE = 6    /* no usable sm_103 device */
+} kb_status;
+
+typedef enum { KB_F32 = 0, KB_BF16 = 1, KB_F16 = 2 } kb_dtype;
+
+/*
+ * Variants (kbench page, "The three GPU kernels"; the tensor-core variant is
+ * this library's sm_103a kernel):
+ *  KB_NAIVE : three passes, the N*S*S fp32 score matrix goes through global
+ *             memory (score GEMM, row softmax in place, P*V GEMM). fp32 only.
+ *  KB_FUSED : one block per query row, the S-length score row kept in shared
+ *             memory. fp32 only; UNSUPPORTED when S*4 bytes exceed the shared
+ *             memory a block may use.
+ *  KB_FLASH : tiled, online softmax (running max and denominator), the score
+ *             matrix never materialised; CUDA cores. fp32 only.
+ *  KB_TC    : tiled, online softmax on the 5th-generation tensor cores
+ *             (tcgen05 MMAs into tensor memory, TMA-staged tiles). bf16/f16.
+ *  KB_AUTO  : KB_TC for bf16/f16, KB_FLASH for fp32.
+ */
+typedef enum { KB_AUTO = 0, KB_NAIVE = 1, KB_FUSED = 2, KB_FLASH = 3, KB_TC = 4 } kb_variant;
+
+/* Device properties used by the roofline peak formulas. */
+typedef struct {
+  int device;               /* CUDA ordinal */
+  int cc_major, cc_minor;   /* compute capability */
+  int sm_count;             /* streaming multiprocessors */
+  int sm_clock_khz;         /* cudaDevAttrClockRate */
+  int mem_clock_khz;        /* cudaDevAttrMemoryClockRate */
+  int mem_bus_width_bits;   /* cudaDevAttrGlobalMemoryBusWidth */
+  int l2_bytes;             /* L2 cache size */
+  int smem_per_block_optin; /* opt-in shared memory per block */
+  int smem_per_sm;          /* shared memory per SM */
+  size_t total_mem_bytes;   /* device memory */
+  char name[256];           /* device name, NUL-terminated */
+} kb_device_info_t;
+
+/*
+ * kb_attn_fwd -- O = softmax(Q K^T * scale [+ causal mask]) V.
+ *   q, k, v : const device pointers, [B, H, S, d] of `dtype`
+ *   o       : device pointer, [B, H, S, d] of `dtype`, written in full
+ *             (bf16/f16 outputs are rounded to nearest even from fp32)
+ *   B, H, S : >= 1; B*H*S*d must fit in int64 and B*H in int32
+ *   d       : head dimension, one of 32, 64, 128 (others -> UNSUPPORTED)
+ *   causal  : 0 or 1
+ *   scale   : finite and > 0 (callers normally pass 1/sqrt(d))
+ *   dtype   : kb_dtype of q, k, v and o
+ *   variant : kb_variant; see the support matrix above
+ *   stream  : cudaStream_t or NULL
+ * KB_TC supports d = 64 and 128 (d = 32 -> UNSUPPORTED).
+ * KB_NAIVE needs N*S*S*4 bytes of workspace: this call takes it from a
+ * per-device cache that it grows with cudaMalloc, synchronising the device
+ * first when it replaces a smaller buffer (so it may allocate and block);
+ * calls on different streams share that cache and must not overlap.
+ * kb_attn_fwd_ws lets the caller supply the workspace instead.
+ */
+KB_API int kb_attn_fwd(const void* q, const void* k, const void* v, void* o,
+                int B, int H, int S, int d, int causal, float scale,
+                int dtype, int variant, void* stream);
+
+/* Workspace bytes kb_attn_fwd_ws needs (0 for every variant but KB_NAIVE,
+ * and 0 for an invalid request). */
+KB_API size_t kb_attn_workspace_bytes(int B, int H, int S, int d, int dtype, int variant);
+
+/* kb_attn_fwd with a caller-owned device workspace of ws_bytes bytes (16-byte
+ * aligned); KB_ERR_NO_MEMORY if ws_bytes < kb_attn_workspace_bytes(...).
+ * The library allocates nothing in this call. */
+KB_API int kb_attn_fwd_ws(const void* q, const void* k, const void* v, void* o,
+                   int B, int H, int S, int d, int causal, float scale,
+                   int dtype, int variant, void* stream,
+                   void* workspace, size_t ws_bytes);
+
+/*
+ * kb_attn_bench -- `warmup` untimed calls, then `iters` calls each bracketed
+ * by CUDA events on `stream`; ms_per_iter[t] (host array of `iters` floats)
+ * receives the t-th call's device time. Synchronises on its own events only.
+ * Uses kb_attn_fwd_ws when workspace != NULL, else kb_attn_fwd.
+ */
+KB_API int kb_attn_bench(const void* q, const void* k, const void* v, void* o,
+                  int B, int H, int S, int d, int causal, float scale,
+                  int dtype, int variant, void* stream,
+                  void* workspace, size_t ws_bytes,
+                  int warmup, int iters, float* ms_per_iter);
+
+/*
+ * kb_triad -- STREAM Triad a[i] = b[i] + s*c[i] for i < n, fp32, computed as
+ * one fused multiply-add (a single rounding of the exact value).
+ *   a       : device pointer, n floats, written
+ *   b, c    : const device pointers, n floats
+ *   n       : element count (0 is a no-op)
+ *   block   : threads per block, one of 128, 256, 512 (0 picks 256)
+ * Pointers must be 16-byte aligned (float4 accesses); any n is accepted, the
+ * tail that is not a multiple of 4 is handled with scalar accesses.
+ */
+KB_API int kb_triad(float* a, const float* b, const float* c, float s, size_t n,
+             int block, void* stream);
+
+/* kb_triad timed like kb_attn_bench. */
+KB_API int kb_triad_bench(float* a, const float* b, const float* c, float s, size_t n,
+                   int block, void* stream, int warmup, int iters, float* ms_per_iter);
+
+/* Device properties of `device` (an ordinal), no launch. */
+KB_API int kb_device_info(int device, kb_device_info_t* out);
+
+/*
+ * kb_check_device_error -- synchronise `stream`, then read and clear the
+ * device error word of the current device. KB_ERR_TIMEOUT if a bounded wait
+ * in any kernel of this library ran out since the last check, else KB_OK
+ * (or KB_ERR_CUDA if synchronising failed).
+ */
+KB_API int kb_check_device_error(void* stream);
+
+/*
+ * kb_selftest_timeout -- launch one block whose thread waits, with the same
+ * bounded wait the tensor-core kernel uses, on an mbarrier that nothing ever
+ * completes; the wait gives up after `limit_ns` nanoseconds (clamped to
+ * [1e3, 2e9]) and records the timeout in the device error word. Exists so
+ * that the timeout path can be tested without hanging a GPU. Asynchronous.
+ */
+KB_API int kb_selftest_timeout(unsigned long long limit_ns, void* stream);
+
+/* Human-readable name of a kb_status (static storage, never NULL). */
+KB_API const char* kb_status_string(int status);
+
+/* cudaError_t of the last call on this thread that returned KB_ERR_CUDA. */
+KB_API int kb_last_cuda_error(void);
+
+/* Library ABI version: 100 * major + minor. */
+KB_API int kb_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KBATTN_H */

@@ -1,0 +1,327 @@
+// api.cu -- the C ABI of libkbattn: argument validation, variant selection,
+// launches on the caller's stream, CUDA-event timing and device properties.
+//
+// kbench page ("kbench -- Transformer Attention Micro-benchmark Harness"):
+// "Architecture" (one problem definition behind run_attention(kernel, cfg)),
+// "Implementation details" (events around the kernel only, configurable
+// warm-up, per-iteration device times). The Triad timing follows the TileOPs
+// "Hardware Microbenchmarks" README, section "Methodology".
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstring>
+#include <limits>
+#include <mutex>
+#include <vector>
+
+#include "internal.h"
+
+namespace kb {
+
+namespace {
+thread_local int t_last_cuda_error = 0;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Validation shared by every attention entry point; no CUDA call is made, so a
+// rejected request has no effect on any device.
+int validate(const void* q, const void* k, const void* v, const void* o, int B, int H, int S, int d,
+             int causal, float scale, int dtype, int variant, int* resolved) {
+  if (!q || !k || !v || !o) return KB_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return KB_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || S < 1 || d < 1) return KB_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return KB_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.0f)) return KB_ERR_INVALID_ARG;
+  if (dtype != KB_F32 && dtype != KB_BF16 && dtype != KB_F16) return KB_ERR_INVALID_ARG;
+  if (variant < KB_AUTO || variant > KB_TC) return KB_ERR_INVALID_ARG;
+  // B*H*S*d elements, times 4 bytes, must fit in int64; B*H in int32.
+  const int64_t N = (int64_t)B * H;
+  if (N > std::numeric_limits<int32_t>::max()) return KB_ERR_INVALID_ARG;
+  const int64_t lim = std::numeric_limits<int64_t>::max() / 4;
+  if (N > lim / S || N * S > lim / d) return KB_ERR_INVALID_ARG;
+  if (d != 32 && d != 64 && d != 128) return KB_ERR_UNSUPPORTED;
+  int var = variant;
+  if (var == KB_AUTO) var = dtype == KB_F32 ? KB_FLASH : KB_TC;
+  if (dtype == KB_F32 && var == KB_TC) return KB_ERR_UNSUPPORTED;
+  if (dtype != KB_F32 && var != KB_TC) return KB_ERR_UNSUPPORTED;
+  // one block per query row (fused) or per 64-row tile (flash, naive)
+  const int64_t grid_limit = std::numeric_limits<int32_t>::max();
+  if (var == KB_FUSED && N * S > grid_limit) return KB_ERR_UNSUPPORTED;
+  if ((var == KB_FLASH || var == KB_NAIVE) && N * ((S + 63) / 64) > grid_limit) return KB_ERR_UNSUPPORTED;
+  if (var == KB_NAIVE && N > 65535) return KB_ERR_UNSUPPORTED;  // grid.z of the score pass
+  *resolved = var;
+  return KB_OK;
+}
+
+int cuda_fail(cudaError_t e) {
+  set_last_cuda_error(e);
+  return KB_ERR_CUDA;
+}
+
+// The current device must be an sm_103 part (this library carries sm_103a code only).
+struct DeviceGate {
+  std::mutex mu;
+  std::vector<int> ok;  // per ordinal: 0 unknown, 1 usable, -1 not usable
+};
+DeviceGate g_gate;
+
+int check_device() {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return KB_ERR_NO_DEVICE;
+  }
+  std::lock_guard<std::mutex> lk(g_gate.mu);
+  if ((int)g_gate.ok.size() <= dev) g_gate.ok.resize(dev + 1, 0);
+  if (g_gate.ok[dev] == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return KB_ERR_NO_DEVICE;
+    }
+    g_gate.ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+  }
+  return g_gate.ok[dev] == 1 ? KB_OK : KB_ERR_NO_DEVICE;
+}
+
+// Per-device workspace of the naive variant, grown on demand.
+struct Workspace {
+  std::mutex mu;
+  std::vector<void*> ptr;
+  std::vector<size_t> bytes;
+};
+Workspace g_ws;
+
+int cached_workspace(size_t need, void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  std::lock_guard<std::mutex> lk(g_ws.mu);
+  if ((int)g_ws.ptr.size() <= dev) {
+    g_ws.ptr.resize(dev + 1, nullptr);
+    g_ws.bytes.resize(dev + 1, 0);
+  }
+  if (g_ws.bytes[dev] < need) {
+    if (g_ws.ptr[dev]) {
+      // in-flight work on any stream may still read the old buffer
+      if ((e = cudaDeviceSynchronize()) != cudaSuccess) return cuda_fail(e);
+      cudaFree(g_ws.ptr[dev]);
+      g_ws.ptr[dev] = nullptr;
+      g_ws.bytes[dev] = 0;
+    }
+    void* p = nullptr;
+    if ((e = cudaMalloc(&p, need)) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return KB_ERR_NO_MEMORY;
+    }
+    g_ws.ptr[dev] = p;
+    g_ws.bytes[dev] = need;
+  }
+  *out = g_ws.ptr[dev];
+  return KB_OK;
+}
+
+int run_attention(const void* q, const void* k, const void* v, void* o, int B, int H, int S, int d, int causal,
+                  float scale, int dtype, int variant, void* stream, void* workspace, size_t ws_bytes,
+                  bool caller_ws) {
+  int var = 0;
+  int st = validate(q, k, v, o, B, H, S, d, causal, scale, dtype, variant, &var);
+  if (st != KB_OK) return st;
+  AttnProblem p{q, k, v, o, (int64_t)B * H, S, d, causal, scale, dtype};
+  float* scores = nullptr;
+  if (var == KB_NAIVE) {
+    const size_t need = naive_workspace_bytes(p.N, S);
+    if (caller_ws) {
+      if (!workspace || ws_bytes < need) return KB_ERR_NO_MEMORY;
+      if (!aligned16(workspace)) return KB_ERR_INVALID_ARG;
+      if ((st = check_device()) != KB_OK) return st;
+      scores = static_cast<float*>(workspace);
+    } else {
+      if ((st = check_device()) != KB_OK) return st;
+      void* w = nullptr;
+      if ((st = cached_workspace(need, &w)) != KB_OK) return st;
+      scores = static_cast<float*>(w);
+    }
+  } else if ((st = check_device()) != KB_OK) {
+    return st;
+  }
+  if (var == KB_FUSED && (st = fused_f32_check(S, d)) != KB_OK) return st;
+  if (var == KB_TC && (st = tc_check(S, d, dtype)) != KB_OK) return st;
+
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  switch (var) {
+    case KB_NAIVE: e = launch_naive_f32(p, scores, cs); break;
+    case KB_FUSED: e = launch_fused_f32(p, cs); break;
+    case KB_FLASH: e = launch_flash_f32(p, cs); break;
+    case KB_TC: e = launch_tc(p, cs); break;
+    default: return KB_ERR_UNSUPPORTED;
+  }
+  return e == cudaSuccess ? KB_OK : cuda_fail(e);
+}
+
+// Records start[t] / stop[t] around each timed call; returns per-call times.
+template <typename Call>
+int time_calls(Call call, cudaStream_t cs, int warmup, int iters, float* ms) {
+  for (int t = 0; t < warmup; ++t) {
+    int st = call();
+    if (st != KB_OK) return st;
+  }
+  std::vector<cudaEvent_t> ev(2 * (size_t)iters, nullptr);
+  cudaError_t e = cudaSuccess;
+  int st = KB_OK;
+  for (auto& x : ev) {
+    if ((e = cudaEventCreate(&x)) != cudaSuccess) break;
+  }
+  if (e == cudaSuccess) {
+    for (int t = 0; t < iters && st == KB_OK && e == cudaSuccess; ++t) {
+      e = cudaEventRecord(ev[2 * t], cs);
+      if (e == cudaSuccess) st = call();
+      if (e == cudaSuccess && st == KB_OK) e = cudaEventRecord(ev[2 * t + 1], cs);
+    }
+  }
+  if (e == cudaSuccess && st == KB_OK && iters > 0) e = cudaEventSynchronize(ev[2 * iters - 1]);
+  for (int t = 0; t < iters && e == cudaSuccess && st == KB_OK; ++t)
+    e = cudaEventElapsedTime(&ms[t], ev[2 * t], ev[2 * t + 1]);
+  for (auto& x : ev)
+    if (x) cudaEventDestroy(x);
+  if (st != KB_OK) return st;
+  return e == cudaSuccess ? KB_OK : cuda_fail(e);
+}
+
+}  // namespace
+
+void set_last_cuda_error(cudaError_t e) { t_last_cuda_error = (int)e; }
+
+}  // namespace kb
+
+using namespace kb;
+
+extern "C" {
+
+int kb_version(void) { return 100; }
+
+int kb_attn_fwd(const void* q, const void* k, const void* v, void* o, int B, int H, int S, int d, int causal,
+                float scale, int dtype, int variant, void* stream) {
+  return run_attention(q, k, v, o, B, H, S, d, causal, scale, dtype, variant, stream, nullptr, 0, false);
+}
+
+size_t kb_attn_workspace_bytes(int B, int H, int S, int d, int dtype, int variant) {
+  int var = 0;
+  const void* dummy = reinterpret_cast<const void*>(static_cast<uintptr_t>(256));
+  if (validate(dummy, dummy, dummy, dummy, B, H, S, d, 0, 1.0f, dtype, variant, &var) != KB_OK) return 0;
+  return var == KB_NAIVE ? naive_workspace_bytes((int64_t)B * H, S) : 0;
+}
+
+int kb_attn_fwd_ws(const void* q, const void* k, const void* v, void* o, int B, int H, int S, int d, int causal,
+                   float scale, int dtype, int variant, void* stream, void* workspace, size_t ws_bytes) {
+  return run_attention(q, k, v, o, B, H, S, d, causal, scale, dtype, variant, stream, workspace, ws_bytes, true);
+}
+
+int kb_attn_bench(const void* q, const void* k, const void* v, void* o, int B, int H, int S, int d, int causal,
+                  float scale, int dtype, int variant, void* stream, void* workspace, size_t ws_bytes, int warmup,
+                  int iters, float* ms_per_iter) {
+  if (warmup < 0 || iters < 1 || !ms_per_iter) return KB_ERR_INVALID_ARG;
+  int var = 0;
+  int st = validate(q, k, v, o, B, H, S, d, causal, scale, dtype, variant, &var);
+  if (st != KB_OK) return st;
+  const bool use_ws = workspace != nullptr;
+  auto call = [&]() {
+    return run_attention(q, k, v, o, B, H, S, d, causal, scale, dtype, variant, stream, workspace, ws_bytes,
+                         use_ws);
+  };
+  return time_calls(call, static_cast<cudaStream_t>(stream), warmup, iters, ms_per_iter);
+}
+
+int kb_triad(float* a, const float* b, const float* c, float s, size_t n, int block, void* stream) {
+  if (n == 0) return KB_OK;
+  if (!a || !b || !c) return KB_ERR_INVALID_ARG;
+  if (!aligned16(a) || !aligned16(b) || !aligned16(c)) return KB_ERR_INVALID_ARG;
+  if (block == 0) block = 256;
+  if (block != 128 && block != 256 && block != 512) return KB_ERR_INVALID_ARG;
+  int st = check_device();
+  if (st != KB_OK) return st;
+  cudaError_t e = launch_triad(a, b, c, s, n, block, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KB_OK : cuda_fail(e);
+}
+
+int kb_triad_bench(float* a, const float* b, const float* c, float s, size_t n, int block, void* stream, int warmup,
+                   int iters, float* ms_per_iter) {
+  if (warmup < 0 || iters < 1 || !ms_per_iter) return KB_ERR_INVALID_ARG;
+  auto call = [&]() { return kb_triad(a, b, c, s, n, block, stream); };
+  return time_calls(call, static_cast<cudaStream_t>(stream), warmup, iters, ms_per_iter);
+}
+
+int kb_device_info(int device, kb_device_info_t* out) {
+  if (!out || device < 0) return KB_ERR_INVALID_ARG;
+  int count = 0;
+  if (cudaGetDeviceCount(&count) != cudaSuccess || device >= count) {
+    (void)cudaGetLastError();
+    return KB_ERR_NO_DEVICE;
+  }
+  std::memset(out, 0, sizeof(*out));
+  out->device = device;
+  struct {
+    cudaDeviceAttr a;
+    int* dst;
+  } attrs[] = {
+      {cudaDevAttrComputeCapabilityMajor, &out->cc_major},
+      {cudaDevAttrComputeCapabilityMinor, &out->cc_minor},
+      {cudaDevAttrMultiProcessorCount, &out->sm_count},
+      {cudaDevAttrClockRate, &out->sm_clock_khz},
+      {cudaDevAttrMemoryClockRate, &out->mem_clock_khz},
+      {cudaDevAttrGlobalMemoryBusWidth, &out->mem_bus_width_bits},
+      {cudaDevAttrL2CacheSize, &out->l2_bytes},
+      {cudaDevAttrMaxSharedMemoryPerBlockOptin, &out->smem_per_block_optin},
+      {cudaDevAttrMaxSharedMemoryPerMultiprocessor, &out->smem_per_sm},
+  };
+  for (auto& x : attrs) {
+    cudaError_t e = cudaDeviceGetAttribute(x.dst, x.a, device);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  cudaDeviceProp prop;
+  cudaError_t e = cudaGetDeviceProperties(&prop, device);
+  if (e != cudaSuccess) return cuda_fail(e);
+  out->total_mem_bytes = prop.totalGlobalMem;
+  std::strncpy(out->name, prop.name, sizeof(out->name) - 1);
+  return KB_OK;
+}
+
+int kb_check_device_error(void* stream) {
+  unsigned int word = 0;
+  int st = check_device();
+  if (st != KB_OK) return st;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = read_and_clear_error_word(&word, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return word ? KB_ERR_TIMEOUT : KB_OK;
+}
+
+int kb_selftest_timeout(unsigned long long limit_ns, void* stream) {
+  int st = check_device();
+  if (st != KB_OK) return st;
+  if (limit_ns < 1000ull) limit_ns = 1000ull;
+  if (limit_ns > 2000000000ull) limit_ns = 2000000000ull;
+  cudaError_t e = launch_selftest_timeout(limit_ns, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KB_OK : cuda_fail(e);
+}
+
+const char* kb_status_string(int status) {
+  switch (status) {
+    case KB_OK: return "KB_OK";
+    case KB_ERR_INVALID_ARG: return "KB_ERR_INVALID_ARG";
+    case KB_ERR_UNSUPPORTED: return "KB_ERR_UNSUPPORTED";
+    case KB_ERR_CUDA: return "KB_ERR_CUDA";
+    case KB_ERR_NO_MEMORY: return "KB_ERR_NO_MEMORY";
+    case KB_ERR_TIMEOUT: return "KB_ERR_TIMEOUT";
+    case KB_ERR_NO_DEVICE: return "KB_ERR_NO_DEVICE";
+  }
+  return "KB_UNKNOWN_STATUS";
+}
+
+int kb_last_cuda_error(void) { return t_last_cuda_error; }
+
+}  // extern "C"

@@ -1,0 +1,473 @@
+// attn_fp32.cu -- the three fp32 CUDA-core attention variants.
+//
+// kbench page ("kbench -- Transformer Attention Micro-benchmark Harness"),
+// section "Implementation details / The three GPU kernels":
+//  * naive: three global passes -- a GEMM that writes the S x S score matrix
+//    to DRAM, a row softmax over it, a second GEMM for P*V;
+//  * fused: one block per query row, the S-length score vector in shared
+//    memory, one pass, shared memory O(S);
+//  * flash: key/value tiles streamed through shared memory with an online
+//    softmax (running max m and denominator l), shared memory O(Bc*d).
+// All three compute O = softmax(Q K^T * scale [+ causal mask]) V over
+// [N, S, d] row-major fp32 with fp32 arithmetic. Scores are carried in base 2
+// (scale*log2(e) folded into one multiply) so that exp becomes exp2.
+#include <cuda_runtime.h>
+
+#include "device_common.cuh"
+#include "internal.h"
+
+namespace kb {
+namespace {
+
+constexpr int kThreads = 256;  // 16 x 16 thread grid for the 64 x 64 tiles
+constexpr int kBR = 64;        // query rows per tile
+constexpr int kBC = 64;        // keys per tile
+constexpr int kLD = kBR + 4;   // padded leading dimension of transposed tiles
+
+template <int D>
+struct Cols {
+  // Output columns a thread owns: groups of W consecutive columns, G groups.
+  static constexpr int W = D >= 64 ? 4 : 2;
+  static constexpr int G = D / (16 * W);
+  static_assert(G * 16 * W == D, "D must be 32, 64 or 128");
+};
+
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+
+// Loads rows [r0, r0+64) x D of a [S, D] matrix into a transposed shared tile
+// dst[k * kLD + r] (feature-major), multiplied by `mul`; rows >= S read as 0.
+// Consecutive threads take consecutive rows so that the shared stores do not
+// conflict; the strided global reads are served from L1 across the k loop.
+template <int D>
+__device__ __forceinline__ void load_transposed(float* dst, const float* src, int r0, int S, float mul) {
+  for (int f = threadIdx.x; f < kBR * (D / 4); f += kThreads) {
+    const int r = f % kBR, k4 = f / kBR;
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (r0 + r < S) x = ld4(src + (int64_t)(r0 + r) * D + 4 * k4);
+    dst[(4 * k4 + 0) * kLD + r] = x.x * mul;
+    dst[(4 * k4 + 1) * kLD + r] = x.y * mul;
+    dst[(4 * k4 + 2) * kLD + r] = x.z * mul;
+    dst[(4 * k4 + 3) * kLD + r] = x.w * mul;
+  }
+}
+
+// Loads rows [r0, r0+64) x D of a [S, D] matrix into dst[r * D + k] (row-major).
+template <int D>
+__device__ __forceinline__ void load_rows(float* dst, const float* src, int r0, int S) {
+  for (int f = threadIdx.x; f < kBC * (D / 4); f += kThreads) {
+    const int r = f / (D / 4), k4 = f % (D / 4);
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (r0 + r < S) x = ld4(src + (int64_t)(r0 + r) * D + 4 * k4);
+    *reinterpret_cast<float4*>(dst + r * D + 4 * k4) = x;
+  }
+}
+
+// acc[a][*] += sum_c P[c][row a] * V[c][col]: P transposed in shared memory
+// (Ps[c * kLD + r]), V row-major (Vs[c * D + col]); `kmax` keys.
+template <int D>
+__device__ __forceinline__ void pv_accumulate(float (&acc)[4][D / 16], const float* Ps, const float* Vs,
+                                              int ty, int tx, int kmax) {
+  using C = Cols<D>;
+  for (int c = 0; c < kmax; ++c) {
+    const float4 pa = ld4(Ps + c * kLD + ty * 4);
+    const float pr[4] = {pa.x, pa.y, pa.z, pa.w};
+#pragma unroll
+    for (int g = 0; g < C::G; ++g) {
+      float vv[C::W];
+      const float* vp = Vs + c * D + g * 16 * C::W + tx * C::W;
+      if constexpr (C::W == 4) {
+        const float4 t = ld4(vp);
+        vv[0] = t.x; vv[1] = t.y; vv[2] = t.z; vv[3] = t.w;
+      } else {
+        const float2 t = *reinterpret_cast<const float2*>(vp);
+        vv[0] = t.x; vv[1] = t.y;
+      }
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int e = 0; e < C::W; ++e) acc[a][g * C::W + e] = fmaf(pr[a], vv[e], acc[a][g * C::W + e]);
+    }
+  }
+}
+
+// s[a][b] = sum_k Qs[k][ty*4+a] * Ks[k][tx*4+b] for the 64 x 64 tile.
+template <int D>
+__device__ __forceinline__ void qk_tile(float (&s)[4][4], const float* Qs, const float* Ks, int ty, int tx) {
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int b = 0; b < 4; ++b) s[a][b] = 0.f;
+#pragma unroll 8
+  for (int k = 0; k < D; ++k) {
+    const float4 qa = ld4(Qs + k * kLD + ty * 4);
+    const float4 kb = ld4(Ks + k * kLD + tx * 4);
+    const float qv[4] = {qa.x, qa.y, qa.z, qa.w};
+    const float kv[4] = {kb.x, kb.y, kb.z, kb.w};
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) s[a][b] = fmaf(qv[a], kv[b], s[a][b]);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// flash: one block per (head, 64-row query tile); grid.x = tiles * N with the
+// heaviest causal tiles scheduled first.
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(kThreads) flash_f32_kernel(const float* __restrict__ Q,
+                                                             const float* __restrict__ K,
+                                                             const float* __restrict__ V,
+                                                             float* __restrict__ O, int64_t N, int S,
+                                                             int causal, float scale_log2) {
+  using C = Cols<D>;
+  extern __shared__ float4 smem4[];
+  float* Qs = reinterpret_cast<float*>(smem4);  // [D][kLD]
+  float* Ks = Qs + D * kLD;                      // [D][kLD]
+  float* Vs = Ks + D * kLD;                      // [kBC][D]
+  float* Ps = Vs + kBC * D;                      // [kBC][kLD]
+
+  const int ntiles = (S + kBR - 1) / kBR;
+  const int64_t n = blockIdx.x % N;
+  const int qt = ntiles - 1 - (int)(blockIdx.x / N);
+  const int q0 = qt * kBR;
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  const float* Qh = Q + n * S * D;
+  const float* Kh = K + n * S * D;
+  const float* Vh = V + n * S * D;
+
+  load_transposed<D>(Qs, Qh, q0, S, scale_log2);
+
+  float m[4], l[4], acc[4][D / 16];
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    m[a] = -INFINITY;
+    l[a] = 0.f;
+#pragma unroll
+    for (int c = 0; c < D / 16; ++c) acc[a][c] = 0.f;
+  }
+
+  const int kt_last = causal ? qt : ntiles - 1;
+  for (int kt = 0; kt <= kt_last; ++kt) {
+    const int k0 = kt * kBC;
+    __syncthreads();  // previous tile's Ks, Vs, Ps are no longer read
+    load_transposed<D>(Ks, Kh, k0, S, 1.0f);
+    load_rows<D>(Vs, Vh, k0, S);
+    __syncthreads();
+
+    float s[4][4];
+    qk_tile<D>(s, Qs, Ks, ty, tx);
+
+    // mask, then the online-softmax update for each of the thread's 4 rows
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      const int row = q0 + ty * 4 + a;
+      float tmax = -INFINITY;
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const int key = k0 + tx * 4 + b;
+        if (key >= S || (causal && key > row)) s[a][b] = -INFINITY;
+        tmax = fmaxf(tmax, s[a][b]);
+      }
+      tmax = group_max<16>(tmax);
+      const float m_new = fmaxf(m[a], tmax);
+      const float m_use = m_new == -INFINITY ? 0.f : m_new;
+      const float alpha = exp2f(m[a] - m_use);
+      float rs = 0.f;
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        s[a][b] = exp2f(s[a][b] - m_use);
+        rs += s[a][b];
+      }
+      rs = group_sum<16>(rs);
+      l[a] = l[a] * alpha + rs;
+      m[a] = m_new;
+#pragma unroll
+      for (int c = 0; c < D / 16; ++c) acc[a][c] *= alpha;
+    }
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+      *reinterpret_cast<float4*>(Ps + (tx * 4 + b) * kLD + ty * 4) = make_float4(s[0][b], s[1][b], s[2][b], s[3][b]);
+    __syncthreads();
+    pv_accumulate<D>(acc, Ps, Vs, ty, tx, kBC);
+  }
+
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    const int row = q0 + ty * 4 + a;
+    if (row >= S) continue;
+    const float inv = 1.0f / l[a];
+    float* orow = O + (n * S + row) * D;
+#pragma unroll
+    for (int g = 0; g < C::G; ++g)
+#pragma unroll
+      for (int e = 0; e < C::W; ++e) orow[g * 16 * C::W + tx * C::W + e] = acc[a][g * C::W + e] * inv;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// naive pass 1: scores[n][i][j] = scale * q_i . k_j as a tiled GEMM; causal
+// entries j > i are written as -inf in the diagonal tile and tiles wholly
+// above the diagonal are skipped (pass 2 and 3 never read them).
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(kThreads) naive_scores_kernel(const float* __restrict__ Q,
+                                                                const float* __restrict__ K,
+                                                                float* __restrict__ Sc, int64_t N, int S,
+                                                                int causal, float scale) {
+  extern __shared__ float4 smem4[];
+  float* Qs = reinterpret_cast<float*>(smem4);  // [D][kLD]
+  float* Ks = Qs + D * kLD;                      // [D][kLD]
+  const int ntiles = (S + kBR - 1) / kBR;
+  const int kt = blockIdx.x, qt = blockIdx.y;
+  const int64_t n = blockIdx.z;
+  if (causal && kt > qt) return;
+  const int q0 = qt * kBR, k0 = kt * kBC;
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  (void)ntiles;
+  load_transposed<D>(Qs, Q + n * S * D, q0, S, scale);
+  load_transposed<D>(Ks, K + n * S * D, k0, S, 1.0f);
+  __syncthreads();
+  float s[4][4];
+  qk_tile<D>(s, Qs, Ks, ty, tx);
+  float* Sh = Sc + n * (int64_t)S * S;
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    const int row = q0 + ty * 4 + a;
+    if (row >= S) continue;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const int key = k0 + tx * 4 + b;
+      if (key >= S) continue;
+      Sh[(int64_t)row * S + key] = (causal && key > row) ? -INFINITY : s[a][b];
+    }
+  }
+}
+
+// naive pass 2: in-place row softmax, one warp per row over its visible keys.
+__global__ void __launch_bounds__(kThreads) naive_softmax_kernel(float* __restrict__ Sc, int64_t rows, int S,
+                                                                 int causal) {
+  const int64_t r = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+  if (r >= rows) return;
+  const int lane = threadIdx.x & 31;
+  const int i = (int)(r % S);
+  const int len = causal ? i + 1 : S;
+  float* row = Sc + r * S;
+  // one read pass: lane-local running max and sum, then combined across lanes
+  float m = -INFINITY, l = 0.f;
+  for (int j = lane; j < len; j += 32) {
+    const float x = row[j] * kLog2e;
+    const float m_new = fmaxf(m, x);
+    l = l * exp2f(m - m_new) + exp2f(x - m_new);
+    m = m_new;
+  }
+  const float mw = warp_max(m);
+  l = warp_sum(m == -INFINITY ? 0.f : l * exp2f(m - mw));
+  const float inv = 1.0f / l;
+  for (int j = lane; j < len; j += 32) row[j] = exp2f(row[j] * kLog2e - mw) * inv;
+}
+
+// naive pass 3: O = P V as a tiled GEMM over the visible key tiles.
+template <int D>
+__global__ void __launch_bounds__(kThreads) naive_pv_kernel(const float* __restrict__ Sc,
+                                                            const float* __restrict__ V, float* __restrict__ O,
+                                                            int64_t N, int S, int causal) {
+  using C = Cols<D>;
+  extern __shared__ float4 smem4[];
+  float* Ps = reinterpret_cast<float*>(smem4);  // [kBC][kLD] (key-major)
+  float* Vs = Ps + kBC * kLD;                    // [kBC][D]
+  const int ntiles = (S + kBR - 1) / kBR;
+  const int64_t n = blockIdx.x % N;
+  const int qt = ntiles - 1 - (int)(blockIdx.x / N);
+  const int q0 = qt * kBR;
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  const float* Sh = Sc + n * (int64_t)S * S;
+  float acc[4][D / 16];
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int c = 0; c < D / 16; ++c) acc[a][c] = 0.f;
+
+  const int kt_last = causal ? qt : ntiles - 1;
+  for (int kt = 0; kt <= kt_last; ++kt) {
+    const int k0 = kt * kBC;
+    __syncthreads();
+    // P tile, transposed to Ps[key][row]; masked and out-of-range entries are 0
+    for (int f = tid; f < kBR * kBC; f += kThreads) {
+      const int key = f % kBC, r = f / kBC;
+      const int row = q0 + r, col = k0 + key;
+      float p = 0.f;
+      if (row < S && col < S && !(causal && col > row)) p = Sh[(int64_t)row * S + col];
+      Ps[key * kLD + r] = p;
+    }
+    load_rows<D>(Vs, V + n * S * D, k0, S);
+    __syncthreads();
+    pv_accumulate<D>(acc, Ps, Vs, ty, tx, kBC);
+  }
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    const int row = q0 + ty * 4 + a;
+    if (row >= S) continue;
+    float* orow = O + (n * S + row) * D;
+#pragma unroll
+    for (int g = 0; g < C::G; ++g)
+#pragma unroll
+      for (int e = 0; e < C::W; ++e) orow[g * 16 * C::W + tx * C::W + e] = acc[a][g * C::W + e];
+  }
+}
+
+// ---------------------------------------------------------------------------
+// fused: one block per (head, query row); the score row lives in shared memory.
+// ---------------------------------------------------------------------------
+constexpr int kFusedThreads = 128;
+
+template <int D>
+__global__ void __launch_bounds__(kFusedThreads) fused_row_f32_kernel(const float* __restrict__ Q,
+                                                                      const float* __restrict__ K,
+                                                                      const float* __restrict__ V,
+                                                                      float* __restrict__ O, int S, int causal,
+                                                                      float scale_log2) {
+  extern __shared__ float4 smem4[];
+  float* qs = reinterpret_cast<float*>(smem4);  // [D]
+  float* red = qs + D;                           // [32]
+  float* part = red + 32;                        // [kFusedThreads]
+  float* sc = part + kFusedThreads;              // [S]
+  const int64_t b = blockIdx.x;
+  const int64_t n = b / S;
+  const int i = (int)(b % S);
+  const int tid = threadIdx.x;
+  const int last = causal ? i : S - 1;
+  const float* Kh = K + n * S * D;
+  const float* Vh = V + n * S * D;
+
+  for (int c = tid; c < D; c += kFusedThreads) qs[c] = Q[(n * S + i) * D + c] * scale_log2;
+  __syncthreads();
+
+  float tmax = -INFINITY;
+  for (int j = tid; j <= last; j += kFusedThreads) {
+    const float* kr = Kh + (int64_t)j * D;
+    float dot = 0.f;
+#pragma unroll
+    for (int c = 0; c < D; c += 4) {
+      const float4 kv = ld4(kr + c);
+      dot = fmaf(qs[c], kv.x, dot);
+      dot = fmaf(qs[c + 1], kv.y, dot);
+      dot = fmaf(qs[c + 2], kv.z, dot);
+      dot = fmaf(qs[c + 3], kv.w, dot);
+    }
+    sc[j] = dot;
+    tmax = fmaxf(tmax, dot);
+  }
+  const float m = block_max(tmax, red);
+  float tsum = 0.f;
+  for (int j = tid; j <= last; j += kFusedThreads) {
+    const float p = exp2f(sc[j] - m);
+    sc[j] = p;
+    tsum += p;
+  }
+  const float l = block_sum(tsum, red);  // its barriers also publish sc[]
+
+  constexpr int R = kFusedThreads / D;  // key groups
+  const int c = tid % D, g = tid / D;
+  float acc = 0.f;
+  for (int j = g; j <= last; j += R) acc = fmaf(sc[j], Vh[(int64_t)j * D + c], acc);
+  part[tid] = acc;
+  __syncthreads();
+  if (g == 0) {
+    float t = 0.f;
+#pragma unroll
+    for (int r = 0; r < R; ++r) t += part[r * D + c];
+    O[(n * S + i) * D + c] = t / l;
+  }
+}
+
+size_t flash_smem(int d) { return sizeof(float) * (size_t)(2 * d * kLD + kBC * d + kBC * kLD); }
+size_t naive_scores_smem(int d) { return sizeof(float) * (size_t)(2 * d * kLD); }
+size_t naive_pv_smem(int d) { return sizeof(float) * (size_t)(kBC * kLD + kBC * d); }
+size_t fused_smem(int S, int d) { return sizeof(float) * (size_t)(d + 32 + kFusedThreads + S); }
+
+template <typename F>
+cudaError_t set_smem(F* kernel, size_t bytes) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+template <int D>
+cudaError_t flash_launch(const AttnProblem& p, cudaStream_t st) {
+  const size_t smem = flash_smem(D);
+  cudaError_t e = set_smem(flash_f32_kernel<D>, smem);
+  if (e != cudaSuccess) return e;
+  const int64_t tiles = (p.S + kBR - 1) / kBR;
+  flash_f32_kernel<D><<<(unsigned)(tiles * p.N), kThreads, smem, st>>>(
+      (const float*)p.q, (const float*)p.k, (const float*)p.v, (float*)p.o, p.N, p.S, p.causal,
+      p.scale * kLog2e);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t naive_launch(const AttnProblem& p, float* scores, cudaStream_t st) {
+  cudaError_t e = set_smem(naive_scores_kernel<D>, naive_scores_smem(D));
+  if (e == cudaSuccess) e = set_smem(naive_pv_kernel<D>, naive_pv_smem(D));
+  if (e != cudaSuccess) return e;
+  const int tiles = (p.S + kBR - 1) / kBR;
+  naive_scores_kernel<D><<<dim3(tiles, tiles, (unsigned)p.N), kThreads, naive_scores_smem(D), st>>>(
+      (const float*)p.q, (const float*)p.k, scores, p.N, p.S, p.causal, p.scale);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const int64_t rows = p.N * p.S;
+  naive_softmax_kernel<<<(unsigned)((rows + kThreads / 32 - 1) / (kThreads / 32)), kThreads, 0, st>>>(
+      scores, rows, p.S, p.causal);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  naive_pv_kernel<D><<<(unsigned)(tiles * p.N), kThreads, naive_pv_smem(D), st>>>(
+      scores, (const float*)p.v, (float*)p.o, p.N, p.S, p.causal);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t fused_launch(const AttnProblem& p, cudaStream_t st) {
+  const size_t smem = fused_smem(p.S, D);
+  cudaError_t e = set_smem(fused_row_f32_kernel<D>, smem);
+  if (e != cudaSuccess) return e;
+  fused_row_f32_kernel<D><<<(unsigned)(p.N * p.S), kFusedThreads, smem, st>>>(
+      (const float*)p.q, (const float*)p.k, (const float*)p.v, (float*)p.o, p.S, p.causal, p.scale * kLog2e);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_flash_f32(const AttnProblem& p, cudaStream_t st) {
+  switch (p.d) {
+    case 32: return flash_launch<32>(p, st);
+    case 64: return flash_launch<64>(p, st);
+    case 128: return flash_launch<128>(p, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+size_t naive_workspace_bytes(int64_t N, int S) { return (size_t)N * (size_t)S * (size_t)S * sizeof(float); }
+
+cudaError_t launch_naive_f32(const AttnProblem& p, float* scores, cudaStream_t st) {
+  switch (p.d) {
+    case 32: return naive_launch<32>(p, scores, st);
+    case 64: return naive_launch<64>(p, scores, st);
+    case 128: return naive_launch<128>(p, scores, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+int fused_f32_check(int S, int d) {
+  int dev = 0, optin = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KB_ERR_NO_DEVICE;
+  if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+    return KB_ERR_CUDA;
+  return fused_smem(S, d) <= (size_t)optin ? KB_OK : KB_ERR_UNSUPPORTED;
+}
+
+cudaError_t launch_fused_f32(const AttnProblem& p, cudaStream_t st) {
+  switch (p.d) {
+    case 32: return fused_launch<32>(p, st);
+    case 64: return fused_launch<64>(p, st);
+    case 128: return fused_launch<128>(p, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace kb

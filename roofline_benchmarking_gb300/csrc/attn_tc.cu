@@ -1,0 +1,485 @@
+// attn_tc.cu -- attention forward on the sm_103a tensor cores (bf16 / f16).
+//
+// The algorithm is the tiled online softmax of the kbench page ("kbench --
+// Transformer Attention Micro-benchmark Harness", section "Implementation
+// details / The three GPU kernels", the flash kernel: keys and values stream
+// through in tiles, a running max m and denominator l are kept per query row,
+// the score matrix is never materialised). It is laid out for GB300:
+//
+//  * one CTA per (head, 128-row query tile), heaviest causal tiles first;
+//  * warp 4 (one lane) stages the Q tile and a ring of K and V tiles with TMA
+//    (128-byte swizzle, 3-D tensor maps [N, S, d], rows past S zero-filled);
+//  * warp 5 (one lane) issues tcgen05 MMAs: S = Q K^T into one of two
+//    128x128 fp32 TMEM buffers, and O += P V into a 128 x d fp32 TMEM
+//    accumulator; completion is signalled through mbarriers by tcgen05.commit;
+//  * warps 0-3 own one query row per thread (TMEM lane = row): they load the
+//    score row from TMEM, apply scale and causal/tail masks, update the
+//    running max (in base 2, scale*log2(e) folded into one FMA), write
+//    P = exp2(s - m) as bf16/f16 into shared memory in the MMA operand layout,
+//    and rescale O in TMEM only when the row max grew by more than 2^8
+//    (the final O / l is exact either way);
+//  * the S MMA of tile j+1 runs while the softmax of tile j does, and P V of
+//    tile j is issued as soon as P_j is written.
+// Every mbarrier wait is bounded by %globaltimer; a wait that runs out sets the
+// library's device error word and an abort flag, every role then leaves its
+// loop, waits (bounded) for its own TMA copies and MMAs in flight, and the
+// tensor memory is released before the CTA exits.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "internal.h"
+#include "tc_ptx.cuh"
+
+namespace kb {
+
+// Device error word: bit 0 = a bounded wait ran out.
+__device__ unsigned int g_kb_error_word;
+
+namespace {
+
+constexpr int kBM = 128;  // query rows per tile (TMEM lanes)
+constexpr int kBN = 128;  // keys per tile
+constexpr int kThreadsTC = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColBlock = 16384;  // one 128-row x 128-byte swizzled block
+constexpr unsigned long long kDefaultWaitLimitNs = 1000000000ull;
+
+template <int D>
+struct TcCfg {
+  static_assert(D == 64 || D == 128, "tensor-core path supports d = 64 and 128");
+  static constexpr int DB = D / 64;          // 128-byte column blocks per tile row
+  static constexpr int TILE = kBM * D * 2;   // bytes of a Q, K or V tile
+  static constexpr int PTILE = kBM * kBN * 2;
+  static constexpr int KS = D == 128 ? 2 : 3;  // K ring stages
+  static constexpr int VS = D == 128 ? 2 : 3;  // V ring stages
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + TILE;
+  static constexpr int OFF_V = OFF_K + KS * TILE;
+  static constexpr int OFF_P = OFF_V + VS * TILE;
+  static constexpr int OFF_BAR = OFF_P + 2 * PTILE;
+  enum {
+    B_Q = 0,
+    B_KFULL = 1,
+    B_KEMPTY = B_KFULL + KS,
+    B_VFULL = B_KEMPTY + KS,
+    B_VEMPTY = B_VFULL + VS,
+    B_SFULL = B_VEMPTY + VS,
+    B_SFREE = B_SFULL + 2,
+    B_PFULL = B_SFREE + 2,
+    B_PFREE = B_PFULL + 2,
+    B_ODONE = B_PFREE + 2,
+    B_OFINAL = B_ODONE + 1,
+    B_DRAIN = B_OFINAL + 1,
+    NBAR = B_DRAIN + 1
+  };
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // [0] TMEM base, [1] abort flag
+  static constexpr int BYTES = OFF_MISC + 16;
+  static constexpr int SMEM = BYTES + 1024;  // slack to align the base to 1024 bytes
+  // TMEM columns: S buffers at 0 and 128, O at 256.
+  static constexpr uint32_t TM_O = 256;
+};
+
+// Bounded wait on phase `parity` of `bar`. Gives up when the abort flag is set
+// (if `honor_abort`) or after `limit` ns, recording the timeout.
+__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                      unsigned long long limit, bool honor_abort) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i)
+      if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (honor_abort && *abort_flag) return false;
+    if (ptx::globaltimer() - t0 > limit) {
+      *abort_flag = 1;
+      atomicOr(&g_kb_error_word, 1u);
+      return false;
+    }
+  }
+}
+
+// All lanes wait; the warp proceeds only if every lane saw the phase complete.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          unsigned long long limit) {
+  const bool ok = wait_bar(bar, parity, abort_flag, limit, true);
+  return __all_sync(0xffffffffu, ok);
+}
+
+template <bool F16>
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  if constexpr (F16) {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  } else {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+
+template <int D, bool F16>
+__global__ void __launch_bounds__(kThreadsTC, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                   const __grid_constant__ CUtensorMap tmv, uint8_t* __restrict__ out, int N, int S, int causal,
+                   float scale_log2, unsigned long long limit) {
+  using C = TcCfg<D>;
+  constexpr uint32_t kAB = F16 ? 0u : 1u;
+  constexpr uint32_t IDESC_QK = ptx::f16_idesc(kBM, kBN, kAB, 0);
+  constexpr uint32_t IDESC_PV = ptx::f16_idesc(kBM, D, kAB, 1);
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* sm = smem_raw + (base - raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::OFF_MISC + 4);
+  auto bar = [&](int i) -> uint32_t { return base + C::OFF_BAR + 8u * (uint32_t)i; };
+
+  const int ntiles = (S + kBM - 1) / kBM;
+  const int n = (int)(blockIdx.x % (unsigned)N);
+  const int qt = ntiles - 1 - (int)(blockIdx.x / (unsigned)N);
+  const int q0 = qt * kBM;
+  const int nkv = causal ? qt + 1 : ntiles;
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    ptx::mbar_init(bar(C::B_Q), 1);
+    for (int s = 0; s < C::KS; ++s) {
+      ptx::mbar_init(bar(C::B_KFULL + s), 1);
+      ptx::mbar_init(bar(C::B_KEMPTY + s), 1);
+    }
+    for (int s = 0; s < C::VS; ++s) {
+      ptx::mbar_init(bar(C::B_VFULL + s), 1);
+      ptx::mbar_init(bar(C::B_VEMPTY + s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(bar(C::B_SFULL + s), 1);
+      ptx::mbar_init(bar(C::B_SFREE + s), 4 * 32);
+      ptx::mbar_init(bar(C::B_PFULL + s), 4 * 32);
+      ptx::mbar_init(bar(C::B_PFREE + s), 1);
+    }
+    ptx::mbar_init(bar(C::B_ODONE), 1);
+    ptx::mbar_init(bar(C::B_OFINAL), 1);
+    ptx::mbar_init(bar(C::B_DRAIN), 1);
+    ptx::fence_mbar_init();
+  }
+  if (warp == 5) {
+    ptx::tmem_alloc(base + C::OFF_MISC, kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + C::OFF_MISC);
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      ptx::tma_prefetch_desc(&tmq);
+      ptx::tma_prefetch_desc(&tmk);
+      ptx::tma_prefetch_desc(&tmv);
+      ptx::mbar_arrive_expect_tx(bar(C::B_Q), C::TILE);
+      for (int b = 0; b < C::DB; ++b)
+        ptx::tma_load_3d(base + C::OFF_Q + b * kColBlock, &tmq, bar(C::B_Q), b * 64, q0, n);
+      int kdone = 0, vdone = 0;  // loads issued
+      bool ok = true;
+      for (int j = 0; j < nkv && ok; ++j) {
+        const int ks = j % C::KS, vs = j % C::VS;
+        if (j >= C::KS) ok = wait_bar(bar(C::B_KEMPTY + ks), ((j / C::KS) & 1) ^ 1, abort_flag, limit, true);
+        if (!ok) break;
+        ptx::mbar_arrive_expect_tx(bar(C::B_KFULL + ks), C::TILE);
+        for (int b = 0; b < C::DB; ++b)
+          ptx::tma_load_3d(base + C::OFF_K + ks * C::TILE + b * kColBlock, &tmk, bar(C::B_KFULL + ks), b * 64,
+                           j * kBN, n);
+        kdone = j + 1;
+        if (j >= C::VS) ok = wait_bar(bar(C::B_VEMPTY + vs), ((j / C::VS) & 1) ^ 1, abort_flag, limit, true);
+        if (!ok) break;
+        ptx::mbar_arrive_expect_tx(bar(C::B_VFULL + vs), C::TILE);
+        for (int b = 0; b < C::DB; ++b)
+          ptx::tma_load_3d(base + C::OFF_V + vs * C::TILE + b * kColBlock, &tmv, bar(C::B_VFULL + vs), b * 64,
+                           j * kBN, n);
+        vdone = j + 1;
+      }
+      // Every copy this CTA started must land before the CTA exits.
+      wait_bar(bar(C::B_Q), 0, abort_flag, limit, false);
+      for (int j = kdone - C::KS < 0 ? 0 : kdone - C::KS; j < kdone; ++j)
+        wait_bar(bar(C::B_KFULL + j % C::KS), (j / C::KS) & 1, abort_flag, limit, false);
+      for (int j = vdone - C::VS < 0 ? 0 : vdone - C::VS; j < vdone; ++j)
+        wait_bar(bar(C::B_VFULL + j % C::VS), (j / C::VS) & 1, abort_flag, limit, false);
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      bool ok = wait_bar(bar(C::B_Q), 0, abort_flag, limit, true);
+      auto issue_pv = [&](int t) -> bool {
+        const int pb = t & 1, vs = t % C::VS;
+        if (!wait_bar(bar(C::B_VFULL + vs), (t / C::VS) & 1, abort_flag, limit, true)) return false;
+        if (!wait_bar(bar(C::B_PFULL + pb), (t >> 1) & 1, abort_flag, limit, true)) return false;
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          const uint64_t a = ptx::sw128_desc(
+              base + C::OFF_P + pb * C::PTILE + (kk >> 2) * kColBlock + (kk & 3) * 32, 16, 1024);
+          const uint64_t b = ptx::sw128_desc(base + C::OFF_V + vs * C::TILE + kk * 16 * 128, kColBlock, 1024);
+          ptx::mma_f16_ss(tmem + C::TM_O, a, b, IDESC_PV, (t > 0 || kk > 0) ? 1u : 0u);
+        }
+        ptx::mma_commit(bar(C::B_ODONE));
+        ptx::mma_commit(bar(C::B_VEMPTY + vs));
+        ptx::mma_commit(bar(C::B_PFREE + pb));
+        return true;
+      };
+      for (int j = 0; j < nkv && ok; ++j) {
+        const int sb = j & 1, ks = j % C::KS;
+        ok = wait_bar(bar(C::B_KFULL + ks), (j / C::KS) & 1, abort_flag, limit, true);
+        if (ok && j >= 2) ok = wait_bar(bar(C::B_SFREE + sb), ((j >> 1) - 1) & 1, abort_flag, limit, true);
+        if (!ok) break;
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kColBlock + (kk & 3) * 32;
+          const uint64_t a = ptx::sw128_desc(base + C::OFF_Q + off, 16, 1024);
+          const uint64_t b = ptx::sw128_desc(base + C::OFF_K + ks * C::TILE + off, 16, 1024);
+          ptx::mma_f16_ss(tmem + (uint32_t)sb * kBN, a, b, IDESC_QK, kk > 0 ? 1u : 0u);
+        }
+        ptx::mma_commit(bar(C::B_SFULL + sb));
+        ptx::mma_commit(bar(C::B_KEMPTY + ks));
+        if (j >= 1) ok = issue_pv(j - 1);
+      }
+      if (ok) ok = issue_pv(nkv - 1);
+      if (ok) ptx::mma_commit(bar(C::B_OFINAL));
+      // No MMA may still be running when the tensor memory is released.
+      ptx::mma_commit(bar(C::B_DRAIN));
+      wait_bar(bar(C::B_DRAIN), 0, abort_flag, limit, false);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax, warps 0-3
+    const int r = warp * 32 + lane;  // row within the tile = TMEM lane
+    const int row = q0 + r;
+    const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nkv; ++j) {
+      const int sb = j & 1;
+      if (!(ok = warp_wait(bar(C::B_SFULL + sb), (j >> 1) & 1, abort_flag, limit))) break;
+      ptx::tc_fence_after();
+      float s[kBN];
+      {
+        uint32_t u[32];
+#pragma unroll
+        for (int cb = 0; cb < kBN / 32; ++cb) {
+          ptx::tmem_ld32(tl + (uint32_t)sb * kBN + cb * 32, u);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) s[cb * 32 + e] = __uint_as_float(u[e]);
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar(C::B_SFREE + sb));
+
+      const int k0 = j * kBN;
+      if ((causal && j == qt) || k0 + kBN > S) {
+#pragma unroll
+        for (int c = 0; c < kBN; ++c) {
+          const int key = k0 + c;
+          if (key >= S || (causal && key > row)) s[c] = -INFINITY;
+        }
+      }
+      float mx[4] = {s[0], s[1], s[2], s[3]};
+#pragma unroll
+      for (int c = 4; c < kBN; c += 4) {
+        mx[0] = fmaxf(mx[0], s[c]);
+        mx[1] = fmaxf(mx[1], s[c + 1]);
+        mx[2] = fmaxf(mx[2], s[c + 2]);
+        mx[3] = fmaxf(mx[3], s[c + 3]);
+      }
+      const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * scale_log2;
+      float alpha = 1.f;
+      bool corr = false;
+      if (j == 0) {
+        m_run = m_tile == -INFINITY ? 0.f : m_tile;
+      } else if (m_tile > m_run + 8.0f) {
+        alpha = ptx::ex2(m_run - m_tile);
+        m_run = m_tile;
+        l_run *= alpha;
+        corr = true;
+      }
+      if (j >= 2 && !(ok = warp_wait(bar(C::B_PFREE + sb), ((j >> 1) - 1) & 1, abort_flag, limit))) break;
+
+      // P = exp2(s*scale_log2 - m) -> 16-bit, stored K-major with the 128-byte swizzle
+      const float neg_m = -m_run;
+      float sum = 0.f;
+      const uint32_t prow = base + C::OFF_P + sb * C::PTILE + (uint32_t)r * 128;
+#pragma unroll
+      for (int c16 = 0; c16 < kBN / 8; ++c16) {
+        float p[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          p[e] = ptx::ex2(fmaf(s[c16 * 8 + e], scale_log2, neg_m));
+          sum += p[e];
+        }
+        const uint32_t addr = prow + (c16 >> 3) * kColBlock + ((uint32_t)((c16 & 7) ^ (r & 7)) << 4);
+        ptx::st_shared_v4(addr, pack2<F16>(p[0], p[1]), pack2<F16>(p[2], p[3]), pack2<F16>(p[4], p[5]),
+                          pack2<F16>(p[6], p[7]));
+      }
+      l_run += sum;
+      ptx::fence_proxy_async_smem();
+
+      if (__any_sync(0xffffffffu, corr)) {
+        // O holds P V of tiles < j; it must be complete before it is rescaled
+        if (!(ok = warp_wait(bar(C::B_ODONE), (j - 1) & 1, abort_flag, limit))) break;
+        ptx::tc_fence_after();
+        uint32_t u[32];
+#pragma unroll
+        for (int cb = 0; cb < D / 32; ++cb) {
+          ptx::tmem_ld32(tl + C::TM_O + cb * 32, u);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * alpha);
+          ptx::tmem_st32(tl + C::TM_O + cb * 32, u);
+        }
+        ptx::tmem_wait_st();
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar(C::B_PFULL + sb));
+    }
+    if (ok) ok = warp_wait(bar(C::B_OFINAL), 0, abort_flag, limit);
+    if (ok) {
+      ptx::tc_fence_after();
+      const float inv = 1.0f / l_run;
+      uint8_t* orow = out + ((size_t)n * S + row) * (size_t)D * 2;
+      uint32_t u[32];
+#pragma unroll
+      for (int cb = 0; cb < D / 32; ++cb) {
+        ptx::tmem_ld32(tl + C::TM_O + cb * 32, u);
+        ptx::tmem_wait_ld();
+        if (row < S) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 w;
+            w.x = pack2<F16>(__uint_as_float(u[q * 8 + 0]) * inv, __uint_as_float(u[q * 8 + 1]) * inv);
+            w.y = pack2<F16>(__uint_as_float(u[q * 8 + 2]) * inv, __uint_as_float(u[q * 8 + 3]) * inv);
+            w.z = pack2<F16>(__uint_as_float(u[q * 8 + 4]) * inv, __uint_as_float(u[q * 8 + 5]) * inv);
+            w.w = pack2<F16>(__uint_as_float(u[q * 8 + 6]) * inv, __uint_as_float(u[q * 8 + 7]) * inv);
+            *reinterpret_cast<uint4*>(orow + cb * 64 + q * 16) = w;
+          }
+        }
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// One thread waits on an mbarrier nothing will complete; the bounded wait must
+// record a timeout and return.
+__global__ void selftest_timeout_kernel(unsigned long long limit) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    ptx::mbar_init(ptx::smem_u32(&bar), 1);
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) wait_bar(ptx::smem_u32(&bar), 0, &abort_flag, limit, false);
+}
+
+// ---- host side ----------------------------------------------------------------
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+    (void)cudaGetLastError();
+  });
+  return fn;
+}
+
+// [N, S, d] row-major 16-bit tensor, boxes of 64 features x 128 rows x 1 head.
+bool make_map(CUtensorMap* m, const void* ptr, int64_t N, int S, int d, bool f16) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)S, (cuuint64_t)N};
+  const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)S * d * 2};
+  const cuuint32_t box[3] = {64, (cuuint32_t)kBM, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                  const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int D, bool F16>
+cudaError_t tc_launch(const AttnProblem& p, cudaStream_t st) {
+  using C = TcCfg<D>;
+  // per-device attribute, so it is set on every launch
+  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, p.q, p.N, p.S, D, F16) || !make_map(&mk, p.k, p.N, p.S, D, F16) ||
+      !make_map(&mv, p.v, p.N, p.S, D, F16))
+    return cudaErrorInvalidValue;
+  const int64_t tiles = (p.S + kBM - 1) / kBM;
+  attn_tc_kernel<D, F16><<<(unsigned)(tiles * p.N), kThreadsTC, C::SMEM, st>>>(
+      mq, mk, mv, static_cast<uint8_t*>(p.o), (int)p.N, p.S, p.causal, p.scale * 1.4426950408889634f,
+      kDefaultWaitLimitNs);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int tc_check(int S, int d, int dtype) {
+  (void)S;
+  if (d != 64 && d != 128) return KB_ERR_UNSUPPORTED;
+  if (dtype != KB_BF16 && dtype != KB_F16) return KB_ERR_UNSUPPORTED;
+  int dev = 0, optin = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KB_ERR_NO_DEVICE;
+  if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+    return KB_ERR_CUDA;
+  const int need = d == 128 ? TcCfg<128>::SMEM : TcCfg<64>::SMEM;
+  return need <= optin ? KB_OK : KB_ERR_UNSUPPORTED;
+}
+
+cudaError_t launch_tc(const AttnProblem& p, cudaStream_t st) {
+  const bool f16 = p.dtype == KB_F16;
+  if (p.d == 128) return f16 ? tc_launch<128, true>(p, st) : tc_launch<128, false>(p, st);
+  if (p.d == 64) return f16 ? tc_launch<64, true>(p, st) : tc_launch<64, false>(p, st);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t read_and_clear_error_word(unsigned int* out, cudaStream_t st) {
+  cudaError_t e = cudaMemcpyFromSymbolAsync(out, g_kb_error_word, sizeof(unsigned int), 0,
+                                            cudaMemcpyDeviceToHost, st);
+  if (e != cudaSuccess) return e;
+  const unsigned int zero = 0;
+  if ((e = cudaMemcpyToSymbolAsync(g_kb_error_word, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, st)) !=
+      cudaSuccess)
+    return e;
+  return cudaStreamSynchronize(st);
+}
+
+cudaError_t launch_selftest_timeout(unsigned long long limit_ns, cudaStream_t st) {
+  selftest_timeout_kernel<<<1, 32, 0, st>>>(limit_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace kb

@@ -1,0 +1,48 @@
+// internal.h -- declarations shared by the library's translation units (not
+// part of the ABI; the public interface is include/kbattn.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/kbattn.h"
+
+namespace kb {
+
+// Attention problem as validated by the API layer.
+struct AttnProblem {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  int64_t N;  // B*H
+  int S;
+  int d;
+  int causal;
+  float scale;
+  int dtype;
+};
+
+// Launchers return a cudaError_t from the launch (or cudaSuccess).
+cudaError_t launch_flash_f32(const AttnProblem& p, cudaStream_t st);
+cudaError_t launch_fused_f32(const AttnProblem& p, cudaStream_t st);
+cudaError_t launch_naive_f32(const AttnProblem& p, float* scores, cudaStream_t st);
+size_t naive_workspace_bytes(int64_t N, int S);
+// 0 if the fused-row kernel can run S keys on the current device, else an error code.
+int fused_f32_check(int S, int d);
+
+cudaError_t launch_tc(const AttnProblem& p, cudaStream_t st);
+int tc_check(int S, int d, int dtype);
+
+cudaError_t launch_triad(float* a, const float* b, const float* c, float s, size_t n, int block,
+                         cudaStream_t st);
+
+// Device error word (bounded waits that ran out).
+cudaError_t read_and_clear_error_word(unsigned int* out, cudaStream_t st);
+cudaError_t launch_selftest_timeout(unsigned long long limit_ns, cudaStream_t st);
+
+// Per-thread record of the last CUDA error returned as KB_ERR_CUDA.
+void set_last_cuda_error(cudaError_t e);
+
+}  // namespace kb

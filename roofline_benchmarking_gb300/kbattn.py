@@ -1,0 +1,263 @@
+"""ctypes binding of libkbattn (include/kbattn.h): the same entry points, with
+argument marshalling only. Every step of the computation runs in the CUDA
+library; there is no fallback. If the library has not been built, loading it
+raises.
+
+Tensors are passed as torch tensors (device memory and streams come from
+PyTorch); the ``*_ptr`` forms take raw integers for callers that manage memory
+themselves.
+"""
+from __future__ import annotations
+
+import ctypes
+import enum
+import os
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIBRARY = os.path.join(HERE, "libkbattn.so")
+
+
+class Status(enum.IntEnum):
+    OK = 0
+    INVALID_ARG = 1
+    UNSUPPORTED = 2
+    CUDA = 3
+    NO_MEMORY = 4
+    TIMEOUT = 5
+    NO_DEVICE = 6
+
+
+class DType(enum.IntEnum):
+    F32 = 0
+    BF16 = 1
+    F16 = 2
+
+
+class Variant(enum.IntEnum):
+    AUTO = 0
+    NAIVE = 1
+    FUSED = 2
+    FLASH = 3
+    TC = 4
+
+
+class DeviceInfo(ctypes.Structure):
+    _fields_ = [
+        ("device", ctypes.c_int),
+        ("cc_major", ctypes.c_int),
+        ("cc_minor", ctypes.c_int),
+        ("sm_count", ctypes.c_int),
+        ("sm_clock_khz", ctypes.c_int),
+        ("mem_clock_khz", ctypes.c_int),
+        ("mem_bus_width_bits", ctypes.c_int),
+        ("l2_bytes", ctypes.c_int),
+        ("smem_per_block_optin", ctypes.c_int),
+        ("smem_per_sm", ctypes.c_int),
+        ("total_mem_bytes", ctypes.c_size_t),
+        ("name", ctypes.c_char * 256),
+    ]
+
+    def as_dict(self) -> dict:
+        d = {f: getattr(self, f) for f, _ in self._fields_}
+        d["name"] = self.name.decode(errors="replace")
+        return d
+
+
+class KbError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)}"
+                         + (f" (cudaError {last_cuda_error()})" if status == Status.CUDA else ""))
+
+
+# Entry points and their C signatures (names identical to include/kbattn.h).
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+_SZ = ctypes.c_size_t
+_FP = ctypes.POINTER(ctypes.c_float)
+SIGNATURES = {
+    "kb_attn_fwd": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P]),
+    "kb_attn_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "kb_attn_fwd_ws": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P, _P, _SZ]),
+    "kb_attn_bench": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P, _P, _SZ, _I, _I, _FP]),
+    "kb_triad": (_I, [_P, _P, _P, _F, _SZ, _I, _P]),
+    "kb_triad_bench": (_I, [_P, _P, _P, _F, _SZ, _I, _P, _I, _I, _FP]),
+    "kb_device_info": (_I, [_I, ctypes.POINTER(DeviceInfo)]),
+    "kb_check_device_error": (_I, [_P]),
+    "kb_selftest_timeout": (_I, [ctypes.c_ulonglong, _P]),
+    "kb_status_string": (ctypes.c_char_p, [_I]),
+    "kb_last_cuda_error": (_I, []),
+    "kb_version": (_I, []),
+}
+
+_lib = None
+_lock = threading.Lock()
+
+
+def load(path: str = LIBRARY) -> ctypes.CDLL:
+    """Load libkbattn (once). Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"libkbattn is not built ({path} missing); run "
+                    "`python -m roofline_benchmarking_gb300.build`")
+            lib = ctypes.CDLL(path)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+        return _lib
+
+
+def status_string(status: int) -> str:
+    return load().kb_status_string(int(status)).decode()
+
+
+def last_cuda_error() -> int:
+    return load().kb_last_cuda_error()
+
+
+def version() -> int:
+    return load().kb_version()
+
+
+def _check(status: int, what: str) -> None:
+    if status != Status.OK:
+        raise KbError(status, what)
+
+
+def _stream_ptr(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+_DTYPES = None
+
+
+def _dtype_code(t) -> int:
+    global _DTYPES
+    if _DTYPES is None:
+        import torch
+        _DTYPES = {torch.float32: DType.F32, torch.bfloat16: DType.BF16, torch.float16: DType.F16}
+    try:
+        return int(_DTYPES[t.dtype])
+    except KeyError:
+        raise ValueError(f"unsupported dtype {t.dtype}") from None
+
+
+def _attn_args(q, k, v, o):
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+        if t.dim() != 4 or t.shape != q.shape or t.dtype != q.dtype:
+            raise ValueError(f"{name} must be [B, H, S, d] like q, with q's dtype")
+    B, H, S, d = q.shape
+    return B, H, S, d, _dtype_code(q)
+
+
+# ---------------------------------------------------------------- attention
+def kb_attn_fwd_ptr(q: int, k: int, v: int, o: int, B: int, H: int, S: int, d: int, causal: bool,
+                    scale: float, dtype: int, variant: int = Variant.AUTO, stream: int | None = 0) -> int:
+    """Raw form: device pointers as integers; returns the kb_status (no raise)."""
+    return load().kb_attn_fwd(q, k, v, o, B, H, S, d, int(causal), float(scale), int(dtype),
+                              int(variant), stream)
+
+
+def kb_attn_fwd(q, k, v, o=None, causal: bool = False, scale: float | None = None,
+                variant: int = Variant.AUTO, stream=None):
+    """O = softmax(Q K^T * scale [+ causal mask]) V on the current CUDA device.
+
+    q, k, v: contiguous CUDA tensors [B, H, S, d] (fp32, bf16 or f16). ``o`` is
+    written if given, else allocated. ``scale`` defaults to 1/sqrt(d).
+    """
+    import torch
+    if o is None:
+        o = torch.empty_like(q)
+    B, H, S, d, dt = _attn_args(q, k, v, o)
+    if scale is None:
+        scale = d ** -0.5
+    st = load().kb_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, H, S, d,
+                            int(bool(causal)), float(scale), dt, int(variant), _stream_ptr(stream))
+    _check(st, "kb_attn_fwd")
+    return o
+
+
+def kb_attn_workspace_bytes(B: int, H: int, S: int, d: int, dtype: int, variant: int) -> int:
+    return int(load().kb_attn_workspace_bytes(B, H, S, d, int(dtype), int(variant)))
+
+
+def kb_attn_fwd_ws(q, k, v, o, workspace, causal: bool = False, scale: float | None = None,
+                   variant: int = Variant.AUTO, stream=None):
+    """kb_attn_fwd with a caller-owned workspace tensor (any dtype, on the device)."""
+    B, H, S, d, dt = _attn_args(q, k, v, o)
+    if scale is None:
+        scale = d ** -0.5
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = load().kb_attn_fwd_ws(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, H, S, d,
+                               int(bool(causal)), float(scale), dt, int(variant), _stream_ptr(stream),
+                               ws_ptr, ws_bytes)
+    _check(st, "kb_attn_fwd_ws")
+    return o
+
+
+def kb_attn_bench(q, k, v, o, causal: bool, scale: float | None = None, variant: int = Variant.AUTO,
+                  warmup: int = 3, iters: int = 10, workspace=None, stream=None) -> list[float]:
+    """Per-call device times in ms of ``iters`` timed calls after ``warmup`` untimed ones."""
+    B, H, S, d, dt = _attn_args(q, k, v, o)
+    if scale is None:
+        scale = d ** -0.5
+    ms = (ctypes.c_float * iters)()
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = load().kb_attn_bench(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, H, S, d,
+                              int(bool(causal)), float(scale), dt, int(variant), _stream_ptr(stream),
+                              ws_ptr, ws_bytes, warmup, iters, ms)
+    _check(st, "kb_attn_bench")
+    return list(ms)
+
+
+# ---------------------------------------------------------------- triad
+def kb_triad(a, b, c, s: float, block: int = 256, stream=None):
+    """a = b + s*c (fp32, one rounding) over every element of the CUDA tensors."""
+    n = a.numel()
+    if b.numel() != n or c.numel() != n:
+        raise ValueError("a, b, c must have the same number of elements")
+    st = load().kb_triad(a.data_ptr(), b.data_ptr(), c.data_ptr(), float(s), n, block, _stream_ptr(stream))
+    _check(st, "kb_triad")
+    return a
+
+
+def kb_triad_bench(a, b, c, s: float, block: int = 256, warmup: int = 3, iters: int = 10,
+                   stream=None) -> list[float]:
+    n = a.numel()
+    ms = (ctypes.c_float * iters)()
+    st = load().kb_triad_bench(a.data_ptr(), b.data_ptr(), c.data_ptr(), float(s), n, block,
+                               _stream_ptr(stream), warmup, iters, ms)
+    _check(st, "kb_triad_bench")
+    return list(ms)
+
+
+# ---------------------------------------------------------------- device
+def kb_device_info(device: int = 0) -> dict:
+    info = DeviceInfo()
+    _check(load().kb_device_info(device, ctypes.byref(info)), "kb_device_info")
+    return info.as_dict()
+
+
+def kb_check_device_error(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device error status."""
+    return int(load().kb_check_device_error(_stream_ptr(stream)))
+
+
+def kb_selftest_timeout(limit_ns: int = 1_000_000, stream=None) -> None:
+    _check(load().kb_selftest_timeout(int(limit_ns), _stream_ptr(stream)), "kb_selftest_timeout")

@@ -1,0 +1,148 @@
+"""The C-ABI boundary without a GPU: the library builds, loads, exports every
+entry point include/kbattn.h declares, and rejects invalid requests before any
+CUDA call (so these run on a CPU-only host)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from roofline_benchmarking_gb300 import build as kb_build
+from roofline_benchmarking_gb300 import kbattn
+from roofline_benchmarking_gb300.kbattn import DType, Status, Variant
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kbattn.h")
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kb_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    kb_build.build()
+    return kbattn.load()
+
+
+def test_header_declares_the_documented_calls():
+    names = header_functions()
+    for want in ("kb_attn_fwd", "kb_attn_fwd_ws", "kb_attn_workspace_bytes", "kb_attn_bench", "kb_triad",
+                 "kb_triad_bench", "kb_device_info", "kb_status_string", "kb_last_cuda_error"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", kbattn.LIBRARY], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(re.findall(r"\s[TW]\s+(\S+)$", out, flags=re.M))
+    missing = [n for n in header_functions() if n not in exported]
+    assert not missing, f"declared but not exported: {missing}"
+    # and the binding covers exactly the declared set
+    assert sorted(kbattn.SIGNATURES) == header_functions()
+    # only the ABI is exported (hidden visibility for everything else)
+    extra = sorted(n for n in exported if n.startswith("kb") and n not in header_functions())
+    assert not extra, extra
+
+
+def test_library_targets_sm103a_only(lib):
+    r = subprocess.run(["cuobjdump", "--list-elf", kbattn.LIBRARY], capture_output=True, text=True)
+    if r.returncode != 0:
+        pytest.skip("cuobjdump unavailable")
+    archs = set(re.findall(r"sm_\w+", r.stdout))
+    assert archs == {"sm_103a"}, archs
+
+
+FAKE = 1 << 20  # an aligned, never-dereferenced address
+
+
+def attn(q=FAKE, k=FAKE, v=FAKE, o=FAKE, B=1, H=1, S=64, d=64, causal=0, scale=0.125, dtype=DType.F32,
+         variant=Variant.FLASH):
+    return kbattn.kb_attn_fwd_ptr(q, k, v, o, B, H, S, d, causal, scale, dtype, variant, None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(q=0), Status.INVALID_ARG),
+    (dict(o=0), Status.INVALID_ARG),
+    (dict(v=FAKE + 4), Status.INVALID_ARG),          # not 16-byte aligned
+    (dict(B=0), Status.INVALID_ARG),
+    (dict(H=-1), Status.INVALID_ARG),
+    (dict(S=0), Status.INVALID_ARG),
+    (dict(d=0), Status.INVALID_ARG),
+    (dict(causal=2), Status.INVALID_ARG),
+    (dict(scale=0.0), Status.INVALID_ARG),
+    (dict(scale=-1.0), Status.INVALID_ARG),
+    (dict(scale=float("nan")), Status.INVALID_ARG),
+    (dict(scale=float("inf")), Status.INVALID_ARG),
+    (dict(dtype=7), Status.INVALID_ARG),
+    (dict(variant=9), Status.INVALID_ARG),
+    (dict(B=1 << 20, H=1 << 20, S=1 << 20, d=64), Status.INVALID_ARG),   # B*H overflows int32
+    (dict(B=1 << 15, H=1 << 15, S=1 << 30, d=128), Status.INVALID_ARG),  # bytes overflow int64
+    (dict(d=48), Status.UNSUPPORTED),
+    (dict(d=256), Status.UNSUPPORTED),
+    (dict(dtype=DType.F32, variant=Variant.TC), Status.UNSUPPORTED),
+    (dict(dtype=DType.BF16, variant=Variant.FLASH), Status.UNSUPPORTED),
+    (dict(dtype=DType.F16, variant=Variant.NAIVE), Status.UNSUPPORTED),
+])
+def test_invalid_requests_are_rejected_before_any_launch(lib, kw, want):
+    assert attn(**kw) == want
+
+
+def test_valid_request_without_a_device_reports_no_device(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    for variant, dtype in ((Variant.FLASH, DType.F32), (Variant.FUSED, DType.F32), (Variant.TC, DType.BF16),
+                           (Variant.AUTO, DType.F16)):
+        assert attn(variant=variant, dtype=dtype) == Status.NO_DEVICE
+    st = kbattn.load().kb_triad(FAKE, FAKE, FAKE, 1.0, 1024, 256, None)
+    assert st == Status.NO_DEVICE
+    info = kbattn.DeviceInfo()
+    assert kbattn.load().kb_device_info(0, ctypes.byref(info)) == Status.NO_DEVICE
+
+
+def test_naive_workspace_contract(lib):
+    assert kbattn.kb_attn_workspace_bytes(1, 8, 1024, 64, DType.F32, Variant.NAIVE) == 8 * 1024 * 1024 * 4
+    assert kbattn.kb_attn_workspace_bytes(2, 3, 5, 32, DType.F32, Variant.NAIVE) == 6 * 25 * 4
+    for v in (Variant.FLASH, Variant.FUSED, Variant.AUTO):
+        assert kbattn.kb_attn_workspace_bytes(1, 8, 1024, 64, DType.F32, v) == 0
+    assert kbattn.kb_attn_workspace_bytes(1, 8, 1024, 64, DType.BF16, Variant.TC) == 0
+    assert kbattn.kb_attn_workspace_bytes(0, 8, 1024, 64, DType.F32, Variant.NAIVE) == 0
+    # too small a workspace is refused before the device is touched
+    st = kbattn.load().kb_attn_fwd_ws(FAKE, FAKE, FAKE, FAKE, 1, 1, 64, 64, 0, 0.125, DType.F32, Variant.NAIVE,
+                                      None, FAKE, 64 * 64 * 4 - 1)
+    assert st == Status.NO_MEMORY
+    st = kbattn.load().kb_attn_fwd_ws(FAKE, FAKE, FAKE, FAKE, 1, 1, 64, 64, 0, 0.125, DType.F32, Variant.NAIVE,
+                                      None, None, 0)
+    assert st == Status.NO_MEMORY
+
+
+def test_triad_and_bench_argument_checks(lib):
+    L = kbattn.load()
+    assert L.kb_triad(FAKE, FAKE, FAKE, 1.0, 0, 256, None) == Status.OK      # n = 0 is a no-op
+    assert L.kb_triad(0, FAKE, FAKE, 1.0, 16, 256, None) == Status.INVALID_ARG
+    assert L.kb_triad(FAKE + 8, FAKE, FAKE, 1.0, 16, 256, None) == Status.INVALID_ARG
+    assert L.kb_triad(FAKE, FAKE, FAKE, 1.0, 16, 384, None) == Status.INVALID_ARG
+    ms = (ctypes.c_float * 1)()
+    assert L.kb_triad_bench(FAKE, FAKE, FAKE, 1.0, 16, 256, None, 0, 0, ms) == Status.INVALID_ARG
+    assert L.kb_attn_bench(FAKE, FAKE, FAKE, FAKE, 1, 1, 64, 64, 0, 0.125, 0, 3, None, None, 0, -1, 2,
+                           ms) == Status.INVALID_ARG
+
+
+def test_status_strings(lib):
+    for s in Status:
+        assert kbattn.status_string(s) == "KB_" + ("OK" if s == Status.OK else "ERR_" + s.name)
+    assert kbattn.status_string(99) == "KB_UNKNOWN_STATUS"
+    assert kbattn.version() == 100
+
+
+def test_binding_refuses_to_run_without_the_library(tmp_path):
+    # the product path fails loudly instead of falling back
+    code = ("import roofline_benchmarking_gb300.kbattn as k\n"
+            f"k.LIBRARY = {str(tmp_path / 'missing.so')!r}\n"
+            "try:\n    k.load(k.LIBRARY)\nexcept RuntimeError as e:\n    print('raised', e)\n")
+    r = subprocess.run(["python", "-c", code], capture_output=True, text=True, cwd=ROOT)
+    assert "raised" in r.stdout and "not built" in r.stdout

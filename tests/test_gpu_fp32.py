@@ -1,0 +1,91 @@
+"""GPU parity of the three fp32 CUDA-core variants (naive, fused-row, flash)
+against the oracle, element by element, max-abs <= 1e-4 (the fp32 tolerance)."""
+import numpy as np
+import pytest
+import torch
+
+from roofline_benchmarking_gb300 import inputs
+from roofline_benchmarking_gb300 import kbattn
+from roofline_benchmarking_gb300.kbattn import Variant
+from tests.gpu_util import Guarded, errors
+
+pytestmark = pytest.mark.gpu
+
+F32_TOL = 1e-4
+VARIANTS = [Variant.NAIVE, Variant.FUSED, Variant.FLASH]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    from roofline_benchmarking_gb300 import build
+    build.build()
+    return kbattn.load()
+
+
+def run(w, variant, use_ws=False):
+    q, k, v = (t.cuda() for t in inputs.make_qkv(w))
+    g = Guarded(q.shape, torch.float32)
+    if use_ws:
+        nbytes = kbattn.kb_attn_workspace_bytes(w.B, w.H, w.S, w.d, kbattn.DType.F32, variant)
+        ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device="cuda")
+        kbattn.kb_attn_fwd_ws(q, k, v, g.out, ws, causal=w.causal, scale=w.scale, variant=variant)
+    else:
+        kbattn.kb_attn_fwd(q, k, v, g.out, causal=w.causal, scale=w.scale, variant=variant)
+    assert kbattn.kb_check_device_error() == kbattn.Status.OK
+    return g.check().cpu().numpy()
+
+
+SMALL = [  # (B, H, S, d, causal): single tiles, several tiles, ragged tails, S = 1
+    (1, 1, 1, 32, False), (1, 2, 1, 64, True), (1, 1, 7, 64, True), (2, 1, 64, 32, False),
+    (1, 2, 65, 128, True), (1, 1, 129, 64, False), (2, 3, 200, 32, True), (1, 2, 255, 128, False),
+    (1, 1, 256, 64, True), (1, 1, 300, 128, True),
+]
+
+
+@pytest.mark.parametrize("variant", VARIANTS, ids=lambda v: v.name)
+@pytest.mark.parametrize("shape", SMALL, ids=lambda s: "b{}h{}s{}d{}{}".format(*s[:4], "c" if s[4] else ""))
+def test_small_shapes_match_oracle(oracle, variant, shape):
+    B, H, S, d, causal = shape
+    w = inputs.Workload("t", B, H, S, d, causal, "f32", 100 + S + d, "uniform")
+    got = run(w, variant)
+    want = oracle.attn(*inputs.make_qkv(w), causal, w.scale)
+    mx, mean, _ = errors(got, want)
+    assert mx <= F32_TOL, (mx, mean)
+
+
+@pytest.mark.parametrize("variant", VARIANTS, ids=lambda v: v.name)
+@pytest.mark.parametrize("w", [inputs.SINGLE_HEAD_F32, inputs.F32_S1024, inputs.F32_S1024_CAUSAL],
+                         ids=lambda w: w.name)
+def test_f32_workloads_match_oracle(oracle, variant, w):
+    got = run(w, variant)
+    want = oracle.attn(*inputs.make_qkv(w), w.causal, w.scale)
+    mx, mean, rel = errors(got, want)
+    assert mx <= F32_TOL, (mx, mean, rel)
+
+
+def test_naive_with_caller_workspace_matches_cached(oracle):
+    w = inputs.F32_S1024_CAUSAL.with_(H=2, S=320)
+    a = run(w, Variant.NAIVE, use_ws=False)
+    b = run(w, Variant.NAIVE, use_ws=True)
+    assert np.array_equal(a, b)
+
+
+def test_variants_agree_on_scale_and_large_scores(oracle):
+    """A large scale makes the softmax sharp: every variant must still match."""
+    w = inputs.Workload("sharp", 1, 2, 192, 64, True, "f32", 7, "uniform")
+    q, k, v = inputs.make_qkv(w)
+    q = (q * 6).contiguous()
+    want = oracle.attn(q, k, v, True, 2.0)
+    for variant in VARIANTS:
+        g = Guarded(q.shape, torch.float32)
+        kbattn.kb_attn_fwd(q.cuda(), k.cuda(), v.cuda(), g.out, causal=True, scale=2.0, variant=variant)
+        mx, _, _ = errors(g.check().cpu().numpy(), want)
+        assert mx <= F32_TOL, (variant, mx)
+
+
+def test_fused_rejects_rows_longer_than_shared_memory():
+    info = kbattn.kb_device_info(torch.cuda.current_device())
+    S = info["smem_per_block_optin"] // 4 + 1024
+    st = kbattn.kb_attn_fwd_ptr(1 << 20, 1 << 20, 1 << 20, 1 << 20, 1, 1, S, 64, False, 0.125,
+                                kbattn.DType.F32, Variant.FUSED, 0)
+    assert st == kbattn.Status.UNSUPPORTED

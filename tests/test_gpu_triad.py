@@ -1,0 +1,52 @@
+"""GPU Triad a = b + s*c: bit-exact against the oracle (one rounding), every
+block size, ragged lengths, and the STREAM constant check."""
+import numpy as np
+import pytest
+import torch
+
+from roofline_benchmarking_gb300 import inputs
+from roofline_benchmarking_gb300 import kbattn
+from tests.gpu_util import Guarded
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    from roofline_benchmarking_gb300 import build
+    build.build()
+    return kbattn.load()
+
+
+@pytest.mark.parametrize("block", [128, 256, 512])
+@pytest.mark.parametrize("n", [1, 3, 4, 5, 1023, 4099, (1 << 20) + 7, 3 * (1 << 22) + 2])
+def test_triad_bit_exact(oracle, n, block):
+    b, c = inputs.make_triad_inputs(n, seed=n)
+    s = -0.3711
+    g = Guarded((n,), torch.float32)
+    kbattn.kb_triad(g.out, b.cuda(), c.cuda(), s, block=block)
+    got = g.check().cpu().numpy()
+    want = oracle.triad(b.numpy(), c.numpy(), s)
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
+def test_triad_stream_constants():
+    n = 64 << 20
+    b = torch.ones(n, device="cuda")
+    c = torch.full((n,), 2.0, device="cuda")
+    a = torch.empty(n, device="cuda")
+    kbattn.kb_triad(a, b, c, 3.0)
+    assert bool((a == 7.0).all())
+
+
+def test_triad_bench_reports_every_iteration():
+    n = 16 << 20
+    a, b, c = (torch.zeros(n, device="cuda") for _ in range(3))
+    ms = kbattn.kb_triad_bench(a, b, c, 1.5, block=256, warmup=2, iters=5)
+    assert len(ms) == 5 and all(t > 0 for t in ms)
+
+
+def test_device_info_is_gb300_class():
+    info = kbattn.kb_device_info(torch.cuda.current_device())
+    assert (info["cc_major"], info["cc_minor"]) == (10, 3)
+    assert info["sm_count"] > 100 and info["mem_bus_width_bits"] > 0 and info["mem_clock_khz"] > 0
