@@ -1,0 +1,496 @@
+#!/usr/bin/env python
+"""Attention-forward benchmark: one JSON line on stdout (rank 0).
+
+A step is one kb_attn_fwd call over the whole workload (default: bf16 causal
+B=4 H=16 S=4096 d=128, seed 2, normal(0,1) rounded to bf16), i.e. one pass of
+the tensor-core hot path: TMA staging, S = Q K^T on tcgen05, online softmax,
+O += P V, normalisation and the bf16 store.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl ours (default): W untimed steps, then exactly K steps between CUDA
+events on the launching stream with a barrier and a device synchronise on both
+sides; the max over ranks is reported. value = FLOPs of all ranks / time.
+Also reported: the roofline fraction of the kernel (per-launch CUDA events),
+SM clocks sampled by nvidia-smi during the timed region, the end-to-end rate
+through the public API with pinned host buffers (copies inside the timed
+region), the STREAM Triad ceiling and the CPU oracle on a bounded row sample.
+
+--impl reference: the CPU oracle (the method's plain definition, one host core,
+double precision) timed on a bounded row sample of the same workload per step.
+
+Under torchrun each rank runs the whole workload on its own GPU (replicas,
+weak scaling): attention heads are independent and no data moves between GPUs.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import platform
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOP/s (bf16, B4 H16 S4096 d128 causal) and % of roofline"
+UNIT = "TFLOP/s"
+TC_SOURCES = ["attn_tc.cu", "tc_ptx.cuh"]
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "attn_tc_bf16_causal_b4h16s4096d128.md")
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="bf16_causal_b4h16s4096d128")
+    p.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle time budget of the CPU baseline")
+    p.add_argument("--reference-seconds", type=float, default=120.0,
+                   help="total oracle time budget of --impl reference")
+    p.add_argument("--e2e-steps", type=int, default=50)
+    p.add_argument("--no-triad", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args(argv)
+
+
+# ----------------------------------------------------------------------------- distributed
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = False
+
+    def init(self, backend: str):
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group(backend=backend)
+            self.pg = True
+
+    def barrier(self):
+        if self.pg:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+        import torch.distributed as dist
+        dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------- clocks
+CLOCK_FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+                "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+                "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+REASON_NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+
+class ClockSampler:
+    """nvidia-smi sampled every 100 ms in a background process; each line is
+    stamped with the host time it was read."""
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.samples: list[tuple[float, list[str]]] = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={','.join(CLOCK_FIELDS)}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float) -> dict:
+        inside = [s for t, s in self.samples if t0 <= t <= t1]
+        window = "timed region"
+        if not inside:  # the timed region was shorter than one sampling period
+            inside = [s for t, s in self.samples if t0 - 0.3 <= t <= t1 + 0.3]
+            window = "timed region +- 0.3 s"
+        out = {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": len(inside), "window": window}
+        sm, smax, power = [], [], []
+        reasons = set()
+        for s in inside:
+            try:
+                sm.append(float(s[1]))
+                smax.append(float(s[2]))
+                power.append(float(s[3]))
+            except (ValueError, IndexError):
+                continue
+            for name, val in zip(REASON_NAMES, s[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if sm:
+            out["sm_mhz"] = statistics.median(sm)
+            out["sm_max_mhz"] = max(smax)
+            out["power_w_max"] = max(power)
+        out["reasons"] = sorted(reasons)
+        return out
+
+
+def gpu_id_for_smi(device: int) -> str:
+    import torch
+    try:
+        uuid = str(torch.cuda.get_device_properties(device).uuid)
+        return uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        ids = [x for x in vis.split(",") if x.strip()]
+        return ids[device] if device < len(ids) else str(device)
+
+
+# ----------------------------------------------------------------------------- helpers
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in TC_SOURCES:
+        with open(os.path.join(ROOT, "roofline_benchmarking_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(expected_hash: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source; else None."""
+    try:
+        text = open(PROFILE_SUMMARY).read()
+    except OSError:
+        return None
+    mh = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    mt = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not mh or not mt or mh.group(1) != expected_hash:
+        return None
+    return float(mt.group(1))
+
+
+def host_cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        m = re.search(r"Model name:\s*(.+)", out)
+        if m:
+            return m.group(1).strip()
+    except Exception:
+        pass
+    return platform.processor() or platform.machine()
+
+
+def workload_config(w, extra=None) -> dict:
+    dist = (f"uniform[-1,1]" if w.dist == "uniform" else
+            f"Q,K normal(0,{w.sigma_qk:g}), V normal(0,{w.sigma_v:g})")
+    cfg = {"workload": w.name, "B": w.B, "H": w.H, "S": w.S, "d": w.d, "causal": w.causal,
+           "dtype": w.dtype, "seed": w.seed, "distribution": dist + (" rounded to bf16" if w.dtype == "bf16" else ""),
+           "scale": "1/sqrt(d)", "flops_per_step": w.flops}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def widen(q, k, v):
+    """Q, K, V as float64 numpy arrays (exact) for the oracle."""
+    import oracle
+    orc = oracle.get()
+    return tuple(orc._f64(t) for t in (q, k, v))
+
+
+def oracle_sample(w, q64, k64, v64, seconds: float, seed: int = 0, gpu_out=None):
+    """Rows of the workload evaluated by the oracle until `seconds` elapse.
+    q64, k64, v64 come from widen(). Returns (flops, elapsed, rows, parity or None)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from roofline_benchmarking_gb300 import inputs
+
+    heads, rows = inputs.sample_rows(w, per_head=64, seed=seed)
+    perm = torch.randperm(len(heads), generator=torch.Generator().manual_seed(seed))
+    heads, rows = heads[perm].numpy(), rows[perm].numpy()
+    orc = oracle.get()
+    done, flops, elapsed = 0, 0.0, 0.0
+    chunk = 4
+    outs = []
+    while done < len(heads) and elapsed < seconds:
+        h, r = heads[done:done + chunk], rows[done:done + chunk]
+        t0 = time.perf_counter()
+        o = orc.attn_rows(q64, k64, v64, w.causal, w.scale, h, r)
+        elapsed += time.perf_counter() - t0
+        outs.append(o)
+        vis = (r + 1) if w.causal else np.full(len(r), w.S)
+        flops += float(np.sum(4.0 * vis * w.d))
+        done += len(h)
+    parity = None
+    if gpu_out is not None and done:
+        got = gpu_out.view(w.N, w.S, w.d)[torch.from_numpy(heads[:done]).cuda(),
+                                           torch.from_numpy(rows[:done]).cuda()].float().cpu().numpy()
+        diff = np.abs(got - np.concatenate(outs))
+        parity = {"rows": int(done), "max_abs": float(diff.max()), "mean_abs": float(diff.mean())}
+    return flops, elapsed, int(done), parity
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args, d: Dist):
+    if d.rank != 0:
+        return 0
+    import numpy as np  # noqa: F401
+
+    from roofline_benchmarking_gb300 import inputs
+
+    w = inputs.WORKLOADS[args.workload]
+    q64, k64, v64 = widen(*inputs.make_qkv(w))
+    per_step = max(args.reference_seconds / max(args.steps + args.warmup, 1), 0.05)
+    for i in range(args.warmup):
+        oracle_sample(w, q64, k64, v64, per_step, seed=1000 + i)
+    tot_f, tot_t, tot_rows = 0.0, 0.0, 0
+    for i in range(args.steps):
+        f, t, n, _ = oracle_sample(w, q64, k64, v64, per_step, seed=i)
+        tot_f += f
+        tot_t += t
+        tot_rows += n
+    value = tot_f / tot_t / 1e12
+    sample = (f"{tot_rows} seeded (head, query) rows of {w.name} over {args.steps} steps "
+              f"(~{per_step:.2f} s of oracle time per step); single thread, float64")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_t / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w, {"rows_per_step": tot_rows / args.steps}),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample,
+                         "cpu": host_cpu_model()},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- our arm
+def triad_ceiling(kbattn, dev_info) -> dict:
+    """STREAM Triad over three 2 GiB fp32 arrays; the TileOPs protocol: 100
+    warm-up launches, then 5 runs of 200 timed launches, per block size."""
+    import torch
+
+    from roofline_benchmarking_gb300 import inputs
+    from roofline_benchmarking_gb300 import roofline as rf
+
+    n = inputs.TRIAD_N
+    a = torch.empty(n, dtype=torch.float32, device="cuda")
+    b = torch.ones(n, dtype=torch.float32, device="cuda")
+    c = torch.full((n,), 2.0, dtype=torch.float32, device="cuda")
+    nbytes = 3.0 * n * 4
+    best, per_block = 0.0, {}
+    for block in (128, 256, 512):
+        kbattn.kb_triad_bench(a, b, c, 3.0, block=block, warmup=100, iters=1)
+        runs = []
+        for _ in range(5):
+            ms = kbattn.kb_triad_bench(a, b, c, 3.0, block=block, warmup=0, iters=200)
+            runs.append(nbytes / (statistics.mean(ms) * 1e-3) / 1e9)
+        per_block[block] = {"best_gbs": max(runs), "median_gbs": statistics.median(runs)}
+        best = max(best, max(runs))
+    ok = bool((a[:1024] == 7.0).all())
+    theo = rf.theoretical_dram_gbs(dev_info["mem_clock_khz"] / 1e3, dev_info["mem_bus_width_bits"])
+    del a, b, c
+    torch.cuda.empty_cache()
+    return {"best_gbs": best, "per_block": per_block, "theoretical_gbs": theo,
+            "calibration": rf.calibration(best, theo), "bytes_per_launch": nbytes, "check_7": ok,
+            "theoretical_formula": "2 x memory clock x bus width / 8 (device attributes)"}
+
+
+def run_ours(args, d: Dist):
+    import torch
+
+    from roofline_benchmarking_gb300 import build as kb_build
+    from roofline_benchmarking_gb300 import inputs, kbattn
+    from roofline_benchmarking_gb300 import roofline as rf
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the attention library has no CPU path)")
+    torch.cuda.set_device(d.local_rank)
+    d.init("nccl")
+    kb_build.build()
+    kbattn.load()
+    w = inputs.WORKLOADS[args.workload]
+    dev = torch.cuda.current_device()
+    info = kbattn.kb_device_info(dev)
+    stream = torch.cuda.current_stream()
+
+    qh, kh, vh = inputs.make_qkv(w)
+    q, k, v = (t.cuda() for t in (qh, kh, vh))
+    o = torch.empty_like(q)
+    variant = kbattn.Variant.TC if w.dtype != "f32" else kbattn.Variant.FLASH
+
+    def step():
+        kbattn.kb_attn_fwd(q, k, v, o, causal=w.causal, scale=w.scale, variant=variant, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if kbattn.kb_check_device_error() != kbattn.Status.OK:
+        raise SystemExit("device error during warm-up")
+
+    sampler = ClockSampler(gpu_id_for_smi(dev))
+    sampler.start()
+    time.sleep(0.35)  # let the sampler attach before the timed region
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    t_begin = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    d.barrier()
+    torch.cuda.synchronize()
+    h0 = time.time()
+    t_begin.record(stream)
+    for i in range(K):
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    h1 = time.time()
+    d.barrier()
+    sampler.stop()
+    total_ms = t_begin.elapsed_time(t_end)
+    launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    if kbattn.kb_check_device_error() != kbattn.Status.OK:
+        raise SystemExit("device error in the timed region")
+    clocks = sampler.summary(h0, h1)
+
+    total_ms = d.max(total_ms)
+    ms_per_step = total_ms / K
+    value = w.flops * d.world / (ms_per_step * 1e-3) / 1e12
+
+    peaks, src = rf.load_measured_peaks()
+    mean_launch_s = statistics.mean(launch_ms) * 1e-3
+    achieved = w.flops / mean_launch_s / 1e12
+    intensity = w.flops / w.io_bytes
+    roof = {
+        "kernel": "attn_tc_kernel<128,bf16>", "bound": "tensor", "achieved": achieved,
+        "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+        "peak_source": f"{src} bf16 burst (cuBLAS 8192^3)",
+        "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
+        "traffic": None, "algorithmic_flops_per_launch": w.flops, "algorithmic_bytes_per_launch": w.io_bytes,
+        "intensity_flop_per_byte": intensity,
+        "attainable": rf.attainable(intensity, peaks["bf16_tflops"] * 1e3, peaks["hbm_gbs"]) / 1e3,
+        "launch_ms": {"mean": statistics.mean(launch_ms), "p50": statistics.median(launch_ms),
+                      "min": min(launch_ms), "p99": sorted(launch_ms)[int(0.99 * (K - 1))]},
+        "timing": "CUDA events around each launch on the launching stream",
+    }
+    traffic = profiled_traffic(kernel_source_hash())
+    if traffic is not None:
+        roof["traffic"] = traffic
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": d.world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == "bf16" else w.dtype, "data": "synthetic",
+        "config": workload_config(w, {
+            "l2": f"no flush: inputs+output {w.io_bytes / 2**20:.0f} MiB > L2 {info['l2_bytes'] / 2**20:.0f} MiB",
+            "parallelism": f"replicas x{d.world} (each GPU runs the whole workload; no collective)",
+            "variant": variant.name, "device": info["name"], "sms": info["sm_count"]}),
+        "clocks": clocks, "gpu_launches": K, "roofline": roof,
+    }
+
+    if not args.no_e2e:
+        line["e2e"] = e2e_rate(args, w, qh, kh, vh, q, k, v, o, variant, stream, d)
+
+    if d.rank == 0 and not args.no_triad and d.world == 1:
+        line["triad"] = triad_ceiling(kbattn, info)
+
+    if d.rank == 0 and d.world == 1 and not args.no_cpu_baseline:
+        f, t, n, parity = oracle_sample(w, *widen(qh, kh, vh), args.cpu_seconds, seed=0, gpu_out=o)
+        line["cpu_baseline"] = {
+            "value": f / t / 1e12, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n} seeded (head, query) rows of {w.name} ({t:.1f} s, single thread, float64)",
+            "cpu": host_cpu_model(), "parity_of_sampled_rows": parity}
+
+    if d.rank == 0:
+        print(json.dumps(line), flush=True)
+    d.close()
+    return 0
+
+
+def e2e_rate(args, w, qh, kh, vh, q, k, v, o, variant, stream, d: Dist) -> dict:
+    """The same metric through the public API with pinned host buffers: every
+    step copies Q, K, V host->device, runs kb_attn_fwd and reads O back."""
+    import torch
+
+    from roofline_benchmarking_gb300 import kbattn
+
+    qp, kp, vp = (t.pin_memory() for t in (qh, kh, vh))
+    op = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+
+    def step():
+        q.copy_(qp, non_blocking=True)
+        k.copy_(kp, non_blocking=True)
+        v.copy_(vp, non_blocking=True)
+        kbattn.kb_attn_fwd(q, k, v, o, causal=w.causal, scale=w.scale, variant=variant, stream=stream)
+        op.copy_(o, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    K = max(args.e2e_steps, 1)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    d.barrier()
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for _ in range(K):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    d.barrier()
+    ms = d.max(t0.elapsed_time(t1)) / K
+    h2d = sum(t.numel() * t.element_size() for t in (qp, kp, vp))
+    d2h = op.numel() * op.element_size()
+    return {"value": w.flops * d.world / (ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": K, "host_buffers": "pinned"}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    d = Dist()
+    if args.impl == "reference":
+        return run_reference(args, d)
+    return run_ours(args, d)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -6,20 +6,23 @@
 // through in tiles, a running max m and denominator l are kept per query row,
 // the score matrix is never materialised). It is laid out for GB300:
 //
-//  * one CTA per (head, 128-row query tile), heaviest causal tiles first;
-//  * warp 4 (one lane) stages the Q tile and a ring of K and V tiles with TMA
+//  * one CTA per (head, pair of 128-row query tiles A and B), heaviest causal
+//    pairs first; the two tiles share every K and V tile the CTA loads;
+//  * warp 8 (one lane) stages both Q tiles and rings of K and V tiles with TMA
 //    (128-byte swizzle, 3-D tensor maps [N, S, d], rows past S zero-filled);
-//  * warp 5 (one lane) issues tcgen05 MMAs: S = Q K^T into one of two
-//    128x128 fp32 TMEM buffers, and O += P V into a 128 x d fp32 TMEM
-//    accumulator; completion is signalled through mbarriers by tcgen05.commit;
-//  * warps 0-3 own one query row per thread (TMEM lane = row): they load the
-//    score row from TMEM, apply scale and causal/tail masks, update the
-//    running max (in base 2, scale*log2(e) folded into one FMA), write
-//    P = exp2(s - m) as bf16/f16 into shared memory in the MMA operand layout,
-//    and rescale O in TMEM only when the row max grew by more than 2^8
-//    (the final O / l is exact either way);
-//  * the S MMA of tile j+1 runs while the softmax of tile j does, and P V of
-//    tile j is issued as soon as P_j is written.
+//  * warp 9 (one lane) issues the tcgen05 MMAs: S = Q K^T from shared memory
+//    into a 128x128 fp32 TMEM tile per query tile, and O += P V with P read
+//    from TMEM and V from shared memory into a 128 x d fp32 TMEM accumulator
+//    per query tile; completion is signalled by tcgen05.commit on mbarriers;
+//  * warps 0-3 (tile A) and 4-7 (tile B) own one query row per thread (TMEM
+//    lane = row): they load the score row from TMEM, apply scale and the
+//    causal/tail masks, update the running max in base 2 (scale*log2(e) in one
+//    FMA), write P = exp2(s - m) as 16-bit pairs back into the first 64 columns
+//    of the score tile, and rescale O in TMEM only when the row max grew by
+//    more than 8 (factor 256; the final O / l is exact either way);
+//  * the MMA order PV_A(j), S_A(j+1), PV_B(j), S_B(j+1) keeps the tensor core on
+//    one tile while the other tile's softmax runs. S_A(j+1) overwrites P_A(j)
+//    only after PV_A(j) has read it: MMAs issued by one thread execute in order.
 // Every mbarrier wait is bounded by %globaltimer; a wait that runs out sets the
 // library's device error word and an abort flag, every role then leaves its
 // loop, waits (bounded) for its own TMA copies and MMAs in flight, and the
@@ -43,7 +46,16 @@ namespace {
 
 constexpr int kBM = 128;  // query rows per tile (TMEM lanes)
 constexpr int kBN = 128;  // keys per tile
-constexpr int kThreadsTC = 192;
+constexpr int kPairRows = 2 * kBM;
+// Three warpgroups: 0 and 1 run the softmax of tiles A and B; in the third,
+// warp 8 drives TMA and warp 9 issues MMAs (warps 10 and 11 only hand their
+// registers over). Launch budget 384 x 168 = 64512 registers, rebalanced as
+// 2 x 128 x 224 + 128 x 56 = 64512.
+constexpr int kThreadsTC = 384;
+constexpr int kWarpTMA = 8;
+constexpr int kWarpMMA = 9;
+constexpr int kRegsSoftmax = 224;
+constexpr int kRegsControl = 56;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColBlock = 16384;  // one 128-row x 128-byte swizzled block
 constexpr unsigned long long kDefaultWaitLimitNs = 1000000000ull;
@@ -51,41 +63,37 @@ constexpr unsigned long long kDefaultWaitLimitNs = 1000000000ull;
 template <int D>
 struct TcCfg {
   static_assert(D == 64 || D == 128, "tensor-core path supports d = 64 and 128");
-  static constexpr int DB = D / 64;          // 128-byte column blocks per tile row
-  static constexpr int TILE = kBM * D * 2;   // bytes of a Q, K or V tile
-  static constexpr int PTILE = kBM * kBN * 2;
+  static constexpr int DB = D / 64;           // 128-byte column blocks per tile row
+  static constexpr int TILE = kBM * D * 2;    // bytes of a Q, K or V tile
   static constexpr int KS = D == 128 ? 2 : 3;  // K ring stages
   static constexpr int VS = D == 128 ? 2 : 3;  // V ring stages
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + TILE;
+  static constexpr int OFF_Q = 0;              // Q_A then Q_B
+  static constexpr int OFF_K = OFF_Q + 2 * TILE;
   static constexpr int OFF_V = OFF_K + KS * TILE;
-  static constexpr int OFF_P = OFF_V + VS * TILE;
-  static constexpr int OFF_BAR = OFF_P + 2 * PTILE;
+  static constexpr int OFF_BAR = OFF_V + VS * TILE;
   enum {
     B_Q = 0,
     B_KFULL = 1,
     B_KEMPTY = B_KFULL + KS,
     B_VFULL = B_KEMPTY + KS,
     B_VEMPTY = B_VFULL + VS,
-    B_SFULL = B_VEMPTY + VS,
-    B_SFREE = B_SFULL + 2,
-    B_PFULL = B_SFREE + 2,
-    B_PFREE = B_PFULL + 2,
-    B_ODONE = B_PFREE + 2,
-    B_OFINAL = B_ODONE + 1,
-    B_DRAIN = B_OFINAL + 1,
+    B_SFULL = B_VEMPTY + VS,  // [2]: S of tile A / B computed
+    B_PFULL = B_SFULL + 2,    // [2]: P of tile A / B written (and O rescaled)
+    B_OFINAL = B_PFULL + 2,   // [2]: last P V of tile A / B done
+    B_DRAIN = B_OFINAL + 2,
     NBAR = B_DRAIN + 1
   };
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // [0] TMEM base, [1] abort flag
   static constexpr int BYTES = OFF_MISC + 16;
   static constexpr int SMEM = BYTES + 1024;  // slack to align the base to 1024 bytes
-  // TMEM columns: S buffers at 0 and 128, O at 256.
-  static constexpr uint32_t TM_O = 256;
+  // TMEM columns of tile g: S (and P in its first 64 columns) at 128 g, O at 256 + 128 g.
+  __host__ __device__ static constexpr uint32_t tm_s(int g) { return 128u * (uint32_t)g; }
+  __host__ __device__ static constexpr uint32_t tm_o(int g) { return 256u + 128u * (uint32_t)g; }
 };
 
 // Bounded wait on phase `parity` of `bar`. Gives up when the abort flag is set
 // (if `honor_abort`) or after `limit` ns, recording the timeout.
-__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                       unsigned long long limit, bool honor_abort) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer();
@@ -110,12 +118,12 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 }
 
 template <bool F16>
-__device__ __forceinline__ uint32_t pack2(float a, float b) {
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   if constexpr (F16) {
-    __half2 h = __floats2half2_rn(a, b);
+    __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);
   } else {
-    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);
   }
 }
@@ -138,11 +146,15 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::OFF_MISC + 4);
   auto bar = [&](int i) -> uint32_t { return base + C::OFF_BAR + 8u * (uint32_t)i; };
 
-  const int ntiles = (S + kBM - 1) / kBM;
+  // Work item: query rows [q0, q0 + 256) of head n, as tiles A and B.
+  const int npairs = (S + kPairRows - 1) / kPairRows;
+  const int nkv_all = (S + kBN - 1) / kBN;
   const int n = (int)(blockIdx.x % (unsigned)N);
-  const int qt = ntiles - 1 - (int)(blockIdx.x / (unsigned)N);
-  const int q0 = qt * kBM;
-  const int nkv = causal ? qt + 1 : ntiles;
+  const int t = npairs - 1 - (int)(blockIdx.x / (unsigned)N);
+  const int q0 = t * kPairRows;
+  // key tiles each query tile visits (tile B is never shorter than tile A)
+  const int nA = causal ? min(2 * t + 1, nkv_all) : nkv_all;
+  const int nB = causal ? min(2 * t + 2, nkv_all) : nkv_all;
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -155,18 +167,15 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       ptx::mbar_init(bar(C::B_VFULL + s), 1);
       ptx::mbar_init(bar(C::B_VEMPTY + s), 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      ptx::mbar_init(bar(C::B_SFULL + s), 1);
-      ptx::mbar_init(bar(C::B_SFREE + s), 4 * 32);
-      ptx::mbar_init(bar(C::B_PFULL + s), 4 * 32);
-      ptx::mbar_init(bar(C::B_PFREE + s), 1);
+    for (int g = 0; g < 2; ++g) {
+      ptx::mbar_init(bar(C::B_SFULL + g), 1);
+      ptx::mbar_init(bar(C::B_PFULL + g), 4 * 32);
+      ptx::mbar_init(bar(C::B_OFINAL + g), 1);
     }
-    ptx::mbar_init(bar(C::B_ODONE), 1);
-    ptx::mbar_init(bar(C::B_OFINAL), 1);
     ptx::mbar_init(bar(C::B_DRAIN), 1);
     ptx::fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == kWarpMMA) {
     ptx::tmem_alloc(base + C::OFF_MISC, kTmemCols);
     ptx::tmem_relinquish();
   }
@@ -175,129 +184,166 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + C::OFF_MISC);
 
-  if (warp == 4) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      ptx::tma_prefetch_desc(&tmq);
-      ptx::tma_prefetch_desc(&tmk);
-      ptx::tma_prefetch_desc(&tmv);
-      ptx::mbar_arrive_expect_tx(bar(C::B_Q), C::TILE);
-      for (int b = 0; b < C::DB; ++b)
-        ptx::tma_load_3d(base + C::OFF_Q + b * kColBlock, &tmq, bar(C::B_Q), b * 64, q0, n);
-      int kdone = 0, vdone = 0;  // loads issued
-      bool ok = true;
-      for (int j = 0; j < nkv && ok; ++j) {
-        const int ks = j % C::KS, vs = j % C::VS;
-        if (j >= C::KS) ok = wait_bar(bar(C::B_KEMPTY + ks), ((j / C::KS) & 1) ^ 1, abort_flag, limit, true);
-        if (!ok) break;
-        ptx::mbar_arrive_expect_tx(bar(C::B_KFULL + ks), C::TILE);
-        for (int b = 0; b < C::DB; ++b)
-          ptx::tma_load_3d(base + C::OFF_K + ks * C::TILE + b * kColBlock, &tmk, bar(C::B_KFULL + ks), b * 64,
-                           j * kBN, n);
-        kdone = j + 1;
-        if (j >= C::VS) ok = wait_bar(bar(C::B_VEMPTY + vs), ((j / C::VS) & 1) ^ 1, abort_flag, limit, true);
-        if (!ok) break;
-        ptx::mbar_arrive_expect_tx(bar(C::B_VFULL + vs), C::TILE);
-        for (int b = 0; b < C::DB; ++b)
-          ptx::tma_load_3d(base + C::OFF_V + vs * C::TILE + b * kColBlock, &tmv, bar(C::B_VFULL + vs), b * 64,
-                           j * kBN, n);
-        vdone = j + 1;
-      }
-      // Every copy this CTA started must land before the CTA exits.
-      wait_bar(bar(C::B_Q), 0, abort_flag, limit, false);
-      for (int j = kdone - C::KS < 0 ? 0 : kdone - C::KS; j < kdone; ++j)
-        wait_bar(bar(C::B_KFULL + j % C::KS), (j / C::KS) & 1, abort_flag, limit, false);
-      for (int j = vdone - C::VS < 0 ? 0 : vdone - C::VS; j < vdone; ++j)
-        wait_bar(bar(C::B_VFULL + j % C::VS), (j / C::VS) & 1, abort_flag, limit, false);
-    }
-    __syncwarp();
-  } else if (warp == 5) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      bool ok = wait_bar(bar(C::B_Q), 0, abort_flag, limit, true);
-      auto issue_pv = [&](int t) -> bool {
-        const int pb = t & 1, vs = t % C::VS;
-        if (!wait_bar(bar(C::B_VFULL + vs), (t / C::VS) & 1, abort_flag, limit, true)) return false;
-        if (!wait_bar(bar(C::B_PFULL + pb), (t >> 1) & 1, abort_flag, limit, true)) return false;
-        ptx::tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint64_t a = ptx::sw128_desc(
-              base + C::OFF_P + pb * C::PTILE + (kk >> 2) * kColBlock + (kk & 3) * 32, 16, 1024);
-          const uint64_t b = ptx::sw128_desc(base + C::OFF_V + vs * C::TILE + kk * 16 * 128, kColBlock, 1024);
-          ptx::mma_f16_ss(tmem + C::TM_O, a, b, IDESC_PV, (t > 0 || kk > 0) ? 1u : 0u);
+  if (warp >= kWarpTMA) {
+    ptx::regs_decrease<kRegsControl>();
+    if (warp == kWarpTMA) {
+      // ------------------------------------------------------------ TMA producer
+      if (lane == 0) {
+        ptx::tma_prefetch_desc(&tmq);
+        ptx::tma_prefetch_desc(&tmk);
+        ptx::tma_prefetch_desc(&tmv);
+        ptx::mbar_arrive_expect_tx(bar(C::B_Q), 2 * C::TILE);
+        for (int g = 0; g < 2; ++g)
+          for (int b = 0; b < C::DB; ++b)
+            ptx::tma_load_3d(base + C::OFF_Q + g * C::TILE + b * kColBlock, &tmq, bar(C::B_Q), b * 64,
+                             q0 + g * kBM, n);
+        int kdone = 0, vdone = 0;  // loads issued
+        bool ok = true;
+        for (int j = 0; j < nB && ok; ++j) {
+          const int ks = j % C::KS, vs = j % C::VS;
+          if (j >= C::KS) ok = wait_bar(bar(C::B_KEMPTY + ks), ((j / C::KS) & 1) ^ 1, abort_flag, limit, true);
+          if (!ok) break;
+          ptx::mbar_arrive_expect_tx(bar(C::B_KFULL + ks), C::TILE);
+          for (int b = 0; b < C::DB; ++b)
+            ptx::tma_load_3d(base + C::OFF_K + ks * C::TILE + b * kColBlock, &tmk, bar(C::B_KFULL + ks), b * 64,
+                             j * kBN, n);
+          kdone = j + 1;
+          if (j >= C::VS) ok = wait_bar(bar(C::B_VEMPTY + vs), ((j / C::VS) & 1) ^ 1, abort_flag, limit, true);
+          if (!ok) break;
+          ptx::mbar_arrive_expect_tx(bar(C::B_VFULL + vs), C::TILE);
+          for (int b = 0; b < C::DB; ++b)
+            ptx::tma_load_3d(base + C::OFF_V + vs * C::TILE + b * kColBlock, &tmv, bar(C::B_VFULL + vs), b * 64,
+                             j * kBN, n);
+          vdone = j + 1;
         }
-        ptx::mma_commit(bar(C::B_ODONE));
-        ptx::mma_commit(bar(C::B_VEMPTY + vs));
-        ptx::mma_commit(bar(C::B_PFREE + pb));
-        return true;
-      };
-      for (int j = 0; j < nkv && ok; ++j) {
-        const int sb = j & 1, ks = j % C::KS;
-        ok = wait_bar(bar(C::B_KFULL + ks), (j / C::KS) & 1, abort_flag, limit, true);
-        if (ok && j >= 2) ok = wait_bar(bar(C::B_SFREE + sb), ((j >> 1) - 1) & 1, abort_flag, limit, true);
-        if (!ok) break;
-        ptx::tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kColBlock + (kk & 3) * 32;
-          const uint64_t a = ptx::sw128_desc(base + C::OFF_Q + off, 16, 1024);
-          const uint64_t b = ptx::sw128_desc(base + C::OFF_K + ks * C::TILE + off, 16, 1024);
-          ptx::mma_f16_ss(tmem + (uint32_t)sb * kBN, a, b, IDESC_QK, kk > 0 ? 1u : 0u);
-        }
-        ptx::mma_commit(bar(C::B_SFULL + sb));
-        ptx::mma_commit(bar(C::B_KEMPTY + ks));
-        if (j >= 1) ok = issue_pv(j - 1);
+        // Every copy this CTA started must land before the CTA exits.
+        wait_bar(bar(C::B_Q), 0, abort_flag, limit, false);
+        for (int j = kdone - C::KS < 0 ? 0 : kdone - C::KS; j < kdone; ++j)
+          wait_bar(bar(C::B_KFULL + j % C::KS), (j / C::KS) & 1, abort_flag, limit, false);
+        for (int j = vdone - C::VS < 0 ? 0 : vdone - C::VS; j < vdone; ++j)
+          wait_bar(bar(C::B_VFULL + j % C::VS), (j / C::VS) & 1, abort_flag, limit, false);
       }
-      if (ok) ok = issue_pv(nkv - 1);
-      if (ok) ptx::mma_commit(bar(C::B_OFINAL));
-      // No MMA may still be running when the tensor memory is released.
-      ptx::mma_commit(bar(C::B_DRAIN));
-      wait_bar(bar(C::B_DRAIN), 0, abort_flag, limit, false);
+      __syncwarp();
+    } else if (warp == kWarpMMA) {
+      // ------------------------------------------------------------ MMA issuer
+      if (lane == 0) {
+        // S_g = Q_g K_j^T (K-major operands, both from shared memory)
+        auto issue_s = [&](int g, int ks) {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kColBlock + (kk & 3) * 32;
+            const uint64_t a = ptx::sw128_desc(base + C::OFF_Q + g * C::TILE + off, 16, 1024);
+            const uint64_t b = ptx::sw128_desc(base + C::OFF_K + ks * C::TILE + off, 16, 1024);
+            ptx::mma_f16_ss(tmem + C::tm_s(g), a, b, IDESC_QK, kk > 0 ? 1u : 0u);
+          }
+          ptx::mma_commit(bar(C::B_SFULL + g));
+        };
+        // O_g += P_g V_j (P from TMEM, V MN-major from shared memory)
+        auto issue_pv = [&](int g, int vs, bool first) {
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk) {
+            const uint64_t b = ptx::sw128_desc(base + C::OFF_V + vs * C::TILE + kk * 16 * 128, kColBlock, 1024);
+            ptx::mma_f16_ts(tmem + C::tm_o(g), tmem + C::tm_s(g) + kk * 8, b, IDESC_PV, (!first || kk > 0) ? 1u : 0u);
+          }
+        };
+        bool ok = wait_bar(bar(C::B_Q), 0, abort_flag, limit, true);
+        if (ok) ok = wait_bar(bar(C::B_KFULL), 0, abort_flag, limit, true);
+        if (ok) {
+          ptx::tc_fence_after();
+          issue_s(0, 0);
+          issue_s(1, 0);
+          ptx::mma_commit(bar(C::B_KEMPTY));
+        }
+        for (int j = 0; j < nB && ok; ++j) {
+          const int vs = j % C::VS;
+          const int jn = j + 1, ksn = jn % C::KS;
+          ok = wait_bar(bar(C::B_VFULL + vs), (j / C::VS) & 1, abort_flag, limit, true);
+          if (ok && j < nA) {  // tile A
+            ok = wait_bar(bar(C::B_PFULL + 0), j & 1, abort_flag, limit, true);
+            if (ok) {
+              ptx::tc_fence_after();
+              issue_pv(0, vs, j == 0);
+              if (jn < nA) {
+                ok = wait_bar(bar(C::B_KFULL + ksn), (jn / C::KS) & 1, abort_flag, limit, true);
+                if (ok) {
+                  ptx::tc_fence_after();
+                  issue_s(0, ksn);
+                }
+              } else {
+                ptx::mma_commit(bar(C::B_OFINAL + 0));
+              }
+            }
+          }
+          if (ok) ok = wait_bar(bar(C::B_PFULL + 1), j & 1, abort_flag, limit, true);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          issue_pv(1, vs, j == 0);  // tile B
+          ptx::mma_commit(bar(C::B_VEMPTY + vs));
+          if (jn < nB) {
+            ok = wait_bar(bar(C::B_KFULL + ksn), (jn / C::KS) & 1, abort_flag, limit, true);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            issue_s(1, ksn);
+            ptx::mma_commit(bar(C::B_KEMPTY + ksn));
+          } else {
+            ptx::mma_commit(bar(C::B_OFINAL + 1));
+          }
+        }
+        // No MMA may still be running when the tensor memory is released.
+        ptx::mma_commit(bar(C::B_DRAIN));
+        wait_bar(bar(C::B_DRAIN), 0, abort_flag, limit, false);
+      }
+      __syncwarp();
     }
-    __syncwarp();
   } else {
-    // ------------------------------------------------------------ softmax, warps 0-3
-    const int r = warp * 32 + lane;  // row within the tile = TMEM lane
-    const int row = q0 + r;
-    const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
+    ptx::regs_increase<kRegsSoftmax>();
+    // ------------------------------------------------------------ softmax, warps 0-7
+    const int g = warp >> 2;  // query tile of this warpgroup
+    const int wq = warp & 3;  // TMEM lane quarter
+    const int r = wq * 32 + lane;
+    const int row = q0 + g * kBM + r;
+    const int nj = g ? nB : nA;
+    const int diag = 2 * t + g;  // the key tile on the diagonal (causal)
+    const uint32_t tl = tmem + ((uint32_t)(wq * 32) << 16);
+    const uint32_t ts = tl + C::tm_s(g), to = tl + C::tm_o(g);
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
-    for (int j = 0; j < nkv; ++j) {
-      const int sb = j & 1;
-      if (!(ok = warp_wait(bar(C::B_SFULL + sb), (j >> 1) & 1, abort_flag, limit))) break;
+    for (int j = 0; j < nj; ++j) {
+      if (!(ok = warp_wait(bar(C::B_SFULL + g), j & 1, abort_flag, limit))) break;
       ptx::tc_fence_after();
       float s[kBN];
       {
-        uint32_t u[32];
+        uint32_t u0[32], u1[32], u2[32], u3[32];
+        ptx::tmem_ld32(ts + 0, u0);
+        ptx::tmem_ld32(ts + 32, u1);
+        ptx::tmem_ld32(ts + 64, u2);
+        ptx::tmem_ld32(ts + 96, u3);
+        ptx::tmem_wait_ld();
 #pragma unroll
-        for (int cb = 0; cb < kBN / 32; ++cb) {
-          ptx::tmem_ld32(tl + (uint32_t)sb * kBN + cb * 32, u);
-          ptx::tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) s[cb * 32 + e] = __uint_as_float(u[e]);
+        for (int e = 0; e < 32; ++e) {
+          s[e] = __uint_as_float(u0[e]);
+          s[32 + e] = __uint_as_float(u1[e]);
+          s[64 + e] = __uint_as_float(u2[e]);
+          s[96 + e] = __uint_as_float(u3[e]);
         }
       }
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(C::B_SFREE + sb));
-
       const int k0 = j * kBN;
-      if ((causal && j == qt) || k0 + kBN > S) {
+      if ((causal && j == diag) || k0 + kBN > S) {
+        const int lim = min(causal ? row - k0 : kBN - 1, S - 1 - k0);  // last visible column
 #pragma unroll
-        for (int c = 0; c < kBN; ++c) {
-          const int key = k0 + c;
-          if (key >= S || (causal && key > row)) s[c] = -INFINITY;
-        }
+        for (int c = 0; c < kBN; ++c)
+          if (c > lim) s[c] = -INFINITY;
       }
-      float mx[4] = {s[0], s[1], s[2], s[3]};
+      float mx[8];
 #pragma unroll
-      for (int c = 4; c < kBN; c += 4) {
-        mx[0] = fmaxf(mx[0], s[c]);
-        mx[1] = fmaxf(mx[1], s[c + 1]);
-        mx[2] = fmaxf(mx[2], s[c + 2]);
-        mx[3] = fmaxf(mx[3], s[c + 3]);
-      }
-      const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * scale_log2;
+      for (int e = 0; e < 8; ++e) mx[e] = s[e];
+#pragma unroll
+      for (int c = 8; c < kBN; c += 8)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mx[e] = fmaxf(mx[e], s[c + e]);
+      const float m_tile =
+          fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) *
+          scale_log2;
       float alpha = 1.f;
       bool corr = false;
       if (j == 0) {
@@ -308,46 +354,43 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         l_run *= alpha;
         corr = true;
       }
-      if (j >= 2 && !(ok = warp_wait(bar(C::B_PFREE + sb), ((j >> 1) - 1) & 1, abort_flag, limit))) break;
-
-      // P = exp2(s*scale_log2 - m) -> 16-bit, stored K-major with the 128-byte swizzle
-      const float neg_m = -m_run;
-      float sum = 0.f;
-      const uint32_t prow = base + C::OFF_P + sb * C::PTILE + (uint32_t)r * 128;
-#pragma unroll
-      for (int c16 = 0; c16 < kBN / 8; ++c16) {
-        float p[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          p[e] = ptx::ex2(fmaf(s[c16 * 8 + e], scale_log2, neg_m));
-          sum += p[e];
-        }
-        const uint32_t addr = prow + (c16 >> 3) * kColBlock + ((uint32_t)((c16 & 7) ^ (r & 7)) << 4);
-        ptx::st_shared_v4(addr, pack2<F16>(p[0], p[1]), pack2<F16>(p[2], p[3]), pack2<F16>(p[4], p[5]),
-                          pack2<F16>(p[6], p[7]));
-      }
-      l_run += sum;
-      ptx::fence_proxy_async_smem();
-
       if (__any_sync(0xffffffffu, corr)) {
-        // O holds P V of tiles < j; it must be complete before it is rescaled
-        if (!(ok = warp_wait(bar(C::B_ODONE), (j - 1) & 1, abort_flag, limit))) break;
-        ptx::tc_fence_after();
+        // S_g(j) completing implies P V of tile j-1 has completed (one issuing
+        // thread, in-order commits), so O holds exactly tiles < j here.
         uint32_t u[32];
 #pragma unroll
         for (int cb = 0; cb < D / 32; ++cb) {
-          ptx::tmem_ld32(tl + C::TM_O + cb * 32, u);
+          ptx::tmem_ld32(to + cb * 32, u);
           ptx::tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * alpha);
-          ptx::tmem_st32(tl + C::TM_O + cb * 32, u);
+          ptx::tmem_st32(to + cb * 32, u);
         }
-        ptx::tmem_wait_st();
       }
+      // P = exp2(s * scale_log2 - m) as 16-bit pairs into columns [0, 64) of S
+      const float neg_m = -m_run;
+      float sum[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) sum[e] = 0.f;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const float p0 = ptx::ex2(fmaf(s[h * 64 + 2 * c], scale_log2, neg_m));
+          const float p1 = ptx::ex2(fmaf(s[h * 64 + 2 * c + 1], scale_log2, neg_m));
+          sum[(2 * c) & 7] += p0;
+          sum[(2 * c + 1) & 7] += p1;
+          pk[c] = pack2<F16>(p0, p1);
+        }
+        ptx::tmem_st32(ts + h * 32, pk);
+      }
+      l_run += ((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7]));
+      ptx::tmem_wait_st();
       ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(C::B_PFULL + sb));
+      ptx::mbar_arrive(bar(C::B_PFULL + g));
     }
-    if (ok) ok = warp_wait(bar(C::B_OFINAL), 0, abort_flag, limit);
+    if (ok) ok = warp_wait(bar(C::B_OFINAL + g), 0, abort_flag, limit);
     if (ok) {
       ptx::tc_fence_after();
       const float inv = 1.0f / l_run;
@@ -355,7 +398,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       uint32_t u[32];
 #pragma unroll
       for (int cb = 0; cb < D / 32; ++cb) {
-        ptx::tmem_ld32(tl + C::TM_O + cb * 32, u);
+        ptx::tmem_ld32(to + cb * 32, u);
         ptx::tmem_wait_ld();
         if (row < S) {
 #pragma unroll
@@ -374,7 +417,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
 
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kWarpMMA) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, kTmemCols);
   }
@@ -438,8 +481,8 @@ cudaError_t tc_launch(const AttnProblem& p, cudaStream_t st) {
   if (!make_map(&mq, p.q, p.N, p.S, D, F16) || !make_map(&mk, p.k, p.N, p.S, D, F16) ||
       !make_map(&mv, p.v, p.N, p.S, D, F16))
     return cudaErrorInvalidValue;
-  const int64_t tiles = (p.S + kBM - 1) / kBM;
-  attn_tc_kernel<D, F16><<<(unsigned)(tiles * p.N), kThreadsTC, C::SMEM, st>>>(
+  const int64_t pairs = (p.S + kPairRows - 1) / kPairRows;
+  attn_tc_kernel<D, F16><<<(unsigned)(pairs * p.N), kThreadsTC, C::SMEM, st>>>(
       mq, mk, mv, static_cast<uint8_t*>(p.o), (int)p.N, p.S, p.causal, p.scale * 1.4426950408889634f,
       kDefaultWaitLimitNs);
   return cudaGetLastError();
