@@ -241,7 +241,7 @@ def oracle_sample(w, q64, k64, v64, seconds: float, seed: int = 0, gpu_out=None)
     import oracle
     from roofline_benchmarking_gb300 import inputs
 
-    heads, rows = inputs.sample_rows(w, per_head=64, seed=seed)
+    heads, rows = inputs.sample_rows(w, per_head=min(w.S, 512), seed=seed)
     perm = torch.randperm(len(heads), generator=torch.Generator().manual_seed(seed))
     heads, rows = heads[perm].numpy(), rows[perm].numpy()
     orc = oracle.get()
