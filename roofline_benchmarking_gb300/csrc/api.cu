@@ -49,6 +49,9 @@ int validate(const void* q, const void* k, const void* v, const void* o, int B, 
   if (var == KB_FUSED && N * S > grid_limit) return KB_ERR_UNSUPPORTED;
   if ((var == KB_FLASH || var == KB_NAIVE) && N * ((S + 63) / 64) > grid_limit) return KB_ERR_UNSUPPORTED;
   if (var == KB_NAIVE && N > 65535) return KB_ERR_UNSUPPORTED;  // grid.z of the score pass
+  if (var == KB_NAIVE && (S + 63) / 64 > 65535) return KB_ERR_UNSUPPORTED;  // grid.y of the score pass
+  // the naive score matrix, N*S*S fp32, must be addressable
+  if (var == KB_NAIVE && N > lim / S / S) return KB_ERR_INVALID_ARG;
   *resolved = var;
   return KB_OK;
 }
@@ -194,6 +197,13 @@ int time_calls(Call call, cudaStream_t cs, int warmup, int iters, float* ms) {
 }  // namespace
 
 void set_last_cuda_error(cudaError_t e) { t_last_cuda_error = (int)e; }
+
+int validate_attention(const void* q, const void* k, const void* v, const void* o, int B, int H, int S, int d,
+                       int causal, float scale, int dtype, int variant, int* resolved) {
+  return validate(q, k, v, o, B, H, S, d, causal, scale, dtype, variant, resolved);
+}
+
+int check_current_device() { return check_device(); }
 
 }  // namespace kb
 

@@ -45,4 +45,9 @@ cudaError_t launch_selftest_timeout(unsigned long long limit_ns, cudaStream_t st
 // Per-thread record of the last CUDA error returned as KB_ERR_CUDA.
 void set_last_cuda_error(cudaError_t e);
 
+// The API layer's argument validation (no CUDA call) and device gate.
+int validate_attention(const void* q, const void* k, const void* v, const void* o, int B, int H, int S, int d,
+                       int causal, float scale, int dtype, int variant, int* resolved);
+int check_current_device();
+
 }  // namespace kb

@@ -81,6 +81,7 @@ def attn(q=FAKE, k=FAKE, v=FAKE, o=FAKE, B=1, H=1, S=64, d=64, causal=0, scale=0
     (dict(variant=9), Status.INVALID_ARG),
     (dict(B=1 << 20, H=1 << 20, S=1 << 20, d=64), Status.INVALID_ARG),   # B*H overflows int32
     (dict(B=1 << 15, H=1 << 15, S=1 << 30, d=128), Status.INVALID_ARG),  # bytes overflow int64
+    (dict(B=2, H=1, S=(1 << 31) - 1, d=32, variant=Variant.NAIVE), Status.UNSUPPORTED),  # score grid
     (dict(d=48), Status.UNSUPPORTED),
     (dict(d=256), Status.UNSUPPORTED),
     (dict(dtype=DType.F32, variant=Variant.TC), Status.UNSUPPORTED),
@@ -111,6 +112,8 @@ def test_naive_workspace_contract(lib):
         assert kbattn.kb_attn_workspace_bytes(1, 8, 1024, 64, DType.F32, v) == 0
     assert kbattn.kb_attn_workspace_bytes(1, 8, 1024, 64, DType.BF16, Variant.TC) == 0
     assert kbattn.kb_attn_workspace_bytes(0, 8, 1024, 64, DType.F32, Variant.NAIVE) == 0
+    # a score matrix too large to address is refused, never a wrapped-around size
+    assert kbattn.kb_attn_workspace_bytes(2, 1, (1 << 31) - 1, 32, DType.F32, Variant.NAIVE) == 0
     # too small a workspace is refused before the device is touched
     st = kbattn.load().kb_attn_fwd_ws(FAKE, FAKE, FAKE, FAKE, 1, 1, 64, 64, 0, 0.125, DType.F32, Variant.NAIVE,
                                       None, FAKE, 64 * 64 * 4 - 1)
