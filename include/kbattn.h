@@ -183,6 +183,36 @@ KB_API int kb_check_device_error(void* stream);
  */
 KB_API int kb_selftest_timeout(unsigned long long limit_ns, void* stream);
 
+/*
+ * Size in bytes of the library-owned score array of kb_attn_fwd_naive_noalloc:
+ * 32 MiB, i.e. N*S*S <= 8388608 (for example 8 heads at S = 1024). Every GPU
+ * that loads the library holds this array until the process exits.
+ */
+#define KB_NAIVE_NOALLOC_MAX_BYTES (32u * 1024u * 1024u)
+
+/*
+ * kb_attn_fwd_naive_noalloc -- the KB_NAIVE fp32 forward (score GEMM, row
+ * softmax, P*V GEMM, the N*S*S scores through global memory) that allocates
+ * nothing. The pages have no counterpart: it exists for callers that cannot
+ * call cudaMalloc -- a caller whose device memory is entirely reserved by its
+ * own pool (an allocation would fail or fragment that pool), or a caller on a
+ * latency-critical path that must not pay cudaMalloc's cost and its implicit
+ * device synchronisation. The caller still passes inputs and outputs; the
+ * score workspace is a fixed array inside the library.
+ *   q, k, v, o, B, H, S, d, causal, scale, stream : as kb_attn_fwd, fp32 only
+ * Returns KB_ERR_NO_MEMORY, before any device work, when N*S*S*4 bytes exceed
+ * KB_NAIVE_NOALLOC_MAX_BYTES. Calls no cudaMalloc, cudaFree or other
+ * allocating routine. The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress) with that device current; make that first
+ * call before any stream capture. All calls share the one array and it keeps
+ * the last call's contents (nothing needs clearing: every score a call reads
+ * it has written first), so calls whose work overlaps on the GPU -- on
+ * different streams or from different host threads -- race on it.
+ */
+KB_API int kb_attn_fwd_naive_noalloc(const void* q, const void* k, const void* v, void* o,
+                                     int B, int H, int S, int d, int causal, float scale,
+                                     void* stream);
+
 /* Human-readable name of a kb_status (static storage, never NULL). */
 KB_API const char* kb_status_string(int status);
 

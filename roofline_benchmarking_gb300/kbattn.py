@@ -90,7 +90,11 @@ SIGNATURES = {
     "kb_status_string": (ctypes.c_char_p, [_I]),
     "kb_last_cuda_error": (_I, []),
     "kb_version": (_I, []),
+    "kb_attn_fwd_naive_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]),
 }
+
+# Bytes of the library-owned score array of kb_attn_fwd_naive_noalloc.
+NAIVE_NOALLOC_MAX_BYTES = 32 * 1024 * 1024
 
 _lib = None
 _lock = threading.Lock()
@@ -224,6 +228,21 @@ def kb_attn_bench(q, k, v, o, causal: bool, scale: float | None = None, variant:
                               ws_ptr, ws_bytes, warmup, iters, ms)
     _check(st, "kb_attn_bench")
     return list(ms)
+
+
+def kb_attn_fwd_naive_noalloc(q, k, v, o, causal: bool = False, scale: float | None = None, stream=None):
+    """The naive fp32 forward with its score workspace in the library's fixed
+    array: for callers that cannot allocate device memory (their memory is all
+    reserved by their own pool, or they must not pay cudaMalloc's cost and
+    implicit synchronisation). ``o`` must be given; nothing is allocated.
+    Calls that overlap on the GPU share the array and race on it."""
+    B, H, S, d, dt = _attn_args(q, k, v, o)
+    if scale is None:
+        scale = d ** -0.5
+    st = load().kb_attn_fwd_naive_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, H, S, d,
+                                          int(bool(causal)), float(scale), _stream_ptr(stream))
+    _check(st, "kb_attn_fwd_naive_noalloc")
+    return o
 
 
 # ---------------------------------------------------------------- triad
