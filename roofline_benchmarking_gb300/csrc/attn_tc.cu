@@ -6,8 +6,12 @@
 // through in tiles, a running max m and denominator l are kept per query row,
 // the score matrix is never materialised). It is laid out for GB300:
 //
-//  * one CTA per (head, pair of 128-row query tiles A and B), heaviest causal
-//    pairs first; the two tiles share every K and V tile the CTA loads;
+//  * a work item is a pair of 128-row query tiles A and B of one head; the two
+//    tiles share every K and V tile loaded for them. The grid is persistent
+//    (at most one CTA per SM): items are sorted heaviest first (causal) and
+//    dealt to the CTAs in a snake order. Within a CTA the next item's Q load
+//    starts as soon as the current item's last score MMA has completed, and
+//    its first P V waits only for the current epilogue to have read O;
 //  * warp 8 (one lane) stages both Q tiles and rings of K and V tiles with TMA
 //    (128-byte swizzle, 3-D tensor maps [N, S, d], rows past S zero-filled);
 //  * warp 9 (one lane) issues the tcgen05 MMAs: S = Q K^T from shared memory
@@ -50,12 +54,12 @@ constexpr int kPairRows = 2 * kBM;
 // Three warpgroups: 0 and 1 run the softmax of tiles A and B; in the third,
 // warp 8 drives TMA and warp 9 issues MMAs (warps 10 and 11 only hand their
 // registers over). Launch budget 384 x 168 = 64512 registers, rebalanced as
-// 2 x 128 x 224 + 128 x 56 = 64512.
+// 2 x 128 x 208 + 128 x 88 = 64512.
 constexpr int kThreadsTC = 384;
 constexpr int kWarpTMA = 8;
 constexpr int kWarpMMA = 9;
-constexpr int kRegsSoftmax = 224;
-constexpr int kRegsControl = 56;
+constexpr int kRegsSoftmax = 208;
+constexpr int kRegsControl = 88;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColBlock = 16384;  // one 128-row x 128-byte swizzled block
 constexpr unsigned long long kDefaultWaitLimitNs = 1000000000ull;
@@ -79,8 +83,10 @@ struct TcCfg {
     B_VEMPTY = B_VFULL + VS,
     B_SFULL = B_VEMPTY + VS,  // [2]: S of tile A / B computed
     B_PFULL = B_SFULL + 2,    // [2]: P of tile A / B written (and O rescaled)
-    B_OFINAL = B_PFULL + 2,   // [2]: last P V of tile A / B done
-    B_DRAIN = B_OFINAL + 2,
+    B_OFINAL = B_PFULL + 2,   // [2]: last P V of tile A / B of an item done
+    B_OFREE = B_OFINAL + 2,   // [2]: O of tile A / B read out by the epilogue
+    B_QFREE = B_OFREE + 2,    // last score MMA of an item done: Q may be replaced
+    B_DRAIN = B_QFREE + 1,
     NBAR = B_DRAIN + 1
   };
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // [0] TMEM base, [1] abort flag
@@ -128,6 +134,37 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   }
 }
 
+// The persistent schedule. Work item i (0 <= i < N * pairs) is query rows
+// [256 t, 256 t + 256) of head n with t = pairs - 1 - i / N, so the heaviest
+// causal items come first. CTA c takes, in round r, item r G + c when r is
+// even and item r G + G - 1 - c when r is odd: a snake over the list sorted
+// by cost keeps the per-CTA totals within a few per cent of each other.
+struct Item {
+  int n, t, q0, nA, nB;  // head, pair, first row, key tiles of tile A and of tile B
+};
+
+struct Schedule {
+  int N, S, causal, pairs, nkv, total;
+  __device__ Schedule(int N_, int S_, int causal_) : N(N_), S(S_), causal(causal_) {
+    pairs = (S + kPairRows - 1) / kPairRows;
+    nkv = (S + kBN - 1) / kBN;
+    total = N * pairs;
+  }
+  // Item of this CTA's round `round`; false once the list is exhausted (the
+  // index grows with the round, so every later round is exhausted too).
+  __device__ bool get(int round, Item& it) const {
+    const int G = (int)gridDim.x, c = (int)blockIdx.x;
+    const int i = round * G + ((round & 1) ? G - 1 - c : c);
+    if (i >= total) return false;
+    it.n = i % N;
+    it.t = pairs - 1 - i / N;
+    it.q0 = it.t * kPairRows;
+    it.nA = causal ? min(2 * it.t + 1, nkv) : nkv;
+    it.nB = causal ? min(2 * it.t + 2, nkv) : nkv;  // never shorter than nA
+    return true;
+  }
+};
+
 template <int D, bool F16>
 __global__ void __launch_bounds__(kThreadsTC, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
@@ -146,15 +183,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::OFF_MISC + 4);
   auto bar = [&](int i) -> uint32_t { return base + C::OFF_BAR + 8u * (uint32_t)i; };
 
-  // Work item: query rows [q0, q0 + 256) of head n, as tiles A and B.
-  const int npairs = (S + kPairRows - 1) / kPairRows;
-  const int nkv_all = (S + kBN - 1) / kBN;
-  const int n = (int)(blockIdx.x % (unsigned)N);
-  const int t = npairs - 1 - (int)(blockIdx.x / (unsigned)N);
-  const int q0 = t * kPairRows;
-  // key tiles each query tile visits (tile B is never shorter than tile A)
-  const int nA = causal ? min(2 * t + 1, nkv_all) : nkv_all;
-  const int nB = causal ? min(2 * t + 2, nkv_all) : nkv_all;
+  const Schedule sched(N, S, causal);
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -171,7 +200,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       ptx::mbar_init(bar(C::B_SFULL + g), 1);
       ptx::mbar_init(bar(C::B_PFULL + g), 4 * 32);
       ptx::mbar_init(bar(C::B_OFINAL + g), 1);
+      ptx::mbar_init(bar(C::B_OFREE + g), 4 * 32);
     }
+    ptx::mbar_init(bar(C::B_QFREE), 1);
     ptx::mbar_init(bar(C::B_DRAIN), 1);
     ptx::fence_mbar_init();
   }
@@ -192,36 +223,43 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         ptx::tma_prefetch_desc(&tmq);
         ptx::tma_prefetch_desc(&tmk);
         ptx::tma_prefetch_desc(&tmv);
-        ptx::mbar_arrive_expect_tx(bar(C::B_Q), 2 * C::TILE);
-        for (int g = 0; g < 2; ++g)
-          for (int b = 0; b < C::DB; ++b)
-            ptx::tma_load_3d(base + C::OFF_Q + g * C::TILE + b * kColBlock, &tmq, bar(C::B_Q), b * 64,
-                             q0 + g * kBM, n);
-        int kdone = 0, vdone = 0;  // loads issued
+        int kdone = 0, vdone = 0, items = 0;  // K tiles, V tiles and items whose loads were issued
         bool ok = true;
-        for (int j = 0; j < nB && ok; ++j) {
-          const int ks = j % C::KS, vs = j % C::VS;
-          if (j >= C::KS) ok = wait_bar(bar(C::B_KEMPTY + ks), ((j / C::KS) & 1) ^ 1, abort_flag, limit, true);
+        Item it;
+        for (int round = 0; ok && sched.get(round, it); ++round) {
+          // Q of both tiles, once the previous item's last score MMA has read the old Q
+          if (items > 0) ok = wait_bar(bar(C::B_QFREE), (items - 1) & 1, abort_flag, limit, true);
           if (!ok) break;
-          ptx::mbar_arrive_expect_tx(bar(C::B_KFULL + ks), C::TILE);
-          for (int b = 0; b < C::DB; ++b)
-            ptx::tma_load_3d(base + C::OFF_K + ks * C::TILE + b * kColBlock, &tmk, bar(C::B_KFULL + ks), b * 64,
-                             j * kBN, n);
-          kdone = j + 1;
-          if (j >= C::VS) ok = wait_bar(bar(C::B_VEMPTY + vs), ((j / C::VS) & 1) ^ 1, abort_flag, limit, true);
-          if (!ok) break;
-          ptx::mbar_arrive_expect_tx(bar(C::B_VFULL + vs), C::TILE);
-          for (int b = 0; b < C::DB; ++b)
-            ptx::tma_load_3d(base + C::OFF_V + vs * C::TILE + b * kColBlock, &tmv, bar(C::B_VFULL + vs), b * 64,
-                             j * kBN, n);
-          vdone = j + 1;
+          ptx::mbar_arrive_expect_tx(bar(C::B_Q), 2 * C::TILE);
+          for (int g = 0; g < 2; ++g)
+            for (int b = 0; b < C::DB; ++b)
+              ptx::tma_load_3d(base + C::OFF_Q + g * C::TILE + b * kColBlock, &tmq, bar(C::B_Q), b * 64,
+                               it.q0 + g * kBM, it.n);
+          for (int j = 0; j < it.nB && ok; ++j) {
+            const int ks = kdone % C::KS, vs = vdone % C::VS;
+            if (kdone >= C::KS) ok = wait_bar(bar(C::B_KEMPTY + ks), ((kdone / C::KS) & 1) ^ 1, abort_flag, limit, true);
+            if (!ok) break;
+            ptx::mbar_arrive_expect_tx(bar(C::B_KFULL + ks), C::TILE);
+            for (int b = 0; b < C::DB; ++b)
+              ptx::tma_load_3d(base + C::OFF_K + ks * C::TILE + b * kColBlock, &tmk, bar(C::B_KFULL + ks), b * 64,
+                               j * kBN, it.n);
+            ++kdone;
+            if (vdone >= C::VS) ok = wait_bar(bar(C::B_VEMPTY + vs), ((vdone / C::VS) & 1) ^ 1, abort_flag, limit, true);
+            if (!ok) break;
+            ptx::mbar_arrive_expect_tx(bar(C::B_VFULL + vs), C::TILE);
+            for (int b = 0; b < C::DB; ++b)
+              ptx::tma_load_3d(base + C::OFF_V + vs * C::TILE + b * kColBlock, &tmv, bar(C::B_VFULL + vs), b * 64,
+                               j * kBN, it.n);
+            ++vdone;
+          }
+          ++items;
         }
         // Every copy this CTA started must land before the CTA exits.
-        wait_bar(bar(C::B_Q), 0, abort_flag, limit, false);
-        for (int j = kdone - C::KS < 0 ? 0 : kdone - C::KS; j < kdone; ++j)
-          wait_bar(bar(C::B_KFULL + j % C::KS), (j / C::KS) & 1, abort_flag, limit, false);
-        for (int j = vdone - C::VS < 0 ? 0 : vdone - C::VS; j < vdone; ++j)
-          wait_bar(bar(C::B_VFULL + j % C::VS), (j / C::VS) & 1, abort_flag, limit, false);
+        if (items > 0) wait_bar(bar(C::B_Q), (items - 1) & 1, abort_flag, limit, false);
+        for (int x = kdone - C::KS < 0 ? 0 : kdone - C::KS; x < kdone; ++x)
+          wait_bar(bar(C::B_KFULL + x % C::KS), (x / C::KS) & 1, abort_flag, limit, false);
+        for (int x = vdone - C::VS < 0 ? 0 : vdone - C::VS; x < vdone; ++x)
+          wait_bar(bar(C::B_VFULL + x % C::VS), (x / C::VS) & 1, abort_flag, limit, false);
       }
       __syncwarp();
     } else if (warp == kWarpMMA) {
@@ -229,65 +267,81 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       if (lane == 0) {
         // S_g = Q_g K_j^T (K-major operands, both from shared memory)
         auto issue_s = [&](int g, int ks) {
+          // descriptors of k-step 0; a k-step moves the start address field (bytes >> 4)
+          const uint64_t a0 = ptx::sw128_desc(base + C::OFF_Q + g * C::TILE, 16, 1024);
+          const uint64_t b0 = ptx::sw128_desc(base + C::OFF_K + ks * C::TILE, 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kColBlock + (kk & 3) * 32;
-            const uint64_t a = ptx::sw128_desc(base + C::OFF_Q + g * C::TILE + off, 16, 1024);
-            const uint64_t b = ptx::sw128_desc(base + C::OFF_K + ks * C::TILE + off, 16, 1024);
-            ptx::mma_f16_ss(tmem + C::tm_s(g), a, b, IDESC_QK, kk > 0 ? 1u : 0u);
+            const uint32_t off = ((kk >> 2) * kColBlock + (kk & 3) * 32) >> 4;
+            ptx::mma_f16_ss(tmem + C::tm_s(g), a0 + off, b0 + off, IDESC_QK, kk > 0 ? 1u : 0u);
           }
           ptx::mma_commit(bar(C::B_SFULL + g));
         };
         // O_g += P_g V_j (P from TMEM, V MN-major from shared memory)
         auto issue_pv = [&](int g, int vs, bool first) {
+          const uint64_t b0 = ptx::sw128_desc(base + C::OFF_V + vs * C::TILE, kColBlock, 1024);
 #pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk) {
-            const uint64_t b = ptx::sw128_desc(base + C::OFF_V + vs * C::TILE + kk * 16 * 128, kColBlock, 1024);
-            ptx::mma_f16_ts(tmem + C::tm_o(g), tmem + C::tm_s(g) + kk * 8, b, IDESC_PV, (!first || kk > 0) ? 1u : 0u);
-          }
+          for (int kk = 0; kk < kBN / 16; ++kk)  // a k-step is 16 keys = 16 rows of 128 bytes
+            ptx::mma_f16_ts(tmem + C::tm_o(g), tmem + C::tm_s(g) + kk * 8, b0 + ((kk * 16 * 128) >> 4), IDESC_PV,
+                            (!first || kk > 0) ? 1u : 0u);
         };
-        bool ok = wait_bar(bar(C::B_Q), 0, abort_flag, limit, true);
-        if (ok) ok = wait_bar(bar(C::B_KFULL), 0, abort_flag, limit, true);
-        if (ok) {
-          ptx::tc_fence_after();
-          issue_s(0, 0);
-          issue_s(1, 0);
-          ptx::mma_commit(bar(C::B_KEMPTY));
-        }
-        for (int j = 0; j < nB && ok; ++j) {
-          const int vs = j % C::VS;
-          const int jn = j + 1, ksn = jn % C::KS;
-          ok = wait_bar(bar(C::B_VFULL + vs), (j / C::VS) & 1, abort_flag, limit, true);
-          if (ok && j < nA) {  // tile A
-            ok = wait_bar(bar(C::B_PFULL + 0), j & 1, abort_flag, limit, true);
-            if (ok) {
-              ptx::tc_fence_after();
-              issue_pv(0, vs, j == 0);
-              if (jn < nA) {
-                ok = wait_bar(bar(C::B_KFULL + ksn), (jn / C::KS) & 1, abort_flag, limit, true);
-                if (ok) {
-                  ptx::tc_fence_after();
-                  issue_s(0, ksn);
-                }
-              } else {
-                ptx::mma_commit(bar(C::B_OFINAL + 0));
-              }
-            }
-          }
-          if (ok) ok = wait_bar(bar(C::B_PFULL + 1), j & 1, abort_flag, limit, true);
+        bool ok = true;
+        int kbase = 0, vbase = 0;  // ring positions of the current item's first K and V tiles
+        int pa = 0, pb = 0;        // P tiles of tile A and of tile B consumed
+        Item it;
+        for (int item = 0; ok && sched.get(item, it); ++item) {
+          const int nA = it.nA, nB = it.nB;
+          ok = wait_bar(bar(C::B_Q), item & 1, abort_flag, limit, true);
+          const int ks0 = kbase % C::KS;
+          if (ok) ok = wait_bar(bar(C::B_KFULL + ks0), (kbase / C::KS) & 1, abort_flag, limit, true);
           if (!ok) break;
           ptx::tc_fence_after();
-          issue_pv(1, vs, j == 0);  // tile B
-          ptx::mma_commit(bar(C::B_VEMPTY + vs));
-          if (jn < nB) {
-            ok = wait_bar(bar(C::B_KFULL + ksn), (jn / C::KS) & 1, abort_flag, limit, true);
+          issue_s(0, ks0);
+          issue_s(1, ks0);
+          ptx::mma_commit(bar(C::B_KEMPTY + ks0));
+          if (nB == 1) ptx::mma_commit(bar(C::B_QFREE));
+          for (int j = 0; j < nB && ok; ++j) {
+            const int vp = vbase + j, vs = vp % C::VS;
+            const int jn = j + 1, kpn = kbase + jn, ksn = kpn % C::KS;
+            ok = wait_bar(bar(C::B_VFULL + vs), (vp / C::VS) & 1, abort_flag, limit, true);
+            if (ok && j < nA) {  // tile A
+              ok = wait_bar(bar(C::B_PFULL + 0), pa & 1, abort_flag, limit, true);
+              if (ok && j == 0 && item > 0) ok = wait_bar(bar(C::B_OFREE + 0), (item - 1) & 1, abort_flag, limit, true);
+              if (ok) {
+                ++pa;
+                ptx::tc_fence_after();
+                issue_pv(0, vs, j == 0);
+                if (jn < nA) {
+                  ok = wait_bar(bar(C::B_KFULL + ksn), (kpn / C::KS) & 1, abort_flag, limit, true);
+                  if (ok) {
+                    ptx::tc_fence_after();
+                    issue_s(0, ksn);
+                  }
+                } else {
+                  ptx::mma_commit(bar(C::B_OFINAL + 0));
+                }
+              }
+            }
+            if (ok) ok = wait_bar(bar(C::B_PFULL + 1), pb & 1, abort_flag, limit, true);
+            if (ok && j == 0 && item > 0) ok = wait_bar(bar(C::B_OFREE + 1), (item - 1) & 1, abort_flag, limit, true);
             if (!ok) break;
+            ++pb;
             ptx::tc_fence_after();
-            issue_s(1, ksn);
-            ptx::mma_commit(bar(C::B_KEMPTY + ksn));
-          } else {
-            ptx::mma_commit(bar(C::B_OFINAL + 1));
+            issue_pv(1, vs, j == 0);  // tile B
+            ptx::mma_commit(bar(C::B_VEMPTY + vs));
+            if (jn < nB) {
+              ok = wait_bar(bar(C::B_KFULL + ksn), (kpn / C::KS) & 1, abort_flag, limit, true);
+              if (!ok) break;
+              ptx::tc_fence_after();
+              issue_s(1, ksn);
+              ptx::mma_commit(bar(C::B_KEMPTY + ksn));
+              if (jn == nB - 1) ptx::mma_commit(bar(C::B_QFREE));  // the item's last score MMA
+            } else {
+              ptx::mma_commit(bar(C::B_OFINAL + 1));
+            }
           }
+          kbase += nB;
+          vbase += nB;
         }
         // No MMA may still be running when the tensor memory is released.
         ptx::mma_commit(bar(C::B_DRAIN));
@@ -301,114 +355,126 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     const int g = warp >> 2;  // query tile of this warpgroup
     const int wq = warp & 3;  // TMEM lane quarter
     const int r = wq * 32 + lane;
-    const int row = q0 + g * kBM + r;
-    const int nj = g ? nB : nA;
-    const int diag = 2 * t + g;  // the key tile on the diagonal (causal)
     const uint32_t tl = tmem + ((uint32_t)(wq * 32) << 16);
     const uint32_t ts = tl + C::tm_s(g), to = tl + C::tm_o(g);
-    float m_run = -INFINITY, l_run = 0.f;
+    int scnt = 0;  // score tiles consumed
     bool ok = true;
-    for (int j = 0; j < nj; ++j) {
-      if (!(ok = warp_wait(bar(C::B_SFULL + g), j & 1, abort_flag, limit))) break;
-      ptx::tc_fence_after();
-      float s[kBN];
-      {
-        uint32_t u0[32], u1[32], u2[32], u3[32];
-        ptx::tmem_ld32(ts + 0, u0);
-        ptx::tmem_ld32(ts + 32, u1);
-        ptx::tmem_ld32(ts + 64, u2);
-        ptx::tmem_ld32(ts + 96, u3);
-        ptx::tmem_wait_ld();
+    Item it;
+    for (int item = 0; ok && sched.get(item, it); ++item) {
+      const int row = it.q0 + g * kBM + r;
+      const int nj = g ? it.nB : it.nA;
+      const int diag = 2 * it.t + g;  // the key tile on the diagonal (causal)
+      float m_run = -INFINITY, l_run = 0.f;
+      for (int j = 0; j < nj; ++j) {
+        if (!(ok = warp_wait(bar(C::B_SFULL + g), scnt & 1, abort_flag, limit))) break;
+        ++scnt;
+        ptx::tc_fence_after();
+        float s[kBN];
+        {
+          uint32_t u0[32], u1[32], u2[32], u3[32];
+          ptx::tmem_ld32(ts + 0, u0);
+          ptx::tmem_ld32(ts + 32, u1);
+          ptx::tmem_ld32(ts + 64, u2);
+          ptx::tmem_ld32(ts + 96, u3);
+          ptx::tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          s[e] = __uint_as_float(u0[e]);
-          s[32 + e] = __uint_as_float(u1[e]);
-          s[64 + e] = __uint_as_float(u2[e]);
-          s[96 + e] = __uint_as_float(u3[e]);
+          for (int e = 0; e < 32; ++e) {
+            s[e] = __uint_as_float(u0[e]);
+            s[32 + e] = __uint_as_float(u1[e]);
+            s[64 + e] = __uint_as_float(u2[e]);
+            s[96 + e] = __uint_as_float(u3[e]);
+          }
         }
+        const int k0 = j * kBN;
+        if ((causal && j == diag) || k0 + kBN > S) {
+          const int lim = min(causal ? row - k0 : kBN - 1, S - 1 - k0);  // last visible column
+#pragma unroll
+          for (int c = 0; c < kBN; ++c)
+            if (c > lim) s[c] = -INFINITY;
+        }
+        float mx[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mx[e] = s[e];
+#pragma unroll
+        for (int c = 8; c < kBN; c += 8)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) mx[e] = fmaxf(mx[e], s[c + e]);
+        const float m_tile =
+            fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) *
+            scale_log2;
+        float alpha = 1.f;
+        bool corr = false;
+        if (j == 0) {
+          m_run = m_tile == -INFINITY ? 0.f : m_tile;
+        } else if (m_tile > m_run + 8.0f) {
+          alpha = ptx::ex2(m_run - m_tile);
+          m_run = m_tile;
+          l_run *= alpha;
+          corr = true;
+        }
+        // P = exp2(s * scale_log2 - m) as 16-bit pairs into columns [0, 64) of S
+        const float neg_m = -m_run;
+        float sum[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) sum[e] = 0.f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const float p0 = ptx::ex2(fmaf(s[h * 64 + 2 * c], scale_log2, neg_m));
+            const float p1 = ptx::ex2(fmaf(s[h * 64 + 2 * c + 1], scale_log2, neg_m));
+            sum[(2 * c) & 7] += p0;
+            sum[(2 * c + 1) & 7] += p1;
+            pk[c] = pack2<F16>(p0, p1);
+          }
+          ptx::tmem_st32(ts + h * 32, pk);
+        }
+        l_run += ((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7]));
+        if (__any_sync(0xffffffffu, corr)) {
+          // Rescale O after P is out (the scores are dead by now). S_g(j)
+          // completing implies P V of tile j-1 has completed (one issuing
+          // thread, in-order commits), so O holds exactly tiles < j here; P V
+          // of tile j waits for the PFULL arrival below.
+          uint32_t u[32];
+#pragma unroll 1
+          for (int cb = 0; cb < D / 32; ++cb) {
+            ptx::tmem_ld32(to + cb * 32, u);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * alpha);
+            ptx::tmem_st32(to + cb * 32, u);
+          }
+        }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(C::B_PFULL + g));
       }
-      const int k0 = j * kBN;
-      if ((causal && j == diag) || k0 + kBN > S) {
-        const int lim = min(causal ? row - k0 : kBN - 1, S - 1 - k0);  // last visible column
-#pragma unroll
-        for (int c = 0; c < kBN; ++c)
-          if (c > lim) s[c] = -INFINITY;
-      }
-      float mx[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) mx[e] = s[e];
-#pragma unroll
-      for (int c = 8; c < kBN; c += 8)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) mx[e] = fmaxf(mx[e], s[c + e]);
-      const float m_tile =
-          fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) *
-          scale_log2;
-      float alpha = 1.f;
-      bool corr = false;
-      if (j == 0) {
-        m_run = m_tile == -INFINITY ? 0.f : m_tile;
-      } else if (m_tile > m_run + 8.0f) {
-        alpha = ptx::ex2(m_run - m_tile);
-        m_run = m_tile;
-        l_run *= alpha;
-        corr = true;
-      }
-      if (__any_sync(0xffffffffu, corr)) {
-        // S_g(j) completing implies P V of tile j-1 has completed (one issuing
-        // thread, in-order commits), so O holds exactly tiles < j here.
+      if (ok) ok = warp_wait(bar(C::B_OFINAL + g), item & 1, abort_flag, limit);
+      if (ok) {
+        ptx::tc_fence_after();
+        const float inv = 1.0f / l_run;
+        uint8_t* orow = out + ((size_t)it.n * S + row) * (size_t)D * 2;
         uint32_t u[32];
-#pragma unroll
+#pragma unroll 1
         for (int cb = 0; cb < D / 32; ++cb) {
           ptx::tmem_ld32(to + cb * 32, u);
           ptx::tmem_wait_ld();
+          if (cb == D / 32 - 1) {
+            // all of O is in registers: the accumulator may take the next item
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(C::B_OFREE + g));
+          }
+          if (row < S) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * alpha);
-          ptx::tmem_st32(to + cb * 32, u);
-        }
-      }
-      // P = exp2(s * scale_log2 - m) as 16-bit pairs into columns [0, 64) of S
-      const float neg_m = -m_run;
-      float sum[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) sum[e] = 0.f;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float p0 = ptx::ex2(fmaf(s[h * 64 + 2 * c], scale_log2, neg_m));
-          const float p1 = ptx::ex2(fmaf(s[h * 64 + 2 * c + 1], scale_log2, neg_m));
-          sum[(2 * c) & 7] += p0;
-          sum[(2 * c + 1) & 7] += p1;
-          pk[c] = pack2<F16>(p0, p1);
-        }
-        ptx::tmem_st32(ts + h * 32, pk);
-      }
-      l_run += ((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7]));
-      ptx::tmem_wait_st();
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(C::B_PFULL + g));
-    }
-    if (ok) ok = warp_wait(bar(C::B_OFINAL + g), 0, abort_flag, limit);
-    if (ok) {
-      ptx::tc_fence_after();
-      const float inv = 1.0f / l_run;
-      uint8_t* orow = out + ((size_t)n * S + row) * (size_t)D * 2;
-      uint32_t u[32];
-#pragma unroll
-      for (int cb = 0; cb < D / 32; ++cb) {
-        ptx::tmem_ld32(to + cb * 32, u);
-        ptx::tmem_wait_ld();
-        if (row < S) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint4 w;
-            w.x = pack2<F16>(__uint_as_float(u[q * 8 + 0]) * inv, __uint_as_float(u[q * 8 + 1]) * inv);
-            w.y = pack2<F16>(__uint_as_float(u[q * 8 + 2]) * inv, __uint_as_float(u[q * 8 + 3]) * inv);
-            w.z = pack2<F16>(__uint_as_float(u[q * 8 + 4]) * inv, __uint_as_float(u[q * 8 + 5]) * inv);
-            w.w = pack2<F16>(__uint_as_float(u[q * 8 + 6]) * inv, __uint_as_float(u[q * 8 + 7]) * inv);
-            *reinterpret_cast<uint4*>(orow + cb * 64 + q * 16) = w;
+            for (int q = 0; q < 4; ++q) {
+              uint4 w;
+              w.x = pack2<F16>(__uint_as_float(u[q * 8 + 0]) * inv, __uint_as_float(u[q * 8 + 1]) * inv);
+              w.y = pack2<F16>(__uint_as_float(u[q * 8 + 2]) * inv, __uint_as_float(u[q * 8 + 3]) * inv);
+              w.z = pack2<F16>(__uint_as_float(u[q * 8 + 4]) * inv, __uint_as_float(u[q * 8 + 5]) * inv);
+              w.w = pack2<F16>(__uint_as_float(u[q * 8 + 6]) * inv, __uint_as_float(u[q * 8 + 7]) * inv);
+              *reinterpret_cast<uint4*>(orow + cb * 64 + q * 16) = w;
+            }
           }
         }
       }
@@ -481,8 +547,12 @@ cudaError_t tc_launch(const AttnProblem& p, cudaStream_t st) {
   if (!make_map(&mq, p.q, p.N, p.S, D, F16) || !make_map(&mk, p.k, p.N, p.S, D, F16) ||
       !make_map(&mv, p.v, p.N, p.S, D, F16))
     return cudaErrorInvalidValue;
-  const int64_t pairs = (p.S + kPairRows - 1) / kPairRows;
-  attn_tc_kernel<D, F16><<<(unsigned)(pairs * p.N), kThreadsTC, C::SMEM, st>>>(
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const int64_t items = (int64_t)((p.S + kPairRows - 1) / kPairRows) * p.N;
+  const int64_t grid = items < sms ? items : sms;  // persistent: at most one CTA per SM
+  attn_tc_kernel<D, F16><<<(unsigned)grid, kThreadsTC, C::SMEM, st>>>(
       mq, mk, mv, static_cast<uint8_t*>(p.o), (int)p.N, p.S, p.causal, p.scale * 1.4426950408889634f,
       kDefaultWaitLimitNs);
   return cudaGetLastError();
