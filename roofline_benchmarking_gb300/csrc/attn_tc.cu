@@ -392,15 +392,16 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
           for (int c = 0; c < kBN; ++c)
             if (c > lim) s[c] = -INFINITY;
         }
+        // row max with 3-input max over 8 accumulators
         float mx[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) mx[e] = s[e];
+        for (int e = 0; e < 8; ++e) mx[e] = fmaxf(s[e], s[8 + e]);
 #pragma unroll
-        for (int c = 8; c < kBN; c += 8)
+        for (int c = 16; c < kBN; c += 16)
 #pragma unroll
-          for (int e = 0; e < 8; ++e) mx[e] = fmaxf(mx[e], s[c + e]);
+          for (int e = 0; e < 8; ++e) mx[e] = ptx::max3(mx[e], s[c + e], s[c + 8 + e]);
         const float m_tile =
-            fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) *
+            fmaxf(ptx::max3(mx[0], mx[1], mx[2]), ptx::max3(mx[3], mx[4], ptx::max3(mx[5], mx[6], mx[7]))) *
             scale_log2;
         float alpha = 1.f;
         bool corr = false;
@@ -412,25 +413,27 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
           l_run *= alpha;
           corr = true;
         }
-        // P = exp2(s * scale_log2 - m) as 16-bit pairs into columns [0, 64) of S
-        const float neg_m = -m_run;
-        float sum[8];
+        // P = exp2(s * scale_log2 - m) as 16-bit pairs into columns [0, 64) of S;
+        // the scale-and-shift and the row sum run two lanes per instruction
+        const float2 sl2 = make_float2(scale_log2, scale_log2);
+        const float2 nm2 = make_float2(-m_run, -m_run);
+        float2 sum2[4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) sum[e] = 0.f;
+        for (int e = 0; e < 4; ++e) sum2[e] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           uint32_t pk[32];
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
-            const float p0 = ptx::ex2(fmaf(s[h * 64 + 2 * c], scale_log2, neg_m));
-            const float p1 = ptx::ex2(fmaf(s[h * 64 + 2 * c + 1], scale_log2, neg_m));
-            sum[(2 * c) & 7] += p0;
-            sum[(2 * c + 1) & 7] += p1;
-            pk[c] = pack2<F16>(p0, p1);
+            const float2 x = ptx::fma2(make_float2(s[h * 64 + 2 * c], s[h * 64 + 2 * c + 1]), sl2, nm2);
+            const float2 pv = make_float2(ptx::ex2(x.x), ptx::ex2(x.y));
+            sum2[c & 3] = ptx::add2(sum2[c & 3], pv);
+            pk[c] = pack2<F16>(pv.x, pv.y);
           }
           ptx::tmem_st32(ts + h * 32, pk);
         }
-        l_run += ((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7]));
+        const float2 t2 = ptx::add2(ptx::add2(sum2[0], sum2[1]), ptx::add2(sum2[2], sum2[3]));
+        l_run += t2.x + t2.y;
         if (__any_sync(0xffffffffu, corr)) {
           // Rescale O after P is out (the scores are dead by now). S_g(j)
           // completing implies P V of tile j-1 has completed (one issuing
