@@ -58,6 +58,12 @@ class Oracle:
         lib.kb_oracle_attn_rows.restype = ctypes.c_int
         lib.kb_oracle_triad.argtypes = [_FP, _FP, _FP, ctypes.c_float, _I64]
         lib.kb_oracle_triad.restype = ctypes.c_int
+        lib.kb_oracle_copy.argtypes = [_FP, _FP, _I64]
+        lib.kb_oracle_copy.restype = ctypes.c_int
+        lib.kb_oracle_fill.argtypes = [_FP, ctypes.c_float, _I64]
+        lib.kb_oracle_fill.restype = ctypes.c_int
+        lib.kb_oracle_sum.argtypes = [_FP, _I64, _DP]
+        lib.kb_oracle_sum.restype = ctypes.c_int
         self.lib = lib
         self.path = path
 
@@ -117,6 +123,27 @@ class Oracle:
         if rc != 0:
             raise ValueError(f"kb_oracle_triad returned {rc}")
         return a
+
+
+    def copy(self, b) -> np.ndarray:
+        b = np.ascontiguousarray(np.asarray(b, dtype=np.float32))
+        a = np.empty_like(b)
+        if self.lib.kb_oracle_copy(a.ctypes.data_as(_FP), b.ctypes.data_as(_FP), b.size) != 0:
+            raise ValueError("kb_oracle_copy failed")
+        return a
+
+    def fill(self, n: int, s: float) -> np.ndarray:
+        a = np.empty(n, dtype=np.float32)
+        if self.lib.kb_oracle_fill(a.ctypes.data_as(_FP), ctypes.c_float(s), n) != 0:
+            raise ValueError("kb_oracle_fill failed")
+        return a
+
+    def sum(self, b) -> float:
+        b = np.ascontiguousarray(np.asarray(b, dtype=np.float32))
+        out = ctypes.c_double()
+        if self.lib.kb_oracle_sum(b.ctypes.data_as(_FP), b.size, ctypes.byref(out)) != 0:
+            raise ValueError("kb_oracle_sum failed")
+        return out.value
 
 
 _default: Oracle | None = None

@@ -21,7 +21,8 @@
  *  - same page, sequence diagram "One MCU measurement": the request carries a
  *    causal flag next to seq and dim.
  *  - TileOPs "Hardware Microbenchmarks" README, section "HBM Bandwidth" and
- *    "Methodology": the STREAM Triad a[i] = b[i] + s*c[i].
+ *    "Methodology": the STREAM Triad a[i] = b[i] + s*c[i], and the copy,
+ *    read-only and write-only reference kernels beside it.
  *
  * Readings where the pages are silent:
  *  - causal: key j is visible to query i iff j <= i;
@@ -35,7 +36,7 @@
  * Parity status: pinned. The attention functions are pinned by a
  * high-precision brute-force evaluation on tiny inputs and by closed-form
  * invariants; the Triad is pinned by exact rational arithmetic and by the
- * STREAM constant check.
+ * STREAM constant check; copy, fill and sum by exact small-integer cases.
  */
 #include <math.h>
 #include <stdint.h>
@@ -130,6 +131,33 @@ int kb_oracle_attn_rows(const double* q, const double* k, const double* v, doubl
   for (int64_t t = 0; t < count; ++t)
     attn_one_row(q, k, v, o + t * d, p, S, d, causal, scale, heads[t], rows[t]);
   free(p);
+  return KB_ORACLE_OK;
+}
+
+/*
+ * The Triad's sibling reference kernels (TileOPs README, "HBM Bandwidth" /
+ * "Methodology": copy 1:1 read:write, read-only, write-only):
+ *   copy : a[i] = b[i]
+ *   fill : a[i] = s             (write-only)
+ *   sum  : sum_i b[i] in double (read-only; the value a reader must produce)
+ */
+int kb_oracle_copy(float* a, const float* b, int64_t n) {
+  if (n < 0 || (n > 0 && (!a || !b))) return KB_ORACLE_BAD_ARG;
+  for (int64_t i = 0; i < n; ++i) a[i] = b[i];
+  return KB_ORACLE_OK;
+}
+
+int kb_oracle_fill(float* a, float s, int64_t n) {
+  if (n < 0 || (n > 0 && !a)) return KB_ORACLE_BAD_ARG;
+  for (int64_t i = 0; i < n; ++i) a[i] = s;
+  return KB_ORACLE_OK;
+}
+
+int kb_oracle_sum(const float* b, int64_t n, double* out) {
+  if (n < 0 || !out || (n > 0 && !b)) return KB_ORACLE_BAD_ARG;
+  double acc = 0.0;
+  for (int64_t i = 0; i < n; ++i) acc += (double)b[i];
+  *out = acc;
   return KB_ORACLE_OK;
 }
 

@@ -264,11 +264,21 @@ def pin_triad_stream_constants(orc):
     assert np.all(a == 7.0)
 
 
+def pin_hbm_reference_kernels(orc):
+    """copy, fill and sum on values whose exact results are known."""
+    b = (np.arange(1, 5001) % 97).astype(np.float32)
+    assert np.array_equal(orc.copy(b), b)
+    assert np.all(orc.fill(3001, -2.5) == np.float32(-2.5)) and orc.fill(3001, 1.0).size == 3001
+    assert orc.sum(b) == float(sum(int(x) for x in b))          # small integers: exact
+    assert orc.sum(np.full(1 << 12, 0.25, np.float32)) == 1024.0
+    assert orc.sum(np.zeros(0, np.float32)) == 0.0
+
+
 PINS = [pin_brute_force, pin_rows_are_probabilities, pin_constant_v, pin_zero_query_is_mean,
         pin_causal_first_row_and_single_key, pin_causal_is_prefix_attention, pin_key_permutation,
         pin_key_shift, pin_affine_in_v, pin_hard_attention_limit, pin_two_key_closed_form,
         pin_heads_are_independent, pin_rows_api_matches_full, pin_triad_exact,
-        pin_triad_stream_constants]
+        pin_triad_stream_constants, pin_hbm_reference_kernels]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -306,6 +316,10 @@ MUTANTS = {
                           "p[0] = 0.0;\n  for (int64_t j = 1; j <= last; ++j) {\n    p[j] = exp"),
     "triad_two_roundings": ("a[i] = fmaf(s, c[i], b[i]);", "a[i] = b[i] + s * c[i];"),
     "triad_swapped_operands": ("a[i] = fmaf(s, c[i], b[i]);", "a[i] = fmaf(s, b[i], c[i]);"),
+    "copy_off_by_one": ("for (int64_t i = 0; i < n; ++i) a[i] = b[i];",
+                        "for (int64_t i = 1; i < n; ++i) a[i] = b[i - 1];"),
+    "sum_drops_last": ("for (int64_t i = 0; i < n; ++i) acc += (double)b[i];",
+                       "for (int64_t i = 0; i + 1 < n; ++i) acc += (double)b[i];"),
 }
 
 
