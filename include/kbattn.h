@@ -159,6 +159,32 @@ KB_API int kb_attn_bench(const void* q, const void* k, const void* v, void* o,
 KB_API int kb_triad(float* a, const float* b, const float* c, float s, size_t n,
              int block, void* stream);
 
+/*
+ * The Triad's reference kernels (TileOPs README, "HBM Bandwidth" /
+ * "Methodology": copy 1:1 read:write, read-only and write-only), float4
+ * vectorised with streaming cache hints, same pointer and block rules as
+ * kb_triad:
+ *   kb_hbm_copy  : a[i] = b[i]                       (4 bytes read, 4 written)
+ *   kb_hbm_write : a[i] = s                          (4 bytes written)
+ *   kb_hbm_read  : *out = sum of b[0..n) in fp32     (4 bytes read); out is a
+ *                  4-byte aligned device float that the call first zeroes on
+ *                  `stream` (partial sums are fp32, so the value is exact only
+ *                  where every partial sum is representable)
+ */
+KB_API int kb_hbm_copy(float* a, const float* b, size_t n, int block, void* stream);
+KB_API int kb_hbm_write(float* a, float s, size_t n, int block, void* stream);
+KB_API int kb_hbm_read(const float* b, size_t n, int block, float* out, void* stream);
+
+typedef enum { KB_HBM_TRIAD = 0, KB_HBM_COPY = 1, KB_HBM_READ = 2, KB_HBM_WRITE = 3 } kb_hbm_op;
+
+/*
+ * kb_hbm_bench -- one of the four HBM kernels (`op`, a kb_hbm_op) timed like
+ * kb_attn_bench; arguments a kernel does not use are ignored (but pointers
+ * must still be valid device pointers).
+ */
+KB_API int kb_hbm_bench(int op, float* a, const float* b, const float* c, float s, size_t n, int block,
+                        float* out, void* stream, int warmup, int iters, float* ms_per_iter);
+
 /* kb_triad timed like kb_attn_bench. */
 KB_API int kb_triad_bench(float* a, const float* b, const float* c, float s, size_t n,
                    int block, void* stream, int warmup, int iters, float* ms_per_iter);

@@ -264,6 +264,57 @@ int kb_triad_bench(float* a, const float* b, const float* c, float s, size_t n, 
   return time_calls(call, static_cast<cudaStream_t>(stream), warmup, iters, ms_per_iter);
 }
 
+namespace {
+// Shared checks of the HBM kernels; 0 floats is a no-op (KB_OK, nothing launched).
+int hbm_args(const void* a, const void* b, const void* c, size_t n, int* block) {
+  if (!a || !b || !c) return KB_ERR_INVALID_ARG;
+  if (!aligned16(a) || !aligned16(b) || !aligned16(c)) return KB_ERR_INVALID_ARG;
+  if (*block == 0) *block = 256;
+  if (*block != 128 && *block != 256 && *block != 512) return KB_ERR_INVALID_ARG;
+  return check_device();
+}
+}  // namespace
+
+int kb_hbm_copy(float* a, const float* b, size_t n, int block, void* stream) {
+  if (n == 0) return KB_OK;
+  int st = hbm_args(a, b, b, n, &block);
+  if (st != KB_OK) return st;
+  cudaError_t e = launch_copy(a, b, n, block, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KB_OK : cuda_fail(e);
+}
+
+int kb_hbm_write(float* a, float s, size_t n, int block, void* stream) {
+  if (n == 0) return KB_OK;
+  int st = hbm_args(a, a, a, n, &block);
+  if (st != KB_OK) return st;
+  cudaError_t e = launch_fill(a, s, n, block, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KB_OK : cuda_fail(e);
+}
+
+int kb_hbm_read(const float* b, size_t n, int block, float* out, void* stream) {
+  if (!out || (reinterpret_cast<uintptr_t>(out) & 3u)) return KB_ERR_INVALID_ARG;
+  int st = n == 0 ? check_device() : hbm_args(b, b, b, n, &block);
+  if (st != KB_OK) return st;
+  cudaError_t e = n == 0 ? cudaMemsetAsync(out, 0, sizeof(float), static_cast<cudaStream_t>(stream))
+                         : launch_read(b, n, out, block, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KB_OK : cuda_fail(e);
+}
+
+int kb_hbm_bench(int op, float* a, const float* b, const float* c, float s, size_t n, int block, float* out,
+                 void* stream, int warmup, int iters, float* ms_per_iter) {
+  if (warmup < 0 || iters < 1 || !ms_per_iter) return KB_ERR_INVALID_ARG;
+  if (op < KB_HBM_TRIAD || op > KB_HBM_WRITE) return KB_ERR_INVALID_ARG;
+  auto call = [&]() {
+    switch (op) {
+      case KB_HBM_TRIAD: return kb_triad(a, b, c, s, n, block, stream);
+      case KB_HBM_COPY: return kb_hbm_copy(a, b, n, block, stream);
+      case KB_HBM_READ: return kb_hbm_read(b, n, block, out, stream);
+      default: return kb_hbm_write(a, s, n, block, stream);
+    }
+  };
+  return time_calls(call, static_cast<cudaStream_t>(stream), warmup, iters, ms_per_iter);
+}
+
 int kb_device_info(int device, kb_device_info_t* out) {
   if (!out || device < 0) return KB_ERR_INVALID_ARG;
   int count = 0;

@@ -37,6 +37,9 @@ int tc_check(int S, int d, int dtype);
 
 cudaError_t launch_triad(float* a, const float* b, const float* c, float s, size_t n, int block,
                          cudaStream_t st);
+cudaError_t launch_copy(float* a, const float* b, size_t n, int block, cudaStream_t st);
+cudaError_t launch_fill(float* a, float s, size_t n, int block, cudaStream_t st);
+cudaError_t launch_read(const float* b, size_t n, float* out, int block, cudaStream_t st);
 
 // Device error word (bounded waits that ran out).
 cudaError_t read_and_clear_error_word(unsigned int* out, cudaStream_t st);

@@ -1,0 +1,198 @@
+"""Measurement harness: every workload x variant of the attention library and
+the four HBM kernels, timed with CUDA events around each launch, placed on the
+roofline, with SM clocks sampled during each row. One schema for all rows,
+written as CSV, Markdown and JSON lines.
+
+  python -m roofline_benchmarking_gb300.harness [--only SUBSTR] [--out DIR]
+                                                [--seconds S] [--quick]
+
+Sources (web pages): the kbench page, "Implementation details" (events around
+the kernel only, configurable warm-up, mean / p50 / p99 / min, achieved GFLOP/s
+and effective GB/s) and "Analysis" (each kernel placed against min(compute
+ceiling, intensity x bandwidth ceiling)); the TileOPs "Hardware Microbenchmarks"
+README, "Methodology" (Triad, copy, read-only and write-only; 100 warm-up
+launches, 5 runs of 200 timed launches, best and median, block sizes
+128/256/512, 2 GiB arrays).
+
+Correctness is not checked here (the harness is product code and never runs
+the oracle); the parity of every row is covered by the GPU tests.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import json
+import math
+import os
+import statistics
+import sys
+import time
+
+import torch
+
+from . import inputs, kbattn
+from . import roofline as rf
+from .clocks import ClockSampler, gpu_id_for_smi
+
+ATTN_VARIANTS = {"f32": [kbattn.Variant.NAIVE, kbattn.Variant.FUSED, kbattn.Variant.FLASH],
+                 "bf16": [kbattn.Variant.TC], "f16": [kbattn.Variant.TC]}
+
+FIELDS = ["kernel", "workload", "variant", "dtype", "block", "p50_ms", "min_ms", "mean_ms", "p99_ms", "tflops",
+          "gbs", "bound", "attainable", "roofline_unit", "roofline_frac", "sm_mhz", "clock_reasons", "iters"]
+
+
+def _stats(ms: list[float]) -> dict:
+    s = sorted(ms)
+    return {"p50_ms": statistics.median(s), "min_ms": s[0], "mean_ms": statistics.mean(s),
+            "p99_ms": s[min(len(s) - 1, int(math.ceil(0.99 * len(s))) - 1)], "iters": len(s)}
+
+
+def naive_score_bytes(w: inputs.Workload) -> float:
+    """Score traffic of the three-pass variant: pass 1 writes each visible score,
+    pass 2 reads it twice and writes it once, pass 3 reads it once."""
+    visible = w.S * (w.S + 1) / 2 if w.causal else float(w.S) * w.S
+    return 5.0 * 4.0 * w.N * visible
+
+
+def attention_row(w, variant, peaks, dev_info, seconds, sampler) -> dict:
+    q, k, v = (t.cuda() for t in inputs.make_qkv(w))
+    o = torch.empty_like(q)
+    ws = None
+    if variant == kbattn.Variant.NAIVE:
+        nbytes = kbattn.kb_attn_workspace_bytes(w.B, w.H, w.S, w.d, kbattn.DType.F32, variant)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    probe = kbattn.kb_attn_bench(q, k, v, o, w.causal, w.scale, variant, warmup=3, iters=3, workspace=ws)
+    iters = max(10, min(5000, int(seconds / max(statistics.median(probe) * 1e-3, 1e-6))))
+    t0 = time.time()
+    ms = kbattn.kb_attn_bench(q, k, v, o, w.causal, w.scale, variant, warmup=10, iters=iters, workspace=ws)
+    t1 = time.time()
+    if kbattn.kb_check_device_error() != kbattn.Status.OK:
+        raise RuntimeError(f"device error in {w.name} {variant.name}")
+    st = _stats(ms)
+    clocks = sampler.summary(t0, t1)
+    sec = st["p50_ms"] * 1e-3
+    tflops = w.flops / sec / 1e12
+    io = w.io_bytes
+    if variant == kbattn.Variant.TC:
+        compute, bound = peaks["bf16_tflops"], "tensor"
+        traffic = io
+    else:
+        # fp32 CUDA-core peak: SMs x 128 lanes x 2 FLOP x the device's maximum clock
+        compute = rf.fp32_peak_gflops(dev_info["sm_count"], dev_info["sm_clock_khz"] / 1e3) / 1e3
+        bound = "fp32"
+        traffic = io + (naive_score_bytes(w) if variant == kbattn.Variant.NAIVE else 0.0)
+    intensity = w.flops / traffic
+    attainable = rf.attainable(intensity, compute * 1e3, peaks["hbm_gbs"]) / 1e3
+    if attainable < compute:
+        bound = "hbm"
+    return {"kernel": "attention", "workload": w.name, "variant": variant.name, "dtype": w.dtype, "block": "",
+            **st, "tflops": tflops, "gbs": traffic / sec / 1e9, "bound": bound, "attainable": attainable,
+            "roofline_unit": "TFLOP/s", "roofline_frac": tflops / attainable, "sm_mhz": clocks["sm_mhz"],
+            "clock_reasons": "+".join(clocks["reasons"]) or "none"}
+
+
+def hbm_rows(peaks, dev_info, quick, sampler, only) -> list[dict]:
+    n = inputs.TRIAD_N if not quick else inputs.TRIAD_N // 8
+    a = torch.empty(n, dtype=torch.float32, device="cuda")
+    b = torch.ones(n, dtype=torch.float32, device="cuda")
+    c = torch.full((n,), 2.0, dtype=torch.float32, device="cuda")
+    out = torch.zeros(1, dtype=torch.float32, device="cuda")
+    theo = rf.theoretical_dram_gbs(dev_info["mem_clock_khz"] / 1e3, dev_info["mem_bus_width_bits"])
+    rows = []
+    runs, iters, warm = (5, 200, 100) if not quick else (2, 20, 5)
+    for op in kbattn.HbmOp:
+        name = op.name.lower()
+        if only and only not in name:
+            continue
+        nbytes = kbattn.HBM_BYTES_PER_ELEMENT[op] * n
+        for block in (128, 256, 512):
+            kbattn.kb_hbm_bench(op, a, b, c, 3.0, out, block=block, warmup=warm, iters=1)
+            t0 = time.time()
+            per_run = [kbattn.kb_hbm_bench(op, a, b, c, 3.0, out, block=block, warmup=0, iters=iters)
+                       for _ in range(runs)]
+            t1 = time.time()
+            clocks = sampler.summary(t0, t1)
+            allms = [x for r in per_run for x in r]
+            st = _stats(allms)
+            gbs_runs = [nbytes / (statistics.mean(r) * 1e-3) / 1e9 for r in per_run]
+            best = max(gbs_runs)
+            rows.append({"kernel": name, "workload": f"{n * 4 >> 20} MiB arrays", "variant": name,
+                         "dtype": "f32", "block": block, **st, "tflops": 0.0, "gbs": best, "bound": "hbm",
+                         "attainable": theo, "roofline_unit": "GB/s", "roofline_frac": best / theo,
+                         "sm_mhz": clocks["sm_mhz"], "clock_reasons": "+".join(clocks["reasons"]) or "none",
+                         "gbs_median_of_runs": statistics.median(gbs_runs),
+                         "frac_of_measured_copy": best / peaks["hbm_gbs"]})
+    del a, b, c
+    torch.cuda.empty_cache()
+    return rows
+
+
+def write_outputs(rows, out_dir, meta):
+    os.makedirs(out_dir, exist_ok=True)
+    with open(os.path.join(out_dir, "results.jsonl"), "w") as f:
+        f.write(json.dumps({"meta": meta}) + "\n")
+        for r in rows:
+            f.write(json.dumps(r) + "\n")
+    with open(os.path.join(out_dir, "results.csv"), "w", newline="") as f:
+        wr = csv.DictWriter(f, fieldnames=FIELDS, extrasaction="ignore")
+        wr.writeheader()
+        wr.writerows(rows)
+    md = [f"Device: {meta['device']} ({meta['sms']} SMs); peaks: {meta['peaks_source']} "
+          f"bf16 {meta['peaks']['bf16_tflops']} TFLOP/s, copy {meta['peaks']['hbm_gbs']} GB/s; "
+          f"theoretical HBM {meta['theoretical_hbm_gbs']:.0f} GB/s; fp32 FMA peak {meta['fp32_peak_tflops']:.1f} TFLOP/s.",
+          "",
+          "| kernel | workload | variant | block | p50 ms | min ms | p99 ms | TFLOP/s | GB/s | bound | attainable | frac | SM MHz |",
+          "|---|---|---|---|---|---|---|---|---|---|---|---|---|"]
+    for r in rows:
+        md.append(f"| {r['kernel']} | {r['workload']} | {r['variant']} | {r['block']} | {r['p50_ms']:.4f} | "
+                  f"{r['min_ms']:.4f} | {r['p99_ms']:.4f} | {r['tflops']:.2f} | {r['gbs']:.0f} | {r['bound']} | "
+                  f"{r['attainable']:.1f} {r['roofline_unit']} | {r['roofline_frac']:.3f} | {r['sm_mhz']} |")
+    with open(os.path.join(out_dir, "results.md"), "w") as f:
+        f.write("\n".join(md) + "\n")
+    return "\n".join(md)
+
+
+def main(argv=None) -> int:
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--only", default="", help="run only rows whose workload, variant or kernel contains this")
+    p.add_argument("--out", default="harness_out")
+    p.add_argument("--seconds", type=float, default=0.5, help="timed seconds per attention row")
+    p.add_argument("--quick", action="store_true", help="small HBM arrays and few repetitions")
+    p.add_argument("--no-hbm", action="store_true")
+    args = p.parse_args(argv)
+    if not torch.cuda.is_available():
+        print("the harness needs a CUDA GPU", file=sys.stderr)
+        return 2
+    from . import build
+    build.build()
+    kbattn.load()
+    dev = torch.cuda.current_device()
+    info = kbattn.kb_device_info(dev)
+    peaks, src = rf.load_measured_peaks()
+    sampler = ClockSampler(gpu_id_for_smi(dev))
+    sampler.start()
+    time.sleep(0.3)
+    rows = []
+    only = args.only.lower()
+    try:
+        for w in inputs.WORKLOADS.values():
+            for variant in ATTN_VARIANTS[w.dtype]:
+                if only and only not in w.name.lower() and only not in variant.name.lower():
+                    continue
+                rows.append(attention_row(w, variant, peaks, info, args.seconds, sampler))
+                print(json.dumps(rows[-1]), flush=True)
+        if not args.no_hbm:
+            for r in hbm_rows(peaks, info, args.quick, sampler, only):
+                rows.append(r)
+                print(json.dumps(r), flush=True)
+    finally:
+        sampler.stop()
+    meta = {"device": info["name"], "sms": info["sm_count"], "peaks": peaks, "peaks_source": src,
+            "theoretical_hbm_gbs": rf.theoretical_dram_gbs(info["mem_clock_khz"] / 1e3, info["mem_bus_width_bits"]),
+            "fp32_peak_tflops": rf.fp32_peak_gflops(info["sm_count"], info["sm_clock_khz"] / 1e3) / 1e3}
+    print(write_outputs(rows, args.out, meta))
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -91,7 +91,22 @@ SIGNATURES = {
     "kb_last_cuda_error": (_I, []),
     "kb_version": (_I, []),
     "kb_attn_fwd_naive_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]),
+    "kb_hbm_copy": (_I, [_P, _P, _SZ, _I, _P]),
+    "kb_hbm_write": (_I, [_P, _F, _SZ, _I, _P]),
+    "kb_hbm_read": (_I, [_P, _SZ, _I, _P, _P]),
+    "kb_hbm_bench": (_I, [_I, _P, _P, _P, _F, _SZ, _I, _P, _P, _I, _I, _FP]),
 }
+
+
+class HbmOp(enum.IntEnum):
+    TRIAD = 0
+    COPY = 1
+    READ = 2
+    WRITE = 3
+
+
+# Bytes each HBM kernel moves per float element.
+HBM_BYTES_PER_ELEMENT = {HbmOp.TRIAD: 12, HbmOp.COPY: 8, HbmOp.READ: 4, HbmOp.WRITE: 4}
 
 # Bytes of the library-owned score array of kb_attn_fwd_naive_noalloc.
 NAIVE_NOALLOC_MAX_BYTES = 32 * 1024 * 1024
@@ -263,6 +278,36 @@ def kb_triad_bench(a, b, c, s: float, block: int = 256, warmup: int = 3, iters: 
     st = load().kb_triad_bench(a.data_ptr(), b.data_ptr(), c.data_ptr(), float(s), n, block,
                                _stream_ptr(stream), warmup, iters, ms)
     _check(st, "kb_triad_bench")
+    return list(ms)
+
+
+def kb_hbm_copy(a, b, block: int = 256, stream=None):
+    """a = b over every element (fp32 CUDA tensors of equal size)."""
+    if b.numel() != a.numel():
+        raise ValueError("a and b must have the same number of elements")
+    _check(load().kb_hbm_copy(a.data_ptr(), b.data_ptr(), a.numel(), block, _stream_ptr(stream)), "kb_hbm_copy")
+    return a
+
+
+def kb_hbm_write(a, s: float, block: int = 256, stream=None):
+    """a = s over every element."""
+    _check(load().kb_hbm_write(a.data_ptr(), float(s), a.numel(), block, _stream_ptr(stream)), "kb_hbm_write")
+    return a
+
+
+def kb_hbm_read(b, out, block: int = 256, stream=None):
+    """out[0] = sum of b (fp32 partial sums); ``out`` is a 1-element fp32 CUDA tensor."""
+    _check(load().kb_hbm_read(b.data_ptr(), b.numel(), block, out.data_ptr(), _stream_ptr(stream)), "kb_hbm_read")
+    return out
+
+
+def kb_hbm_bench(op: int, a, b, c, s: float, out, block: int = 256, warmup: int = 3, iters: int = 10,
+                 stream=None) -> list[float]:
+    """Per-call device times (ms) of one HBM kernel over a.numel() floats."""
+    ms = (ctypes.c_float * iters)()
+    st = load().kb_hbm_bench(int(op), a.data_ptr(), b.data_ptr(), c.data_ptr(), float(s), a.numel(), block,
+                             out.data_ptr(), _stream_ptr(stream), warmup, iters, ms)
+    _check(st, "kb_hbm_bench")
     return list(ms)
 
 

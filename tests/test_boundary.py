@@ -135,6 +135,19 @@ def test_triad_and_bench_argument_checks(lib):
                            ms) == Status.INVALID_ARG
 
 
+def test_hbm_argument_checks(lib):
+    L = kbattn.load()
+    assert L.kb_hbm_copy(FAKE, FAKE, 0, 256, None) == Status.OK          # n = 0 is a no-op
+    assert L.kb_hbm_copy(FAKE, 0, 16, 256, None) == Status.INVALID_ARG
+    assert L.kb_hbm_copy(FAKE, FAKE + 4, 16, 256, None) == Status.INVALID_ARG
+    assert L.kb_hbm_write(FAKE, 1.0, 16, 96, None) == Status.INVALID_ARG
+    assert L.kb_hbm_read(FAKE, 16, 256, None, None) == Status.INVALID_ARG
+    assert L.kb_hbm_read(FAKE, 16, 256, FAKE + 2, None) == Status.INVALID_ARG
+    ms = (ctypes.c_float * 1)()
+    assert L.kb_hbm_bench(7, FAKE, FAKE, FAKE, 1.0, 16, 256, FAKE, None, 0, 1, ms) == Status.INVALID_ARG
+    assert L.kb_hbm_bench(0, FAKE, FAKE, FAKE, 1.0, 16, 256, FAKE, None, 0, 0, ms) == Status.INVALID_ARG
+
+
 def test_status_strings(lib):
     for s in Status:
         assert kbattn.status_string(s) == "KB_" + ("OK" if s == Status.OK else "ERR_" + s.name)

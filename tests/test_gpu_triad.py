@@ -50,3 +50,30 @@ def test_device_info_is_gb300_class():
     info = kbattn.kb_device_info(torch.cuda.current_device())
     assert (info["cc_major"], info["cc_minor"]) == (10, 3)
     assert info["sm_count"] > 100 and info["mem_bus_width_bits"] > 0 and info["mem_clock_khz"] > 0
+
+
+@pytest.mark.parametrize("block", [128, 256, 512])
+@pytest.mark.parametrize("n", [1, 3, 4, 1023, 4099, (1 << 20) + 7])
+def test_copy_write_read_match_oracle(oracle, n, block):
+    b, _ = inputs.make_triad_inputs(n, seed=n + 1)
+    g = Guarded((n,), torch.float32)
+    kbattn.kb_hbm_copy(g.out, b.cuda(), block=block)
+    assert np.array_equal(g.check().cpu().numpy().view(np.uint32), oracle.copy(b.numpy()).view(np.uint32))
+    g = Guarded((n,), torch.float32)
+    kbattn.kb_hbm_write(g.out, -1.75, block=block)
+    assert np.array_equal(g.check().cpu().numpy(), oracle.fill(n, -1.75))
+    # small integers: every fp32 partial sum is exact, so the read kernel's sum is exact
+    ints = ((torch.arange(n) % 7) - 3).to(torch.float32)
+    out = torch.full((1,), 123.0, device="cuda")
+    kbattn.kb_hbm_read(ints.cuda(), out, block=block)
+    assert float(out.item()) == oracle.sum(ints.numpy())
+
+
+def test_hbm_bench_runs_every_kernel():
+    n = 8 << 20
+    a, b, c = (torch.ones(n, device="cuda") for _ in range(3))
+    out = torch.zeros(1, device="cuda")
+    for op in kbattn.HbmOp:
+        ms = kbattn.kb_hbm_bench(op, a, b, c, 2.0, out, block=256, warmup=1, iters=3)
+        assert len(ms) == 3 and all(t > 0 for t in ms)
+    assert float(out.item()) == n  # the last READ summed n ones

@@ -1,0 +1,39 @@
+"""Host logic of the measurement harness (no GPU): the naive variant's score
+traffic model and the one-schema CSV / Markdown / JSON output."""
+import csv
+import json
+
+import pytest
+
+from roofline_benchmarking_gb300 import harness, inputs
+
+
+def test_naive_score_traffic_model():
+    w = inputs.F32_S1024                      # 8 heads, S = 1024, all S^2 scores visible
+    assert harness.naive_score_bytes(w) == 5 * 4 * 8 * 1024 * 1024
+    wc = inputs.F32_S1024_CAUSAL              # the lower triangle including the diagonal
+    assert harness.naive_score_bytes(wc) == 5 * 4 * 8 * (1024 * 1025 / 2)
+
+
+def test_outputs_share_one_schema(tmp_path):
+    row = {k: 0 for k in harness.FIELDS}
+    row.update(kernel="attention", workload="w", variant="TC", dtype="bf16", block="", p50_ms=0.2, min_ms=0.19,
+               mean_ms=0.2, p99_ms=0.21, tflops=1200.0, gbs=1000.0, bound="tensor", attainable=1961.8,
+               roofline_unit="TFLOP/s", roofline_frac=0.61, sm_mhz=1900.0, clock_reasons="none", iters=10)
+    meta = {"device": "GPU", "sms": 152, "peaks": {"bf16_tflops": 1961.8, "hbm_gbs": 6655.3}, "peaks_source": "measured",
+            "theoretical_hbm_gbs": 7928.0, "fp32_peak_tflops": 80.5}
+    md = harness.write_outputs([row, dict(row, kernel="triad", block=256)], str(tmp_path), meta)
+    assert md.count("\n| ") == 3 and "0.610" in md
+    lines = (tmp_path / "results.jsonl").read_text().splitlines()
+    assert json.loads(lines[0])["meta"]["sms"] == 152 and len(lines) == 3
+    rows = list(csv.DictReader(open(tmp_path / "results.csv")))
+    assert [r["kernel"] for r in rows] == ["attention", "triad"] and list(rows[0]) == harness.FIELDS
+
+
+@pytest.mark.gpu
+def test_harness_runs_a_quick_sweep(tmp_path):
+    assert harness.main(["--only", "f32_b1h1s64d32", "--no-hbm", "--seconds", "0.02",
+                         "--out", str(tmp_path)]) == 0
+    rows = [json.loads(x) for x in (tmp_path / "results.jsonl").read_text().splitlines()[1:]]
+    assert {r["variant"] for r in rows} == {"NAIVE", "FUSED", "FLASH"}
+    assert all(r["p50_ms"] > 0 and 0 < r["roofline_frac"] < 2 for r in rows)
