@@ -226,7 +226,8 @@ def run_reference(args, d: Dist):
 # ----------------------------------------------------------------------------- our arm
 def triad_ceiling(kbattn, dev_info) -> dict:
     """STREAM Triad over three 2 GiB fp32 arrays; the TileOPs protocol: 100
-    warm-up launches, then 5 runs of 200 timed launches, per block size."""
+    warm-up launches, then 5 runs of 200 timed launches, per block size
+    (128/256/512 as on the page, plus 1024); the best run calibrates."""
     import torch
 
     from roofline_benchmarking_gb300 import inputs
@@ -238,7 +239,7 @@ def triad_ceiling(kbattn, dev_info) -> dict:
     c = torch.full((n,), 2.0, dtype=torch.float32, device="cuda")
     nbytes = 3.0 * n * 4
     best, per_block = 0.0, {}
-    for block in (128, 256, 512):
+    for block in (128, 256, 512, 1024):
         kbattn.kb_triad_bench(a, b, c, 3.0, block=block, warmup=100, iters=1)
         runs = []
         for _ in range(5):

@@ -152,7 +152,8 @@ KB_API int kb_attn_bench(const void* q, const void* k, const void* v, void* o,
  *   a       : device pointer, n floats, written
  *   b, c    : const device pointers, n floats
  *   n       : element count (0 is a no-op)
- *   block   : threads per block, one of 128, 256, 512 (0 picks 256)
+ *   block   : threads per block, one of 128, 256, 512 (the TileOPs sweep) or
+ *             1024 (0 picks 256)
  * Pointers must be 16-byte aligned (float4 accesses); any n is accepted, the
  * tail that is not a multiple of 4 is handled with scalar accesses.
  */

@@ -250,7 +250,7 @@ int kb_triad(float* a, const float* b, const float* c, float s, size_t n, int bl
   if (!a || !b || !c) return KB_ERR_INVALID_ARG;
   if (!aligned16(a) || !aligned16(b) || !aligned16(c)) return KB_ERR_INVALID_ARG;
   if (block == 0) block = 256;
-  if (block != 128 && block != 256 && block != 512) return KB_ERR_INVALID_ARG;
+  if (block != 128 && block != 256 && block != 512 && block != 1024) return KB_ERR_INVALID_ARG;
   int st = check_device();
   if (st != KB_OK) return st;
   cudaError_t e = launch_triad(a, b, c, s, n, block, static_cast<cudaStream_t>(stream));
@@ -270,7 +270,7 @@ int hbm_args(const void* a, const void* b, const void* c, size_t n, int* block) 
   if (!a || !b || !c) return KB_ERR_INVALID_ARG;
   if (!aligned16(a) || !aligned16(b) || !aligned16(c)) return KB_ERR_INVALID_ARG;
   if (*block == 0) *block = 256;
-  if (*block != 128 && *block != 256 && *block != 512) return KB_ERR_INVALID_ARG;
+  if (*block != 128 && *block != 256 && *block != 512 && *block != 1024) return KB_ERR_INVALID_ARG;
   return check_device();
 }
 }  // namespace

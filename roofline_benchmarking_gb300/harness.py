@@ -12,7 +12,7 @@ and effective GB/s) and "Analysis" (each kernel placed against min(compute
 ceiling, intensity x bandwidth ceiling)); the TileOPs "Hardware Microbenchmarks"
 README, "Methodology" (Triad, copy, read-only and write-only; 100 warm-up
 launches, 5 runs of 200 timed launches, best and median, block sizes
-128/256/512, 2 GiB arrays).
+128/256/512 -- plus 1024 here -- on 2 GiB arrays).
 
 Correctness is not checked here (the harness is product code and never runs
 the oracle); the parity of every row is covered by the GPU tests.
@@ -105,7 +105,7 @@ def hbm_rows(peaks, dev_info, quick, sampler, only) -> list[dict]:
         if only and only not in name:
             continue
         nbytes = kbattn.HBM_BYTES_PER_ELEMENT[op] * n
-        for block in (128, 256, 512):
+        for block in (128, 256, 512, 1024):
             kbattn.kb_hbm_bench(op, a, b, c, 3.0, out, block=block, warmup=warm, iters=1)
             t0 = time.time()
             per_run = [kbattn.kb_hbm_bench(op, a, b, c, 3.0, out, block=block, warmup=0, iters=iters)
@@ -159,6 +159,7 @@ def main(argv=None) -> int:
     p.add_argument("--seconds", type=float, default=0.5, help="timed seconds per attention row")
     p.add_argument("--quick", action="store_true", help="small HBM arrays and few repetitions")
     p.add_argument("--no-hbm", action="store_true")
+    p.add_argument("--no-attention", action="store_true")
     args = p.parse_args(argv)
     if not torch.cuda.is_available():
         print("the harness needs a CUDA GPU", file=sys.stderr)
@@ -175,7 +176,7 @@ def main(argv=None) -> int:
     rows = []
     only = args.only.lower()
     try:
-        for w in inputs.WORKLOADS.values():
+        for w in ([] if args.no_attention else inputs.WORKLOADS.values()):
             for variant in ATTN_VARIANTS[w.dtype]:
                 if only and only not in w.name.lower() and only not in variant.name.lower():
                     continue

@@ -18,7 +18,7 @@ def lib():
     return kbattn.load()
 
 
-@pytest.mark.parametrize("block", [128, 256, 512])
+@pytest.mark.parametrize("block", [128, 256, 512, 1024])
 @pytest.mark.parametrize("n", [1, 3, 4, 5, 1023, 4099, (1 << 20) + 7, 3 * (1 << 22) + 2])
 def test_triad_bit_exact(oracle, n, block):
     b, c = inputs.make_triad_inputs(n, seed=n)
@@ -52,7 +52,7 @@ def test_device_info_is_gb300_class():
     assert info["sm_count"] > 100 and info["mem_bus_width_bits"] > 0 and info["mem_clock_khz"] > 0
 
 
-@pytest.mark.parametrize("block", [128, 256, 512])
+@pytest.mark.parametrize("block", [128, 256, 512, 1024])
 @pytest.mark.parametrize("n", [1, 3, 4, 1023, 4099, (1 << 20) + 7])
 def test_copy_write_read_match_oracle(oracle, n, block):
     b, _ = inputs.make_triad_inputs(n, seed=n + 1)
