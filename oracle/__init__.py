@@ -58,6 +58,8 @@ class Oracle:
         lib.kb_oracle_attn_rows.restype = ctypes.c_int
         lib.kb_oracle_triad.argtypes = [_FP, _FP, _FP, ctypes.c_float, _I64]
         lib.kb_oracle_triad.restype = ctypes.c_int
+        lib.kb_oracle_lse.argtypes = [_DP, _DP, _DP, _I64, _I64, _I64, ctypes.c_int, ctypes.c_double]
+        lib.kb_oracle_lse.restype = ctypes.c_int
         lib.kb_oracle_copy.argtypes = [_FP, _FP, _I64]
         lib.kb_oracle_copy.restype = ctypes.c_int
         lib.kb_oracle_fill.argtypes = [_FP, ctypes.c_float, _I64]
@@ -124,6 +126,19 @@ class Oracle:
             raise ValueError(f"kb_oracle_triad returned {rc}")
         return a
 
+
+    def lse(self, q, k, causal: bool, scale: float) -> np.ndarray:
+        """log(sum_j exp(score_ij)) over the visible keys; q, k [B, H, S, d] -> [B, H, S]."""
+        q, k = self._f64(q), self._f64(k)
+        if q.ndim != 4 or q.shape != k.shape:
+            raise ValueError("q and k must share one [B,H,S,d] shape")
+        B, H, S, d = q.shape
+        out = np.empty((B, H, S), dtype=np.float64)
+        rc = self.lib.kb_oracle_lse(q.ctypes.data_as(_DP), k.ctypes.data_as(_DP), out.ctypes.data_as(_DP),
+                                    B * H, S, d, int(bool(causal)), float(scale))
+        if rc != 0:
+            raise ValueError(f"kb_oracle_lse returned {rc}")
+        return out
 
     def copy(self, b) -> np.ndarray:
         b = np.ascontiguousarray(np.asarray(b, dtype=np.float32))

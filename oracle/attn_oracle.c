@@ -47,36 +47,43 @@
 #define KB_ORACLE_NO_MEMORY 4
 
 /*
- * One query row of one head.
- *   q, k, v : [N, S, d] row-major, N = B*H (head n = b*H + h)
- *   o_row   : d outputs for query i of head n
- *   p       : caller-provided scratch of S doubles
- *
- * Steps, each as written on the kbench page (one query row at a time):
+ * Steps 1-3 for one query row of one head, as written on the kbench page
+ * (one query row at a time):
  *   1. score s_j = scale * sum_c q[n,i,c] * k[n,j,c]   for every key j
  *   2. causal: keys j > i are left out (probability exactly 0)
  *   3. m = max_j s_j over the visible keys
+ *   q, k : [N, S, d] row-major, N = B*H (head n = b*H + h)
+ *   p    : caller-provided scratch of S doubles; receives the scores
+ * Returns the index of the last visible key; *m_out receives m.
+ */
+static int64_t row_scores(const double* q, const double* k, double* p, int64_t S, int64_t d, int causal,
+                          double scale, int64_t n, int64_t i, double* m_out) {
+  const double* qi = q + (n * S + i) * d;
+  const double* kh = k + n * S * d;
+  int64_t last = causal ? i : S - 1; /* last visible key */
+  for (int64_t j = 0; j <= last; ++j) {
+    double dot = 0.0;
+    for (int64_t c = 0; c < d; ++c) dot += qi[c] * kh[j * d + c];
+    p[j] = scale * dot;
+  }
+  double m = p[0];
+  for (int64_t j = 1; j <= last; ++j)
+    if (p[j] > m) m = p[j];
+  *m_out = m;
+  return last;
+}
+
+/*
+ * One query row of one head, steps 4-5 after row_scores:
  *   4. p_j = exp(s_j - m), l = sum_j p_j
  *   5. o[c] = (sum_j p_j * v[n,j,c]) / l
  */
 static void attn_one_row(const double* q, const double* k, const double* v,
                          double* o_row, double* p, int64_t S, int64_t d,
                          int causal, double scale, int64_t n, int64_t i) {
-  const double* qi = q + (n * S + i) * d;
-  const double* kh = k + n * S * d;
   const double* vh = v + n * S * d;
-  int64_t last = causal ? i : S - 1; /* last visible key */
-
-  /* 1. scores */
-  for (int64_t j = 0; j <= last; ++j) {
-    double dot = 0.0;
-    for (int64_t c = 0; c < d; ++c) dot += qi[c] * kh[j * d + c];
-    p[j] = scale * dot;
-  }
-  /* 3. row maximum over the visible keys */
-  double m = p[0];
-  for (int64_t j = 1; j <= last; ++j)
-    if (p[j] > m) m = p[j];
+  double m;
+  int64_t last = row_scores(q, k, p, S, d, causal, scale, n, i, &m);
   /* 4. unnormalised probabilities and their sum */
   double l = 0.0;
   for (int64_t j = 0; j <= last; ++j) {
@@ -110,6 +117,30 @@ int kb_oracle_attn(const double* q, const double* k, const double* v, double* o,
   for (int64_t n = 0; n < N; ++n)
     for (int64_t i = 0; i < S; ++i)
       attn_one_row(q, k, v, o + (n * S + i) * d, p, S, d, causal, scale, n, i);
+  free(p);
+  return KB_ORACLE_OK;
+}
+
+/*
+ * Log-sum-exp of every score row: lse[n,i] = log(sum_j exp(s_j)) over the
+ * visible keys (the natural log of the softmax denominator; the flash page's
+ * running max m and denominator l give it as m + log l). Computed as
+ * m + log(sum_j exp(s_j - m)) with the row maximum m. lse is [N, S].
+ */
+int kb_oracle_lse(const double* q, const double* k, double* lse, int64_t N, int64_t S, int64_t d,
+                  int causal, double scale) {
+  if (N < 1 || !lse || !attn_args_ok(q, k, k, lse, S, d, scale)) return KB_ORACLE_BAD_ARG;
+  double* p = (double*)malloc((size_t)S * sizeof(double));
+  if (!p) return KB_ORACLE_NO_MEMORY;
+  for (int64_t n = 0; n < N; ++n) {
+    for (int64_t i = 0; i < S; ++i) {
+      double m;
+      int64_t last = row_scores(q, k, p, S, d, causal, scale, n, i, &m);
+      double l = 0.0;
+      for (int64_t j = 0; j <= last; ++j) l += exp(p[j] - m);
+      lse[n * S + i] = m + log(l);
+    }
+  }
   free(p);
   return KB_ORACLE_OK;
 }

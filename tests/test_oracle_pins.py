@@ -264,6 +264,43 @@ def pin_triad_stream_constants(orc):
     assert np.all(a == 7.0)
 
 
+def pin_lse(orc):
+    """log-sum-exp of the score rows: 40-digit brute force, and closed forms."""
+    rng = _rng(24)
+    try:
+        import mpmath
+        mpmath.mp.dps = 40
+        mexp, mlog, mpf = mpmath.exp, mpmath.log, mpmath.mpf
+    except ImportError:  # pragma: no cover
+        mexp, mlog, mpf = math.exp, math.log, float
+    for (B, H, S, d) in [(1, 1, 1, 2), (1, 2, 5, 3), (2, 1, 6, 4)]:
+        for causal in (False, True):
+            q, k = _rand(rng, (B, H, S, d), -2, 2), _rand(rng, (B, H, S, d), -2, 2)
+            scale = 0.7
+            got = orc.lse(q, k, causal, scale)
+            for b in range(B):
+                for h in range(H):
+                    for i in range(S):
+                        last = i if causal else S - 1
+                        z = sum(mexp(mpf(scale) * sum(mpf(float(q[b, h, i, c])) * mpf(float(k[b, h, j, c]))
+                                                      for c in range(d))) for j in range(last + 1))
+                        assert abs(got[b, h, i] - float(mlog(z))) < 1e-13
+    # Q = 0: every visible score is 0, so lse = log(#visible keys)
+    S = 9
+    z = orc.lse(np.zeros((1, 2, S, 3)), _rand(rng, (1, 2, S, 3)), True, 0.5)
+    assert np.max(np.abs(z - np.log(np.arange(1, S + 1))[None, None, :])) < TOL
+    z = orc.lse(np.zeros((1, 2, S, 3)), _rand(rng, (1, 2, S, 3)), False, 0.5)
+    assert np.max(np.abs(z - math.log(S))) < TOL
+    # S = 1: lse is the single score; huge scores do not overflow (the max is subtracted)
+    q, k = _rand(rng, (1, 1, 1, 4)), _rand(rng, (1, 1, 1, 4))
+    assert abs(orc.lse(q, k, False, 1e5)[0, 0, 0] - 1e5 * float(q[0, 0, 0] @ k[0, 0, 0])) < 1e-6
+    # shifting every key by u shifts row i by scale * q_i . u
+    q, k = _rand(rng, (1, 1, 7, 3)), _rand(rng, (1, 1, 7, 3))
+    u = _rand(rng, (3,), -2, 2)
+    d0, d1 = orc.lse(q, k, True, 0.9), orc.lse(q, k + u, True, 0.9)
+    assert np.max(np.abs(d1 - d0 - 0.9 * (q[0, 0] @ u))) < 1e-12
+
+
 def pin_hbm_reference_kernels(orc):
     """copy, fill and sum on values whose exact results are known."""
     b = (np.arange(1, 5001) % 97).astype(np.float32)
@@ -278,7 +315,7 @@ PINS = [pin_brute_force, pin_rows_are_probabilities, pin_constant_v, pin_zero_qu
         pin_causal_first_row_and_single_key, pin_causal_is_prefix_attention, pin_key_permutation,
         pin_key_shift, pin_affine_in_v, pin_hard_attention_limit, pin_two_key_closed_form,
         pin_heads_are_independent, pin_rows_api_matches_full, pin_triad_exact,
-        pin_triad_stream_constants, pin_hbm_reference_kernels]
+        pin_triad_stream_constants, pin_hbm_reference_kernels, pin_lse]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -301,7 +338,7 @@ def test_oracle_rejects_bad_arguments(oracle):
 # planted mistakes: every one must fail at least one pin
 # --------------------------------------------------------------------------
 MUTANTS = {
-    "transposed_operand_v_for_k": ("dot += qi[c] * kh[j * d + c];", "dot += qi[c] * vh[j * d + c];"),
+    "transposed_key_operand": ("dot += qi[c] * kh[j * d + c];", "dot += qi[c] * kh[c * S + j];"),
     "dropped_scale": ("p[j] = scale * dot;", "p[j] = dot;"),
     "mask_off_by_one": ("int64_t last = causal ? i : S - 1;",
                         "int64_t last = causal ? (i > 0 ? i - 1 : 0) : S - 1;"),
@@ -318,6 +355,7 @@ MUTANTS = {
     "triad_swapped_operands": ("a[i] = fmaf(s, c[i], b[i]);", "a[i] = fmaf(s, b[i], c[i]);"),
     "copy_off_by_one": ("for (int64_t i = 0; i < n; ++i) a[i] = b[i];",
                         "for (int64_t i = 1; i < n; ++i) a[i] = b[i - 1];"),
+    "lse_drops_max": ("      lse[n * S + i] = m + log(l);", "      lse[n * S + i] = log(l);"),
     "sum_drops_last": ("for (int64_t i = 0; i < n; ++i) acc += (double)b[i];",
                        "for (int64_t i = 0; i + 1 < n; ++i) acc += (double)b[i];"),
 }
