@@ -122,6 +122,20 @@ KB_API int kb_attn_fwd(const void* q, const void* k, const void* v, void* o,
                 int B, int H, int S, int d, int causal, float scale,
                 int dtype, int variant, void* stream);
 
+/*
+ * kb_attn_fwd_lse -- kb_attn_fwd that also writes the log-sum-exp of every
+ * score row, lse[n, i] = log(sum over visible keys j of exp(scale * q_i.k_j)),
+ * the natural log of the softmax denominator (the flash kernel's running max m
+ * and denominator l give it as m + log l; kbench page, "The three GPU kernels").
+ *   lse     : device pointer, [B, H, S] fp32 (4-byte aligned), written in full
+ *   others  : as kb_attn_fwd
+ * Supported for KB_TC and KB_FLASH (and KB_AUTO); KB_NAIVE and KB_FUSED return
+ * KB_ERR_UNSUPPORTED.
+ */
+KB_API int kb_attn_fwd_lse(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int B, int H, int S, int d, int causal, float scale,
+                           int dtype, int variant, void* stream);
+
 /* Workspace bytes kb_attn_fwd_ws needs (0 for every variant but KB_NAIVE,
  * and 0 for an invalid request). */
 KB_API size_t kb_attn_workspace_bytes(int B, int H, int S, int d, int dtype, int variant);

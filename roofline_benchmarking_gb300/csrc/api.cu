@@ -128,11 +128,12 @@ int cached_workspace(size_t need, void** out) {
 
 int run_attention(const void* q, const void* k, const void* v, void* o, int B, int H, int S, int d, int causal,
                   float scale, int dtype, int variant, void* stream, void* workspace, size_t ws_bytes,
-                  bool caller_ws) {
+                  bool caller_ws, float* lse = nullptr) {
   int var = 0;
   int st = validate(q, k, v, o, B, H, S, d, causal, scale, dtype, variant, &var);
   if (st != KB_OK) return st;
   AttnProblem p{q, k, v, o, (int64_t)B * H, S, d, causal, scale, dtype};
+  p.lse = lse;
   float* scores = nullptr;
   if (var == KB_NAIVE) {
     const size_t need = naive_workspace_bytes(p.N, S);
@@ -216,6 +217,16 @@ int kb_version(void) { return 100; }
 int kb_attn_fwd(const void* q, const void* k, const void* v, void* o, int B, int H, int S, int d, int causal,
                 float scale, int dtype, int variant, void* stream) {
   return run_attention(q, k, v, o, B, H, S, d, causal, scale, dtype, variant, stream, nullptr, 0, false);
+}
+
+int kb_attn_fwd_lse(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int S, int d,
+                    int causal, float scale, int dtype, int variant, void* stream) {
+  if (!lse || (reinterpret_cast<uintptr_t>(lse) & 3u)) return KB_ERR_INVALID_ARG;
+  int var = 0;
+  int st = validate(q, k, v, o, B, H, S, d, causal, scale, dtype, variant, &var);
+  if (st != KB_OK) return st;
+  if (var != KB_TC && var != KB_FLASH) return KB_ERR_UNSUPPORTED;
+  return run_attention(q, k, v, o, B, H, S, d, causal, scale, dtype, variant, stream, nullptr, 0, false, lse);
 }
 
 size_t kb_attn_workspace_bytes(int B, int H, int S, int d, int dtype, int variant) {

@@ -118,8 +118,8 @@ template <int D>
 __global__ void __launch_bounds__(kThreads) flash_f32_kernel(const float* __restrict__ Q,
                                                              const float* __restrict__ K,
                                                              const float* __restrict__ V,
-                                                             float* __restrict__ O, int64_t N, int S,
-                                                             int causal, float scale_log2) {
+                                                             float* __restrict__ O, float* __restrict__ lse,
+                                                             int64_t N, int S, int causal, float scale_log2) {
   using C = Cols<D>;
   extern __shared__ float4 smem4[];
   float* Qs = reinterpret_cast<float*>(smem4);  // [D][kLD]
@@ -197,6 +197,8 @@ __global__ void __launch_bounds__(kThreads) flash_f32_kernel(const float* __rest
     const int row = q0 + ty * 4 + a;
     if (row >= S) continue;
     const float inv = 1.0f / l[a];
+    // natural log of sum_j exp(score): the scores sum to 2^m * l in base 2
+    if (lse != nullptr && tx == 0) lse[n * S + row] = (m[a] + log2f(l[a])) * 0.6931471805599453f;
     float* orow = O + (n * S + row) * D;
 #pragma unroll
     for (int g = 0; g < C::G; ++g)
@@ -398,7 +400,7 @@ cudaError_t flash_launch(const AttnProblem& p, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   const int64_t tiles = (p.S + kBR - 1) / kBR;
   flash_f32_kernel<D><<<(unsigned)(tiles * p.N), kThreads, smem, st>>>(
-      (const float*)p.q, (const float*)p.k, (const float*)p.v, (float*)p.o, p.N, p.S, p.causal,
+      (const float*)p.q, (const float*)p.k, (const float*)p.v, (float*)p.o, p.lse, p.N, p.S, p.causal,
       p.scale * kLog2e);
   return cudaGetLastError();
 }

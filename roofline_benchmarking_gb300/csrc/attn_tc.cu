@@ -168,8 +168,8 @@ struct Schedule {
 template <int D, bool F16>
 __global__ void __launch_bounds__(kThreadsTC, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                   const __grid_constant__ CUtensorMap tmv, uint8_t* __restrict__ out, int N, int S, int causal,
-                   float scale_log2, unsigned long long limit) {
+                   const __grid_constant__ CUtensorMap tmv, uint8_t* __restrict__ out, float* __restrict__ lse, int N,
+                   int S, int causal, float scale_log2, unsigned long long limit) {
   using C = TcCfg<D>;
   constexpr uint32_t kAB = F16 ? 0u : 1u;
   constexpr uint32_t IDESC_QK = ptx::f16_idesc(kBM, kBN, kAB, 0);
@@ -457,6 +457,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       if (ok) {
         ptx::tc_fence_after();
         const float inv = 1.0f / l_run;
+        // natural log of sum_j exp(score): the scores sum to 2^m_run * l_run in base 2
+        if (lse != nullptr && row < S) lse[(size_t)it.n * S + row] = (m_run + log2f(l_run)) * 0.6931471805599453f;
         uint8_t* orow = out + ((size_t)it.n * S + row) * (size_t)D * 2;
         uint32_t u[32];
 #pragma unroll 1
@@ -556,7 +558,7 @@ cudaError_t tc_launch(const AttnProblem& p, cudaStream_t st) {
   const int64_t items = (int64_t)((p.S + kPairRows - 1) / kPairRows) * p.N;
   const int64_t grid = items < sms ? items : sms;  // persistent: at most one CTA per SM
   attn_tc_kernel<D, F16><<<(unsigned)grid, kThreadsTC, C::SMEM, st>>>(
-      mq, mk, mv, static_cast<uint8_t*>(p.o), (int)p.N, p.S, p.causal, p.scale * 1.4426950408889634f,
+      mq, mk, mv, static_cast<uint8_t*>(p.o), p.lse, (int)p.N, p.S, p.causal, p.scale * 1.4426950408889634f,
       kDefaultWaitLimitNs);
   return cudaGetLastError();
 }

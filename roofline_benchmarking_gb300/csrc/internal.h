@@ -22,6 +22,7 @@ struct AttnProblem {
   int causal;
   float scale;
   int dtype;
+  float* lse = nullptr;  // optional [N, S] fp32 log-sum-exp of the score rows
 };
 
 // Launchers return a cudaError_t from the launch (or cudaSuccess).

@@ -80,6 +80,7 @@ _FP = ctypes.POINTER(ctypes.c_float)
 SIGNATURES = {
     "kb_attn_fwd": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P]),
     "kb_attn_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "kb_attn_fwd_lse": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P]),
     "kb_attn_fwd_ws": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P, _P, _SZ]),
     "kb_attn_bench": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P, _P, _SZ, _I, _I, _FP]),
     "kb_triad": (_I, [_P, _P, _P, _F, _SZ, _I, _P]),
@@ -208,6 +209,26 @@ def kb_attn_fwd(q, k, v, o=None, causal: bool = False, scale: float | None = Non
                             int(bool(causal)), float(scale), dt, int(variant), _stream_ptr(stream))
     _check(st, "kb_attn_fwd")
     return o
+
+
+def kb_attn_fwd_lse(q, k, v, o=None, lse=None, causal: bool = False, scale: float | None = None,
+                    variant: int = Variant.AUTO, stream=None):
+    """kb_attn_fwd that also returns the natural-log log-sum-exp of every score
+    row, an fp32 [B, H, S] tensor (written into ``lse`` if given)."""
+    import torch
+    if o is None:
+        o = torch.empty_like(q)
+    B, H, S, d, dt = _attn_args(q, k, v, o)
+    if lse is None:
+        lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
+    if not lse.is_cuda or lse.dtype != torch.float32 or not lse.is_contiguous() or lse.numel() != B * H * S:
+        raise ValueError("lse must be a contiguous fp32 CUDA tensor of B*H*S elements")
+    if scale is None:
+        scale = d ** -0.5
+    st = load().kb_attn_fwd_lse(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, S,
+                                d, int(bool(causal)), float(scale), dt, int(variant), _stream_ptr(stream))
+    _check(st, "kb_attn_fwd_lse")
+    return o, lse
 
 
 def kb_attn_workspace_bytes(B: int, H: int, S: int, d: int, dtype: int, variant: int) -> int:

@@ -135,6 +135,16 @@ def test_triad_and_bench_argument_checks(lib):
                            ms) == Status.INVALID_ARG
 
 
+def test_lse_argument_checks(lib):
+    L = kbattn.load()
+    args = (FAKE, FAKE, FAKE, FAKE)
+    assert L.kb_attn_fwd_lse(*args, None, 1, 1, 64, 64, 0, 0.125, DType.BF16, Variant.TC, None) == Status.INVALID_ARG
+    assert L.kb_attn_fwd_lse(*args, FAKE + 2, 1, 1, 64, 64, 0, 0.125, DType.BF16, Variant.TC, None) == Status.INVALID_ARG
+    for v in (Variant.NAIVE, Variant.FUSED):
+        assert L.kb_attn_fwd_lse(*args, FAKE, 1, 1, 64, 64, 0, 0.125, DType.F32, v, None) == Status.UNSUPPORTED
+    assert L.kb_attn_fwd_lse(*args, FAKE, 1, 1, 0, 64, 0, 0.125, DType.F32, Variant.FLASH, None) == Status.INVALID_ARG
+
+
 def test_hbm_argument_checks(lib):
     L = kbattn.load()
     assert L.kb_hbm_copy(FAKE, FAKE, 0, 256, None) == Status.OK          # n = 0 is a no-op
