@@ -10,7 +10,8 @@ precision, the attention forward O = softmax(Q K^T * scale [+ causal mask]) V
 of the kbench page ("kbench -- Transformer Attention Micro-benchmark Harness",
 section "Implementation details / The three GPU kernels") and the STREAM Triad
 a = b + s*c of the TileOPs "Hardware Microbenchmarks" README (section
-"HBM Bandwidth").
+"HBM Bandwidth"), and the page's Q15 fixed-point model of the microcontroller
+path (section "CPU reference + cache profiling").
 """
 from __future__ import annotations
 
@@ -43,6 +44,8 @@ _I64 = ctypes.c_int64
 _DP = ctypes.POINTER(ctypes.c_double)
 _FP = ctypes.POINTER(ctypes.c_float)
 _I64P = ctypes.POINTER(ctypes.c_int64)
+_I16P = ctypes.POINTER(ctypes.c_int16)
+_U16P = ctypes.POINTER(ctypes.c_uint16)
 
 
 class Oracle:
@@ -66,6 +69,11 @@ class Oracle:
         lib.kb_oracle_fill.restype = ctypes.c_int
         lib.kb_oracle_sum.argtypes = [_FP, _I64, _DP]
         lib.kb_oracle_sum.restype = ctypes.c_int
+        lib.kb_oracle_attn_q15.argtypes = [_I16P, _I16P, _I16P, _I16P, _I64, _I64, _I64, ctypes.c_int,
+                                           ctypes.c_double]
+        lib.kb_oracle_attn_q15.restype = ctypes.c_int
+        lib.kb_oracle_q15_exp_table.argtypes = [_U16P]
+        lib.kb_oracle_q15_exp_table.restype = ctypes.c_int
         self.lib = lib
         self.path = path
 
@@ -138,6 +146,28 @@ class Oracle:
                                     B * H, S, d, int(bool(causal)), float(scale))
         if rc != 0:
             raise ValueError(f"kb_oracle_lse returned {rc}")
+        return out
+
+    def attn_q15(self, q, k, v, causal: bool, scale: float) -> np.ndarray:
+        """The Q15 fixed-point model: int16 q, k, v [..., S, d] -> int16 O of the same shape."""
+        q, k, v = (np.ascontiguousarray(np.asarray(x.numpy() if hasattr(x, "numpy") else x, dtype=np.int16))
+                   for x in (q, k, v))
+        if q.ndim < 2 or q.shape != k.shape or q.shape != v.shape:
+            raise ValueError("q, k, v must share one [..., S, d] shape")
+        S, d = q.shape[-2], q.shape[-1]
+        N = int(np.prod(q.shape[:-2])) if q.ndim > 2 else 1
+        o = np.empty_like(q)
+        rc = self.lib.kb_oracle_attn_q15(q.ctypes.data_as(_I16P), k.ctypes.data_as(_I16P),
+                                         v.ctypes.data_as(_I16P), o.ctypes.data_as(_I16P),
+                                         N, S, d, int(bool(causal)), float(scale))
+        if rc != 0:
+            raise ValueError(f"kb_oracle_attn_q15 returned {rc}")
+        return o
+
+    def q15_exp_table(self) -> np.ndarray:
+        out = np.empty(64, dtype=np.uint16)
+        if self.lib.kb_oracle_q15_exp_table(out.ctypes.data_as(_U16P)) != 0:
+            raise ValueError("kb_oracle_q15_exp_table failed")
         return out
 
     def copy(self, b) -> np.ndarray:

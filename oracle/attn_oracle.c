@@ -201,3 +201,136 @@ int kb_oracle_triad(float* a, const float* b, const float* c, float s, int64_t n
   for (int64_t i = 0; i < n; ++i) a[i] = fmaf(s, c[i], b[i]);
   return KB_ORACLE_OK;
 }
+
+/* --------------------------------------------------------------------------
+ * Q15 fixed-point model of the microcontroller path.
+ *
+ * kbench page, section "CPU reference + cache profiling": the second CPU
+ * reference is a bit-accurate model of the board's fixed-point path, with Q15
+ * inputs, Q15.16 score accumulation and a 64-entry exp table. Section
+ * "ARM Cortex-M4 firmware": that path handles one query row at a time and
+ * streams the keys like the flash kernel, with an online-rescaled softmax, in
+ * scalar fixed point because the core has no hardware exp.
+ *
+ * The pages print neither the table nor any rounding rule. The readings taken
+ * here (the plainest fixed-point choices):
+ *   Q15      int16, value = x / 2^15.
+ *   Q15.16   int64 holding value * 2^16 (scores, in base-2 units).
+ *   score    the exact integer sum of the d products q_c * k_c (Q30), shifted
+ *            right by 14 (floor) to Q15.16, then multiplied by
+ *            C = round(scale * log2(e) * 2^16) and shifted right by 16
+ *            (floor), so that exp(x) becomes 2^z.
+ *   exp      2^(-t) for t >= 0 in Q15.16 is T[f] >> n, where n = floor(t),
+ *            f = the top 6 bits of the fraction of t, and the 64-entry table
+ *            holds T[f] = round(2^15 * 2^(-f/64)); the result is 0 once
+ *            n >= 16. Weights p are therefore Q15 in [0, 2^15].
+ *   stream   keys in tiles of 32 from key 0 (the last tile clipped to the
+ *            last visible key). For each tile: its scores and their maximum;
+ *            if the maximum rose above the running maximum m, scale l and
+ *            every acc_c by a = 2^(-(m_new - m)) (product shifted right by
+ *            15, floor) and set m = m_new; then for each key p = 2^(-(m - z)),
+ *            l += p, acc_c += p * v_c (exact, Q30).
+ *   output   o_c = acc_c / l rounded to nearest (halves away from zero),
+ *            saturated to int16.
+ * Limits that keep every intermediate inside int64: S <= 65536, d <= 1024,
+ * C <= 2^30.
+ * -------------------------------------------------------------------------- */
+#define KB_Q15_TILE 32
+#define KB_Q15_LOG2E 1.4426950408889634074
+
+/* floor(x / 2^s), written without relying on how >> treats negative values */
+static int64_t q15_floor_shift(int64_t x, int s) {
+  const int64_t p = (int64_t)1 << s;
+  return x >= 0 ? x / p : -((-x + p - 1) / p);
+}
+
+/* T[f] = round(2^15 * 2^(-f/64)), f = 0..63 */
+static void q15_exp_table(uint16_t t[64]) {
+  for (int f = 0; f < 64; ++f) t[f] = (uint16_t)llround(32768.0 * exp2(-(double)f / 64.0));
+}
+
+/* 2^(-t) in Q15 for t >= 0 in Q15.16, from the table */
+static int64_t q15_pow2_neg(int64_t t, const uint16_t tab[64]) {
+  const int64_t n = t / 65536;          /* integer part */
+  const int64_t f = (t % 65536) / 1024; /* top 6 bits of the fraction */
+  if (n >= 16) return 0;
+  return (int64_t)tab[f] / ((int64_t)1 << n);
+}
+
+/* a / b for b > 0, rounded to nearest with halves away from zero */
+static int64_t q15_round_div(int64_t a, int64_t b) {
+  return a >= 0 ? (a + b / 2) / b : -((-a + b / 2) / b);
+}
+
+/* One query row of one head; acc is scratch of d int64. */
+static void q15_one_row(const int16_t* q, const int16_t* k, const int16_t* v, int16_t* o_row,
+                        int64_t* acc, int64_t S, int64_t d, int causal, int64_t C,
+                        const uint16_t tab[64], int64_t n, int64_t i) {
+  const int16_t* qi = q + (n * S + i) * d;
+  const int16_t* kh = k + n * S * d;
+  const int16_t* vh = v + n * S * d;
+  const int64_t last_key = causal ? i : S - 1;
+  int64_t z[KB_Q15_TILE];
+  int64_t m = 0, l = 0;
+  int have_m = 0;
+  for (int64_t c = 0; c < d; ++c) acc[c] = 0;
+  for (int64_t t0 = 0; t0 <= last_key; t0 += KB_Q15_TILE) {
+    const int64_t t1 = t0 + KB_Q15_TILE - 1 < last_key ? t0 + KB_Q15_TILE - 1 : last_key;
+    /* scores of the tile (Q15.16, base 2) and the tile maximum */
+    int64_t mt = 0;
+    for (int64_t j = t0; j <= t1; ++j) {
+      int64_t dot = 0;
+      for (int64_t c = 0; c < d; ++c) dot += (int64_t)qi[c] * (int64_t)kh[j * d + c];
+      const int64_t s16 = q15_floor_shift(dot, 14);
+      z[j - t0] = q15_floor_shift(s16 * C, 16);
+      if (j == t0 || z[j - t0] > mt) mt = z[j - t0];
+    }
+    /* online rescale when the running maximum rises */
+    if (!have_m) {
+      m = mt;
+      have_m = 1;
+    } else if (mt > m) {
+      const int64_t a = q15_pow2_neg(mt - m, tab);
+      l = q15_floor_shift(l * a, 15);
+      for (int64_t c = 0; c < d; ++c) acc[c] = q15_floor_shift(acc[c] * a, 15);
+      m = mt;
+    }
+    /* weights of the tile's keys, accumulated */
+    for (int64_t j = t0; j <= t1; ++j) {
+      const int64_t p = q15_pow2_neg(m - z[j - t0], tab);
+      l += p;
+      for (int64_t c = 0; c < d; ++c) acc[c] += p * (int64_t)vh[j * d + c];
+    }
+  }
+  for (int64_t c = 0; c < d; ++c) {
+    int64_t r = q15_round_div(acc[c], l);
+    if (r > 32767) r = 32767;
+    if (r < -32768) r = -32768;
+    o_row[c] = (int16_t)r;
+  }
+}
+
+/* The 64-entry exp table of the Q15 model. */
+int kb_oracle_q15_exp_table(uint16_t* out) {
+  if (!out) return KB_ORACLE_BAD_ARG;
+  q15_exp_table(out);
+  return KB_ORACLE_OK;
+}
+
+/* Q15 attention forward over [N, S, d] int16 tensors (head n = b*H + h). */
+int kb_oracle_attn_q15(const int16_t* q, const int16_t* k, const int16_t* v, int16_t* o,
+                       int64_t N, int64_t S, int64_t d, int causal, double scale) {
+  if (!q || !k || !v || !o || N < 1 || S < 1 || S > 65536 || d < 1 || d > 1024) return KB_ORACLE_BAD_ARG;
+  if (!(scale > 0.0) || isinf(scale)) return KB_ORACLE_BAD_ARG;
+  const double cd = scale * KB_Q15_LOG2E * 65536.0;
+  if (!(cd <= 1073741824.0)) return KB_ORACLE_BAD_ARG;
+  const int64_t C = llround(cd);
+  uint16_t tab[64];
+  q15_exp_table(tab);
+  int64_t* acc = (int64_t*)malloc((size_t)d * sizeof(int64_t));
+  if (!acc) return KB_ORACLE_NO_MEMORY;
+  for (int64_t n = 0; n < N; ++n)
+    for (int64_t i = 0; i < S; ++i) q15_one_row(q, k, v, o + (n * S + i) * d, acc, S, d, causal, C, tab, n, i);
+  free(acc);
+  return KB_ORACLE_OK;
+}

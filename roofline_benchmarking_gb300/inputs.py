@@ -9,6 +9,8 @@ the workload's seed draws Q, then K, then V, each as a full fp32 [B, H, S, d]
 tensor. "uniform" is ``rand * 2 - 1`` (U[-1, 1]); "normal(0, sigma)" is
 ``randn * sigma`` (sigma is the standard deviation). bf16 workloads then round
 each fp32 draw to bf16 with round-to-nearest-even (``Tensor.to(torch.bfloat16)``).
+Q15 workloads (int16, value = x / 2^15) round each fp32 draw times 2^15 to the
+nearest integer (ties to even) and saturate it to [-32768, 32767].
 """
 from __future__ import annotations
 
@@ -26,7 +28,7 @@ class Workload:
     S: int
     d: int
     causal: bool
-    dtype: str          # "f32", "bf16" or "f16"
+    dtype: str          # "f32", "bf16", "f16" or "q15"
     seed: int
     dist: str           # "uniform" or "normal"
     sigma_qk: float = 1.0
@@ -68,14 +70,20 @@ BF16_S2048_D64 = Workload("bf16_b16h12s2048d64", 16, 12, 2048, 64, False, "bf16"
 BF16_CAUSAL_S16384 = Workload("bf16_causal_b1h32s16384d128_sharp", 1, 32, 16384, 128, True, "bf16", 4,
                               "normal", sigma_qk=3.0, sigma_v=1.0)
 
+# The Q15 fixed-point model runs on the fp32 workloads' shapes and draws.
+Q15_SINGLE_HEAD = SINGLE_HEAD_F32.with_(name="q15_b1h1s64d32", dtype="q15")
+Q15_S1024 = F32_S1024.with_(name="q15_b1h8s1024d64", dtype="q15")
+Q15_S1024_CAUSAL = F32_S1024_CAUSAL.with_(name="q15_b1h8s1024d64_causal", dtype="q15")
+
 WORKLOADS = {w.name: w for w in (SINGLE_HEAD_F32, F32_S1024, F32_S1024_CAUSAL,
-                                 BF16_CAUSAL_S4096, BF16_S2048_D64, BF16_CAUSAL_S16384)}
+                                 BF16_CAUSAL_S4096, BF16_S2048_D64, BF16_CAUSAL_S16384,
+                                 Q15_SINGLE_HEAD, Q15_S1024, Q15_S1024_CAUSAL)}
 
 # STREAM Triad working set: three fp32 arrays of 2 GiB each.
 TRIAD_ARRAY_BYTES = 2 << 30
 TRIAD_N = TRIAD_ARRAY_BYTES // 4
 
-_TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
+_TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16, "q15": torch.int16}
 
 
 def torch_dtype(dtype: str) -> torch.dtype:
@@ -96,8 +104,21 @@ def make_qkv(w: Workload):
             x = torch.randn(shape, generator=g, dtype=torch.float32) * sigma
         else:
             raise ValueError(f"unknown distribution {w.dist!r}")
-        out.append(x.to(torch_dtype(w.dtype)).contiguous())
+        if w.dtype == "q15":
+            out.append(to_q15(x))
+        else:
+            out.append(x.to(torch_dtype(w.dtype)).contiguous())
     return tuple(out)
+
+
+def to_q15(x: torch.Tensor) -> torch.Tensor:
+    """Storage rounding to Q15: round(x * 2^15) (ties to even), saturated to int16."""
+    return torch.round(x.float() * 32768.0).clamp(-32768, 32767).to(torch.int16).contiguous()
+
+
+def from_q15(x) -> torch.Tensor:
+    """The exact value an int16 Q15 tensor stands for, as float64."""
+    return torch.as_tensor(x).double() / 32768.0
 
 
 def sample_rows(w: Workload, per_head: int = 64, seed: int = 12345):
