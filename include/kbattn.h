@@ -66,7 +66,11 @@ typedef enum {
   KB_ERR_NO_DEVICE = 6    /* no usable sm_103 device */
 } kb_status;
 
-typedef enum { KB_F32 = 0, KB_BF16 = 1, KB_F16 = 2 } kb_dtype;
+/*
+ * Element types. KB_Q15 is int16 fixed point, value = x / 2^15 (the kbench
+ * page's fixed-point path, section "CPU reference + cache profiling").
+ */
+typedef enum { KB_F32 = 0, KB_BF16 = 1, KB_F16 = 2, KB_Q15 = 3 } kb_dtype;
 
 /*
  * Variants (kbench page, "The three GPU kernels"; the tensor-core variant is
@@ -80,9 +84,23 @@ typedef enum { KB_F32 = 0, KB_BF16 = 1, KB_F16 = 2 } kb_dtype;
  *             matrix never materialised; CUDA cores. fp32 only.
  *  KB_TC    : tiled, online softmax on the 5th-generation tensor cores
  *             (tcgen05 MMAs into tensor memory, TMA-staged tiles). bf16/f16.
- *  KB_AUTO  : KB_TC for bf16/f16, KB_FLASH for fp32.
+ *  KB_FIXEDPOINT : the Q15 fixed-point path (kbench page, "CPU reference +
+ *             cache profiling" and "ARM Cortex-M4 firmware"), integer
+ *             arithmetic only, defined bit for bit. KB_Q15 only. Q15 inputs;
+ *             score = floor(floor(sum_c q_c*k_c / 2^14) * C / 2^16) in Q15.16
+ *             base-2 units with C = round(scale*log2(e)*2^16); keys in tiles of
+ *             32 from key 0 with an online-rescaled softmax whose weights come
+ *             from a 64-entry table T[f] = round(2^15 * 2^(-f/64))
+ *             (2^(-t) = T[top 6 fraction bits of t] >> floor(t), 0 once
+ *             floor(t) >= 16); l and the 64-bit accumulators are rescaled by
+ *             floor(x * 2^(-dm) / 2^15) when the running maximum rises by dm;
+ *             o = acc / l rounded to nearest (halves away from zero),
+ *             saturated to int16. Requires S <= 65536 and
+ *             scale*log2(e)*2^16 <= 2^30 (else KB_ERR_INVALID_ARG).
+ *  KB_AUTO  : KB_TC for bf16/f16, KB_FLASH for fp32, KB_FIXEDPOINT for Q15.
  */
-typedef enum { KB_AUTO = 0, KB_NAIVE = 1, KB_FUSED = 2, KB_FLASH = 3, KB_TC = 4 } kb_variant;
+typedef enum { KB_AUTO = 0, KB_NAIVE = 1, KB_FUSED = 2, KB_FLASH = 3, KB_TC = 4,
+               KB_FIXEDPOINT = 5 } kb_variant;
 
 /* Device properties used by the roofline peak formulas. */
 typedef struct {
@@ -159,6 +177,26 @@ KB_API int kb_attn_bench(const void* q, const void* k, const void* v, void* o,
                   int dtype, int variant, void* stream,
                   void* workspace, size_t ws_bytes,
                   int warmup, int iters, float* ms_per_iter);
+
+/*
+ * kb_attn_bench_graph -- the kbench page, section "Implementation details"
+ * (launch overhead of tiny problems, measured with the launches captured in
+ * a CUDA graph): `launches` consecutive kb_attn_fwd(_ws) calls are captured
+ * into one CUDA graph on a private stream, then the graph is launched on
+ * `stream` `warmup` times untimed and `iters` times between CUDA events;
+ * ms_per_graph[t] (host array of `iters` floats) receives the t-th graph's
+ * device time, so one call costs ms_per_graph[t] / launches.
+ *   launches : 1 ... 100000 (else KB_ERR_INVALID_ARG)
+ * Before capturing, one plain call runs and `stream` is synchronised (it
+ * validates the arguments and sets up any cached workspace). Arguments are
+ * validated as in kb_attn_fwd; a failed call inside the capture ends the
+ * capture and its status is returned. The graph is destroyed before return.
+ */
+KB_API int kb_attn_bench_graph(const void* q, const void* k, const void* v, void* o,
+                               int B, int H, int S, int d, int causal, float scale,
+                               int dtype, int variant, void* stream,
+                               void* workspace, size_t ws_bytes,
+                               int launches, int warmup, int iters, float* ms_per_graph);
 
 /*
  * kb_triad -- STREAM Triad a[i] = b[i] + s*c[i] for i < n, fp32, computed as
@@ -262,6 +300,13 @@ KB_API int kb_last_cuda_error(void);
 
 /* Library ABI version: 100 * major + minor. */
 KB_API int kb_version(void);
+
+/*
+ * kb_q15_exp_table -- the 64-entry table of the KB_FIXEDPOINT path,
+ * out64[f] = round(2^15 * 2^(-f/64)) (out64: host array of 64 entries).
+ * Host only, no CUDA call. KB_ERR_INVALID_ARG for a null pointer.
+ */
+KB_API int kb_q15_exp_table(unsigned short* out64);
 
 #ifdef __cplusplus
 }

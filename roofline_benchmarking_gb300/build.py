@@ -18,7 +18,7 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIBRARY = os.path.join(HERE, "libkbattn.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
-SOURCES = ["api.cu", "attn_fp32.cu", "attn_tc.cu", "hbm.cu", "naive_noalloc.cu"]
+SOURCES = ["api.cu", "attn_fp32.cu", "attn_tc.cu", "attn_q15.cu", "hbm.cu", "naive_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
               "-Xcompiler", "-fvisibility=hidden"]

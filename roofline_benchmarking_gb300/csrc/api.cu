@@ -32,8 +32,8 @@ int validate(const void* q, const void* k, const void* v, const void* o, int B, 
   if (B < 1 || H < 1 || S < 1 || d < 1) return KB_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return KB_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.0f)) return KB_ERR_INVALID_ARG;
-  if (dtype != KB_F32 && dtype != KB_BF16 && dtype != KB_F16) return KB_ERR_INVALID_ARG;
-  if (variant < KB_AUTO || variant > KB_TC) return KB_ERR_INVALID_ARG;
+  if (dtype != KB_F32 && dtype != KB_BF16 && dtype != KB_F16 && dtype != KB_Q15) return KB_ERR_INVALID_ARG;
+  if (variant < KB_AUTO || variant > KB_FIXEDPOINT) return KB_ERR_INVALID_ARG;
   // B*H*S*d elements, times 4 bytes, must fit in int64; B*H in int32.
   const int64_t N = (int64_t)B * H;
   if (N > std::numeric_limits<int32_t>::max()) return KB_ERR_INVALID_ARG;
@@ -41,9 +41,15 @@ int validate(const void* q, const void* k, const void* v, const void* o, int B, 
   if (N > lim / S || N * S > lim / d) return KB_ERR_INVALID_ARG;
   if (d != 32 && d != 64 && d != 128) return KB_ERR_UNSUPPORTED;
   int var = variant;
-  if (var == KB_AUTO) var = dtype == KB_F32 ? KB_FLASH : KB_TC;
+  if (var == KB_AUTO) var = dtype == KB_F32 ? KB_FLASH : (dtype == KB_Q15 ? KB_FIXEDPOINT : KB_TC);
+  if ((dtype == KB_Q15) != (var == KB_FIXEDPOINT)) return KB_ERR_UNSUPPORTED;
   if (dtype == KB_F32 && var == KB_TC) return KB_ERR_UNSUPPORTED;
-  if (dtype != KB_F32 && var != KB_TC) return KB_ERR_UNSUPPORTED;
+  if ((dtype == KB_BF16 || dtype == KB_F16) && var != KB_TC) return KB_ERR_UNSUPPORTED;
+  if (var == KB_FIXEDPOINT) {
+    // keeps every fixed-point intermediate inside 64 bits
+    if (S > 65536 || !q15_scale_ok(scale)) return KB_ERR_INVALID_ARG;
+    if (N * ((S + 31) / 32) > std::numeric_limits<int32_t>::max()) return KB_ERR_UNSUPPORTED;
+  }
   // one block per query row (fused) or per 64-row tile (flash, naive)
   const int64_t grid_limit = std::numeric_limits<int32_t>::max();
   if (var == KB_FUSED && N * S > grid_limit) return KB_ERR_UNSUPPORTED;
@@ -161,6 +167,7 @@ int run_attention(const void* q, const void* k, const void* v, void* o, int B, i
     case KB_FUSED: e = launch_fused_f32(p, cs); break;
     case KB_FLASH: e = launch_flash_f32(p, cs); break;
     case KB_TC: e = launch_tc(p, cs); break;
+    case KB_FIXEDPOINT: e = launch_q15(p, cs); break;
     default: return KB_ERR_UNSUPPORTED;
   }
   return e == cudaSuccess ? KB_OK : cuda_fail(e);
@@ -214,6 +221,11 @@ extern "C" {
 
 int kb_version(void) { return 100; }
 
+int kb_q15_exp_table(unsigned short* out64) {
+  if (!out64) return KB_ERR_INVALID_ARG;
+  return kb::q15_exp_table(out64);
+}
+
 int kb_attn_fwd(const void* q, const void* k, const void* v, void* o, int B, int H, int S, int d, int causal,
                 float scale, int dtype, int variant, void* stream) {
   return run_attention(q, k, v, o, B, H, S, d, causal, scale, dtype, variant, stream, nullptr, 0, false);
@@ -254,6 +266,49 @@ int kb_attn_bench(const void* q, const void* k, const void* v, void* o, int B, i
                          use_ws);
   };
   return time_calls(call, static_cast<cudaStream_t>(stream), warmup, iters, ms_per_iter);
+}
+
+int kb_attn_bench_graph(const void* q, const void* k, const void* v, void* o, int B, int H, int S, int d,
+                        int causal, float scale, int dtype, int variant, void* stream, void* workspace,
+                        size_t ws_bytes, int launches, int warmup, int iters, float* ms_per_graph) {
+  if (launches < 1 || launches > 100000 || warmup < 0 || iters < 1 || !ms_per_graph) return KB_ERR_INVALID_ARG;
+  int var = 0;
+  int st = validate(q, k, v, o, B, H, S, d, causal, scale, dtype, variant, &var);
+  if (st != KB_OK) return st;
+  const bool use_ws = workspace != nullptr;
+  // One plain call first: it checks the device and grows the cached workspace,
+  // so nothing inside the capture allocates or synchronises.
+  cudaStream_t user = static_cast<cudaStream_t>(stream);
+  st = run_attention(q, k, v, o, B, H, S, d, causal, scale, dtype, variant, user, workspace, ws_bytes, use_ws);
+  if (st != KB_OK) return st;
+  cudaError_t e = cudaStreamSynchronize(user);
+  if (e != cudaSuccess) return cuda_fail(e);
+  // Capture on a private stream (the caller's may be the legacy stream, which
+  // cannot be captured); the instantiated graph is then launched on `stream`.
+  cudaStream_t cap = nullptr;
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  if ((e = cudaStreamCreateWithFlags(&cap, cudaStreamNonBlocking)) != cudaSuccess) return cuda_fail(e);
+  e = cudaStreamBeginCapture(cap, cudaStreamCaptureModeThreadLocal);
+  if (e == cudaSuccess) {
+    for (int t = 0; t < launches && st == KB_OK; ++t)
+      st = run_attention(q, k, v, o, B, H, S, d, causal, scale, dtype, variant, cap, workspace, ws_bytes, use_ws);
+    cudaError_t e2 = cudaStreamEndCapture(cap, &graph);  // ends the capture even after a failed call
+    if (st == KB_OK) e = e2;
+  }
+  if (st == KB_OK && e == cudaSuccess) e = cudaGraphInstantiate(&exec, graph, 0);
+  if (st == KB_OK && e == cudaSuccess) {
+    auto call = [&]() {
+      cudaError_t le = cudaGraphLaunch(exec, user);
+      return le == cudaSuccess ? (int)KB_OK : cuda_fail(le);
+    };
+    st = time_calls(call, user, warmup, iters, ms_per_graph);
+  }
+  if (exec) cudaGraphExecDestroy(exec);
+  if (graph) cudaGraphDestroy(graph);
+  cudaStreamDestroy(cap);
+  if (st != KB_OK) return st;
+  return e == cudaSuccess ? KB_OK : cuda_fail(e);
 }
 
 int kb_triad(float* a, const float* b, const float* c, float s, size_t n, int block, void* stream) {

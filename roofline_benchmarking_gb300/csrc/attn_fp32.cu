@@ -320,8 +320,13 @@ __global__ void __launch_bounds__(kThreads) naive_pv_kernel(const float* __restr
 
 // ---------------------------------------------------------------------------
 // fused: one block per (head, query row); the score row lives in shared memory.
+// Key tiles of 64 rows are staged in shared memory with coalesced loads and
+// each dot product is split over 4 threads, thread q of a key taking float4
+// q, q + 4, ...; rows are padded by 16 floats so that the 8 threads of one
+// 128-bit load phase (2 keys x 4 parts) touch 8 distinct bank groups.
 // ---------------------------------------------------------------------------
-constexpr int kFusedThreads = 128;
+constexpr int kFusedThreads = 256;
+constexpr int kFusedKeys = 64;  // keys per staged tile
 
 template <int D>
 __global__ void __launch_bounds__(kFusedThreads) fused_row_f32_kernel(const float* __restrict__ Q,
@@ -329,8 +334,10 @@ __global__ void __launch_bounds__(kFusedThreads) fused_row_f32_kernel(const floa
                                                                       const float* __restrict__ V,
                                                                       float* __restrict__ O, int S, int causal,
                                                                       float scale_log2) {
+  constexpr int LDK = D + 16;
   extern __shared__ float4 smem4[];
-  float* qs = reinterpret_cast<float*>(smem4);  // [D]
+  float* Ks = reinterpret_cast<float*>(smem4);  // [kFusedKeys][LDK]
+  float* qs = Ks + kFusedKeys * LDK;             // [D]
   float* red = qs + D;                           // [32]
   float* part = red + 32;                        // [kFusedThreads]
   float* sc = part + kFusedThreads;              // [S]
@@ -343,31 +350,45 @@ __global__ void __launch_bounds__(kFusedThreads) fused_row_f32_kernel(const floa
   const float* Vh = V + n * S * D;
 
   for (int c = tid; c < D; c += kFusedThreads) qs[c] = Q[(n * S + i) * D + c] * scale_log2;
-  __syncthreads();
 
+  // scores: thread tid works on key tid / 4 of the tile, float4 (tid % 4) + 4 t
+  const int kl = tid >> 2, qp = tid & 3;
   float tmax = -INFINITY;
-  for (int j = tid; j <= last; j += kFusedThreads) {
-    const float* kr = Kh + (int64_t)j * D;
+  for (int k0 = 0; k0 <= last; k0 += kFusedKeys) {
+    __syncthreads();  // the previous tile is no longer read (and qs is written)
+    for (int f = tid; f < kFusedKeys * (D / 4); f += kFusedThreads) {
+      const int r = f / (D / 4), c4 = f % (D / 4);
+      float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (k0 + r <= last) x = ld4(Kh + (int64_t)(k0 + r) * D + 4 * c4);
+      *reinterpret_cast<float4*>(Ks + r * LDK + 4 * c4) = x;
+    }
+    __syncthreads();
     float dot = 0.f;
 #pragma unroll
-    for (int c = 0; c < D; c += 4) {
-      const float4 kv = ld4(kr + c);
-      dot = fmaf(qs[c], kv.x, dot);
-      dot = fmaf(qs[c + 1], kv.y, dot);
-      dot = fmaf(qs[c + 2], kv.z, dot);
-      dot = fmaf(qs[c + 3], kv.w, dot);
+    for (int c = 4 * qp; c < D; c += 16) {
+      const float4 kv = ld4(Ks + kl * LDK + c);
+      const float4 qv = ld4(qs + c);
+      dot = fmaf(qv.x, kv.x, dot);
+      dot = fmaf(qv.y, kv.y, dot);
+      dot = fmaf(qv.z, kv.z, dot);
+      dot = fmaf(qv.w, kv.w, dot);
     }
-    sc[j] = dot;
-    tmax = fmaxf(tmax, dot);
+    dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+    dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+    const int key = k0 + kl;
+    if (qp == 0 && key <= last) {
+      sc[key] = dot;
+      tmax = fmaxf(tmax, dot);
+    }
   }
-  const float m = block_max(tmax, red);
+  const float m = block_max(tmax, red);  // its barriers also publish sc[]
   float tsum = 0.f;
   for (int j = tid; j <= last; j += kFusedThreads) {
     const float p = exp2f(sc[j] - m);
     sc[j] = p;
     tsum += p;
   }
-  const float l = block_sum(tsum, red);  // its barriers also publish sc[]
+  const float l = block_sum(tsum, red);  // its barriers also publish the new sc[]
 
   constexpr int R = kFusedThreads / D;  // key groups
   const int c = tid % D, g = tid / D;
@@ -386,7 +407,9 @@ __global__ void __launch_bounds__(kFusedThreads) fused_row_f32_kernel(const floa
 size_t flash_smem(int d) { return sizeof(float) * (size_t)(2 * d * kLD + kBC * d + kBC * kLD); }
 size_t naive_scores_smem(int d) { return sizeof(float) * (size_t)(2 * d * kLD); }
 size_t naive_pv_smem(int d) { return sizeof(float) * (size_t)(kBC * kLD + kBC * d); }
-size_t fused_smem(int S, int d) { return sizeof(float) * (size_t)(d + 32 + kFusedThreads + S); }
+size_t fused_smem(int S, int d) {
+  return sizeof(float) * (size_t)(kFusedKeys * (d + 16) + d + 32 + kFusedThreads + S);
+}
 
 template <typename F>
 cudaError_t set_smem(F* kernel, size_t bytes) {

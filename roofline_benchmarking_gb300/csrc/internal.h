@@ -36,6 +36,12 @@ int fused_f32_check(int S, int d);
 cudaError_t launch_tc(const AttnProblem& p, cudaStream_t st);
 int tc_check(int S, int d, int dtype);
 
+// Q15 fixed-point path: launcher, the scale limit (scale*log2(e)*2^16 <= 2^30)
+// and the 64-entry exp table it uses.
+cudaError_t launch_q15(const AttnProblem& p, cudaStream_t st);
+bool q15_scale_ok(float scale);
+int q15_exp_table(unsigned short* out);
+
 cudaError_t launch_triad(float* a, const float* b, const float* c, float s, size_t n, int block,
                          cudaStream_t st);
 cudaError_t launch_copy(float* a, const float* b, size_t n, int block, cudaStream_t st);

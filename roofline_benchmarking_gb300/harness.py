@@ -35,7 +35,7 @@ from . import roofline as rf
 from .clocks import ClockSampler, gpu_id_for_smi
 
 ATTN_VARIANTS = {"f32": [kbattn.Variant.NAIVE, kbattn.Variant.FUSED, kbattn.Variant.FLASH],
-                 "bf16": [kbattn.Variant.TC], "f16": [kbattn.Variant.TC]}
+                 "bf16": [kbattn.Variant.TC], "f16": [kbattn.Variant.TC], "q15": [kbattn.Variant.FIXEDPOINT]}
 
 FIELDS = ["kernel", "workload", "variant", "dtype", "block", "p50_ms", "min_ms", "mean_ms", "p99_ms", "tflops",
           "gbs", "bound", "attainable", "roofline_unit", "roofline_frac", "sm_mhz", "clock_reasons", "iters"]
@@ -76,6 +76,11 @@ def attention_row(w, variant, peaks, dev_info, seconds, sampler) -> dict:
     if variant == kbattn.Variant.TC:
         compute, bound = peaks["bf16_tflops"], "tensor"
         traffic = io
+    elif variant == kbattn.Variant.FIXEDPOINT:
+        # integer path: multiply-adds counted like FMAs (2 operations each)
+        compute = rf.int32_mad_peak_gops(dev_info["sm_count"], dev_info["sm_clock_khz"] / 1e3) / 1e3
+        bound = "alu"
+        traffic = io
     else:
         # fp32 CUDA-core peak: SMs x 128 lanes x 2 FLOP x the device's maximum clock
         compute = rf.fp32_peak_gflops(dev_info["sm_count"], dev_info["sm_clock_khz"] / 1e3) / 1e3
@@ -89,6 +94,34 @@ def attention_row(w, variant, peaks, dev_info, seconds, sampler) -> dict:
             **st, "tflops": tflops, "gbs": traffic / sec / 1e9, "bound": bound, "attainable": attainable,
             "roofline_unit": "TFLOP/s", "roofline_frac": tflops / attainable, "sm_mhz": clocks["sm_mhz"],
             "clock_reasons": "+".join(clocks["reasons"]) or "none"}
+
+
+GRAPH_LAUNCHES = 200
+
+
+def graph_row(w, variant, base: dict, sampler) -> dict:
+    """The same problem as ``base`` timed as one CUDA graph of 200 captured
+    launches (kbench page, "Implementation details": the launch cost of tiny
+    problems); the per-launch statistics are graph times / 200."""
+    q, k, v = (t.cuda() for t in inputs.make_qkv(w))
+    o = torch.empty_like(q)
+    t0 = time.time()
+    ms = kbattn.kb_attn_bench_graph(q, k, v, o, w.causal, w.scale, variant, launches=GRAPH_LAUNCHES,
+                                    warmup=5, iters=50)
+    t1 = time.time()
+    if kbattn.kb_check_device_error() != kbattn.Status.OK:
+        raise RuntimeError(f"device error in {w.name} {variant.name} graph")
+    st = _stats([x / GRAPH_LAUNCHES for x in ms])
+    st["iters"] = len(ms) * GRAPH_LAUNCHES
+    sec = st["p50_ms"] * 1e-3
+    tflops = w.flops / sec / 1e12
+    clocks = sampler.summary(t0, t1)
+    row = dict(base)
+    row.update({**st, "variant": f"{variant.name}+graph{GRAPH_LAUNCHES}", "tflops": tflops,
+                "gbs": base["gbs"] * base["p50_ms"] / st["p50_ms"],
+                "roofline_frac": tflops / base["attainable"], "sm_mhz": clocks["sm_mhz"],
+                "clock_reasons": "+".join(clocks["reasons"]) or "none"})
+    return row
 
 
 def hbm_rows(peaks, dev_info, quick, sampler, only) -> list[dict]:
@@ -182,6 +215,9 @@ def main(argv=None) -> int:
                     continue
                 rows.append(attention_row(w, variant, peaks, info, args.seconds, sampler))
                 print(json.dumps(rows[-1]), flush=True)
+                if w.flops < 1e8:  # launch-bound sizes: also timed as a CUDA graph
+                    rows.append(graph_row(w, variant, rows[-1], sampler))
+                    print(json.dumps(rows[-1]), flush=True)
         if not args.no_hbm:
             for r in hbm_rows(peaks, info, args.quick, sampler, only):
                 rows.append(r)

@@ -32,6 +32,7 @@ class DType(enum.IntEnum):
     F32 = 0
     BF16 = 1
     F16 = 2
+    Q15 = 3
 
 
 class Variant(enum.IntEnum):
@@ -40,6 +41,7 @@ class Variant(enum.IntEnum):
     FUSED = 2
     FLASH = 3
     TC = 4
+    FIXEDPOINT = 5
 
 
 class DeviceInfo(ctypes.Structure):
@@ -83,6 +85,7 @@ SIGNATURES = {
     "kb_attn_fwd_lse": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P]),
     "kb_attn_fwd_ws": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P, _P, _SZ]),
     "kb_attn_bench": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P, _P, _SZ, _I, _I, _FP]),
+    "kb_attn_bench_graph": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P, _P, _SZ, _I, _I, _I, _FP]),
     "kb_triad": (_I, [_P, _P, _P, _F, _SZ, _I, _P]),
     "kb_triad_bench": (_I, [_P, _P, _P, _F, _SZ, _I, _P, _I, _I, _FP]),
     "kb_device_info": (_I, [_I, ctypes.POINTER(DeviceInfo)]),
@@ -91,6 +94,7 @@ SIGNATURES = {
     "kb_status_string": (ctypes.c_char_p, [_I]),
     "kb_last_cuda_error": (_I, []),
     "kb_version": (_I, []),
+    "kb_q15_exp_table": (_I, [ctypes.POINTER(ctypes.c_uint16)]),
     "kb_attn_fwd_naive_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]),
     "kb_hbm_copy": (_I, [_P, _P, _SZ, _I, _P]),
     "kb_hbm_write": (_I, [_P, _F, _SZ, _I, _P]),
@@ -167,7 +171,8 @@ def _dtype_code(t) -> int:
     global _DTYPES
     if _DTYPES is None:
         import torch
-        _DTYPES = {torch.float32: DType.F32, torch.bfloat16: DType.BF16, torch.float16: DType.F16}
+        _DTYPES = {torch.float32: DType.F32, torch.bfloat16: DType.BF16, torch.float16: DType.F16,
+                   torch.int16: DType.Q15}
     try:
         return int(_DTYPES[t.dtype])
     except KeyError:
@@ -263,6 +268,31 @@ def kb_attn_bench(q, k, v, o, causal: bool, scale: float | None = None, variant:
                               int(bool(causal)), float(scale), dt, int(variant), _stream_ptr(stream),
                               ws_ptr, ws_bytes, warmup, iters, ms)
     _check(st, "kb_attn_bench")
+    return list(ms)
+
+
+def kb_q15_exp_table() -> list[int]:
+    """The 64-entry table of the fixed-point path, round(2^15 * 2^(-f/64))."""
+    out = (ctypes.c_uint16 * 64)()
+    _check(load().kb_q15_exp_table(out), "kb_q15_exp_table")
+    return list(out)
+
+
+def kb_attn_bench_graph(q, k, v, o, causal: bool, scale: float | None = None, variant: int = Variant.AUTO,
+                        launches: int = 200, warmup: int = 3, iters: int = 10, workspace=None,
+                        stream=None) -> list[float]:
+    """Device times in ms of ``iters`` replays of one CUDA graph holding
+    ``launches`` captured calls (per call: divide by ``launches``)."""
+    B, H, S, d, dt = _attn_args(q, k, v, o)
+    if scale is None:
+        scale = d ** -0.5
+    ms = (ctypes.c_float * iters)()
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = load().kb_attn_bench_graph(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, H, S, d,
+                                    int(bool(causal)), float(scale), dt, int(variant), _stream_ptr(stream),
+                                    ws_ptr, ws_bytes, launches, warmup, iters, ms)
+    _check(st, "kb_attn_bench_graph")
     return list(ms)
 
 

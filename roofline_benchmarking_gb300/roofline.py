@@ -35,6 +35,17 @@ def fp32_peak_gflops(sms: int, clock_mhz: float, cores_per_sm: int = CUDA_CORES_
     return sms * cores_per_sm * 2.0 * clock_mhz * 1e6 / 1e9
 
 
+# 32-bit integer multiply-add lanes per SM: half the FP32 lanes, the ratio of
+# the integer multiply-add rate to the FP32 FMA rate in NVIDIA's published
+# per-SM throughput tables for recent architectures (an assumption for sm_103).
+INT32_MAD_PER_SM = 64
+
+
+def int32_mad_peak_gops(sms: int, clock_mhz: float, lanes_per_sm: int = INT32_MAD_PER_SM) -> float:
+    """SMs x integer multiply-add lanes per SM x 2 operations (one multiply-add) x clock."""
+    return sms * lanes_per_sm * 2.0 * clock_mhz * 1e6 / 1e9
+
+
 def clock_from_throughput(gflops: float, sms: int, cores_per_sm: int = CUDA_CORES_PER_SM) -> float:
     """The same formula solved for the clock (MHz) a measured FP32 rate implies."""
     return gflops * 1e9 / (sms * cores_per_sm * 2.0) / 1e6

@@ -6,23 +6,43 @@ CANARY = 4096  # elements of poison before and after every output
 
 
 class Guarded:
-    """An output tensor carved from the middle of a NaN-filled buffer; the
-    regions before and after it must still hold the poison afterwards."""
+    """An output tensor carved from the middle of a poisoned buffer (NaN for
+    floating point, ``poison`` for integers); the regions before and after it
+    must still hold the poison afterwards. For integer outputs, where every
+    value is legal, completeness is checked by writing twice into buffers with
+    different poisons (see ``run_twice``)."""
 
-    def __init__(self, shape, dtype, device="cuda"):
+    def __init__(self, shape, dtype, device="cuda", poison=0x5A5A):
         n = int(np.prod(shape))
-        self.buf = torch.full((CANARY + n + CANARY,), float("nan"), dtype=dtype, device=device)
+        self.is_float = dtype.is_floating_point
+        fill = float("nan") if self.is_float else poison
+        self.poison = fill
+        self.buf = torch.full((CANARY + n + CANARY,), fill, dtype=dtype, device=device)
         self.n = n
         self.out = self.buf[CANARY:CANARY + n].view(*shape)
-        self._poison = self.buf[:CANARY].clone()
 
     def check(self):
         torch.cuda.synchronize()
         head = self.buf[:CANARY]
         tail = self.buf[CANARY + self.n:]
-        assert torch.isnan(head).all() and torch.isnan(tail).all(), "write outside the output tensor"
-        assert not torch.isnan(self.out).any(), "part of the output was not written"
+        if self.is_float:
+            assert torch.isnan(head).all() and torch.isnan(tail).all(), "write outside the output tensor"
+            assert not torch.isnan(self.out).any(), "part of the output was not written"
+        else:
+            assert (head == self.poison).all() and (tail == self.poison).all(), "write outside the output tensor"
         return self.out
+
+
+def run_twice(shape, dtype, launch):
+    """Integer outputs: ``launch(out)`` into two guarded buffers poisoned with
+    different values; equal results mean every element was written."""
+    a = Guarded(shape, dtype, poison=0x5A5A)
+    launch(a.out)
+    b = Guarded(shape, dtype, poison=-0x3C3D)
+    launch(b.out)
+    ra, rb = a.check(), b.check()
+    assert torch.equal(ra, rb), "part of the output was not written (or the result is not deterministic)"
+    return ra
 
 
 def errors(got, want):

@@ -135,6 +135,44 @@ def test_triad_and_bench_argument_checks(lib):
                            ms) == Status.INVALID_ARG
 
 
+def test_graph_bench_argument_checks(lib):
+    L = lib
+    ms = (ctypes.c_float * 4)()
+    base = (FAKE, FAKE, FAKE, FAKE, 1, 1, 64, 32, 0, 0.125, DType.F32, Variant.FLASH, None, None, 0)
+    for launches, warmup, iters in ((0, 1, 1), (100001, 1, 1), (10, -1, 1), (10, 1, 0)):
+        assert L.kb_attn_bench_graph(*base, launches, warmup, iters, ms) == Status.INVALID_ARG
+    assert L.kb_attn_bench_graph(*base, 10, 1, 1, None) == Status.INVALID_ARG
+    bad = base[:6] + (0,) + base[7:]  # S = 0
+    assert L.kb_attn_bench_graph(*bad, 10, 1, 1, ms) == Status.INVALID_ARG
+
+
+def test_fixed_point_support_matrix(lib):
+    L = lib
+    args = (FAKE, FAKE, FAKE, FAKE, 1, 1, 64, 64, 0)
+    assert L.kb_attn_fwd(*args, 0.125, DType.Q15, Variant.TC, None) == Status.UNSUPPORTED
+    assert L.kb_attn_fwd(*args, 0.125, DType.Q15, Variant.FLASH, None) == Status.UNSUPPORTED
+    assert L.kb_attn_fwd(*args, 0.125, DType.F32, Variant.FIXEDPOINT, None) == Status.UNSUPPORTED
+    assert L.kb_attn_fwd(*args, 0.125, DType.BF16, Variant.FIXEDPOINT, None) == Status.UNSUPPORTED
+    assert L.kb_attn_fwd(*args, 1e5, DType.Q15, Variant.FIXEDPOINT, None) == Status.INVALID_ARG  # C > 2^30
+    big = (FAKE, FAKE, FAKE, FAKE, 1, 1, 65537, 64, 0, 0.125)
+    assert L.kb_attn_fwd(*big, DType.Q15, Variant.AUTO, None) == Status.INVALID_ARG
+    assert L.kb_attn_fwd(FAKE, FAKE, FAKE, FAKE, 1, 1, 64, 48, 0, 0.125, DType.Q15, Variant.AUTO,
+                         None) == Status.UNSUPPORTED
+    ms = (ctypes.c_float * 1)()
+    assert L.kb_attn_fwd_lse(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 64, 64, 0, 0.125, DType.Q15, Variant.AUTO,
+                             None) == Status.UNSUPPORTED
+    import torch
+    if not torch.cuda.is_available():  # never launch on the fake pointers where a GPU exists
+        assert L.kb_attn_fwd(*args, 0.125, DType.Q15, Variant.AUTO, None) == Status.NO_DEVICE
+
+
+def test_fixed_point_table_is_exact(lib):
+    import mpmath
+    mpmath.mp.dps = 50
+    want = [int(mpmath.nint(32768 * mpmath.power(2, mpmath.mpf(-f) / 64))) for f in range(64)]
+    assert kbattn.kb_q15_exp_table() == want
+
+
 def test_lse_argument_checks(lib):
     L = kbattn.load()
     args = (FAKE, FAKE, FAKE, FAKE)

@@ -89,3 +89,22 @@ def test_fused_rejects_rows_longer_than_shared_memory():
     st = kbattn.kb_attn_fwd_ptr(1 << 20, 1 << 20, 1 << 20, 1 << 20, 1, 1, S, 64, False, 0.125,
                                 kbattn.DType.F32, Variant.FUSED, 0)
     assert st == kbattn.Status.UNSUPPORTED
+
+
+@pytest.mark.parametrize("variant", VARIANTS + [Variant.TC], ids=lambda v: v.name)
+def test_graph_replay_matches_oracle(oracle, variant):
+    """The CUDA-graph timing path (200 captured launches of the smallest
+    workload) leaves the same output as one plain call."""
+    w = inputs.SINGLE_HEAD_F32
+    if variant == Variant.TC:
+        w = inputs.Workload("t", 1, 1, 64, 64, False, "bf16", 0, "uniform")
+    q, k, v = (t.cuda() for t in inputs.make_qkv(w))
+    g = Guarded(q.shape, q.dtype)
+    ms = kbattn.kb_attn_bench_graph(q, k, v, g.out, causal=w.causal, scale=w.scale, variant=variant,
+                                    launches=200, warmup=2, iters=3)
+    assert kbattn.kb_check_device_error() == kbattn.Status.OK
+    assert len(ms) == 3 and all(x > 0 for x in ms)
+    got = g.check().float().cpu().numpy()
+    want = oracle.attn(*inputs.make_qkv(w), w.causal, w.scale)
+    mx, _, _ = errors(got, want)
+    assert mx <= (F32_TOL if variant != Variant.TC else 2e-2), mx

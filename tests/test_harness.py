@@ -35,5 +35,6 @@ def test_harness_runs_a_quick_sweep(tmp_path):
     assert harness.main(["--only", "f32_b1h1s64d32", "--no-hbm", "--seconds", "0.02",
                          "--out", str(tmp_path)]) == 0
     rows = [json.loads(x) for x in (tmp_path / "results.jsonl").read_text().splitlines()[1:]]
-    assert {r["variant"] for r in rows} == {"NAIVE", "FUSED", "FLASH"}
+    assert {r["variant"] for r in rows} == {"NAIVE", "FUSED", "FLASH", "NAIVE+graph200", "FUSED+graph200",
+                                            "FLASH+graph200"}
     assert all(r["p50_ms"] > 0 and 0 < r["roofline_frac"] < 2 for r in rows)
