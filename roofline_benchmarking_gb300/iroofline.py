@@ -210,11 +210,13 @@ def roofline_points(mean: dict, seconds: float, ceil: dict) -> dict:
             att = min(peak, ii * bw)
         levels[lvl] = {"transactions": txn, "intensity": ii, "ceiling_gtxn_s": bw, "attainable_gips": att,
                        "achieved_gtxn_s": txn / seconds / 1e9}
-    bound = None
+    bound, att = None, None
     bounded = {k: v for k, v in levels.items() if v["attainable_gips"] is not None and k != "TMA L2->smem"}
     if bounded:
         bound = min(bounded, key=lambda k: bounded[k]["attainable_gips"])
-    att = bounded[bound]["attainable_gips"] if bound else None
+        att = bounded[bound]["attainable_gips"]
+        if peak is not None and att >= peak:
+            bound = "instruction issue"  # every level's memory ceiling lies above the peak
     return {"warp_instructions": inst / 32.0, "warp_gips": gips, "peak_warp_gips": peak, "levels": levels,
             "bound": bound, "attainable_gips": att, "frac": (gips / att) if att else None}
 

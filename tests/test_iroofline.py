@@ -75,3 +75,11 @@ def test_metric_list_covers_every_level():
     for ms in ir.LEVELS.values():
         assert set(ms) <= set(names)
     assert ir.INSTRUCTIONS in names and ir.DURATION in names and len(names) == len(set(names))
+
+
+def test_compute_bound_kernel_reports_instruction_issue():
+    mean = {ir.INSTRUCTIONS: 32e9, "dram__sectors_read.sum": 1e6, "smsp__inst_executed.sum.peak_sustained": 608,
+            "sm__cycles_elapsed.avg.per_second": 2e9}
+    pts = ir.roofline_points(mean, 1.0, ir.ceilings(mean, hbm_gbs=6400.0))
+    assert pts["bound"] == "instruction issue" and pts["attainable_gips"] == pytest.approx(1216)
+    assert pts["warp_gips"] == pytest.approx(1.0) and pts["frac"] == pytest.approx(1.0 / 1216)
