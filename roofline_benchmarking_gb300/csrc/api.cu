@@ -39,12 +39,13 @@ int validate(const void* q, const void* k, const void* v, const void* o, int B, 
   if (N > std::numeric_limits<int32_t>::max()) return KB_ERR_INVALID_ARG;
   const int64_t lim = std::numeric_limits<int64_t>::max() / 4;
   if (N > lim / S || N * S > lim / d) return KB_ERR_INVALID_ARG;
-  if (d != 32 && d != 64 && d != 128) return KB_ERR_UNSUPPORTED;
+  if (d != 32 && d != 64 && d != 128 && d != 256) return KB_ERR_UNSUPPORTED;
   int var = variant;
   if (var == KB_AUTO) var = dtype == KB_F32 ? KB_FLASH : (dtype == KB_Q15 ? KB_FIXEDPOINT : KB_TC);
   if ((dtype == KB_Q15) != (var == KB_FIXEDPOINT)) return KB_ERR_UNSUPPORTED;
   if (dtype == KB_F32 && var == KB_TC) return KB_ERR_UNSUPPORTED;
   if ((dtype == KB_BF16 || dtype == KB_F16) && var != KB_TC) return KB_ERR_UNSUPPORTED;
+  if (d == 256 && var != KB_TC) return KB_ERR_UNSUPPORTED;  // d = 256: tensor-core path only
   if (var == KB_FIXEDPOINT) {
     // keeps every fixed-point intermediate inside 64 bits
     if (S > 65536 || !q15_scale_ok(scale)) return KB_ERR_INVALID_ARG;

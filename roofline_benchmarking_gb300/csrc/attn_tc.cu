@@ -494,6 +494,375 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// d = 256. Two 128 x 256 fp32 O accumulators would take all 512 TMEM columns,
+// so here a work item is ONE 128-row query tile, and TMEM holds two 128 x 64
+// score buffers (the scores of key tile j+1 are computed while the softmax
+// works on tile j) and the 128 x 256 O. Key tiles are 64 keys; K and V rings
+// of two 32 KB stages each plus the 64 KB Q tile use 192 KB of shared memory.
+// Warps 0-3 run the softmax (thread = row = TMEM lane), warp 4 drives TMA,
+// warp 5 issues the MMAs. MMA order per item: S(0), S(1), then for each j:
+// PV(j), S(j+2). S(j+2) reuses the buffer of P(j) only after PV(j) read it
+// (in-order execution); since PV(j) is no longer ordered before S(j+1), a
+// softmax that must rescale O first waits for the PVDONE commit of PV(j-1).
+// ---------------------------------------------------------------------------
+constexpr int kThreads256 = 192;
+constexpr int kWarpTMA256 = 4;
+constexpr int kWarpMMA256 = 5;
+constexpr int kBN256 = 64;
+
+struct Tc256 {
+  static constexpr int D = 256;
+  static constexpr int QTILE = kBM * D * 2;      // 64 KB
+  static constexpr int KTILE = kBN256 * D * 2;   // 32 KB (K or V)
+  static constexpr int KS = 2, VS = 2;
+  static constexpr uint32_t QBLK = kBM * 128;     // a 64-feature column block of Q: 128 rows x 128 bytes
+  static constexpr uint32_t KBLK = kBN256 * 128;  // a 64-feature column block of K or V: 64 rows x 128 bytes
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + QTILE;
+  static constexpr int OFF_V = OFF_K + KS * KTILE;
+  static constexpr int OFF_BAR = OFF_V + VS * KTILE;
+  enum {
+    B_Q = 0,
+    B_KFULL = 1,
+    B_KEMPTY = B_KFULL + KS,
+    B_VFULL = B_KEMPTY + KS,
+    B_VEMPTY = B_VFULL + VS,
+    B_SFULL = B_VEMPTY + VS,  // [2]: score buffer b computed
+    B_PFULL = B_SFULL + 2,    // [2]: P written into buffer b (and O rescaled)
+    B_PVDONE = B_PFULL + 2,   // every P V completed, in order
+    B_OFINAL = B_PVDONE + 1,  // last P V of an item completed
+    B_OFREE = B_OFINAL + 1,   // O read out by the epilogue
+    B_QFREE = B_OFREE + 1,    // last score MMA of an item completed
+    B_DRAIN = B_QFREE + 1,
+    NBAR = B_DRAIN + 1
+  };
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int BYTES = OFF_MISC + 16;
+  static constexpr int SMEM = BYTES + 1024;
+  static constexpr uint32_t TM_O = 256;  // O in columns 256-511; score buffer b in 64 b .. 64 b + 63
+};
+
+// One query tile per item; heaviest (causal) first, dealt in a snake order.
+struct Item256 {
+  int n, q0, nk;  // head, first row, key tiles
+};
+
+struct Schedule256 {
+  int N, S, causal, tiles, nkv, total;
+  __device__ Schedule256(int N_, int S_, int causal_) : N(N_), S(S_), causal(causal_) {
+    tiles = (S + kBM - 1) / kBM;
+    nkv = (S + kBN256 - 1) / kBN256;
+    total = N * tiles;
+  }
+  __device__ bool get(int round, Item256& it) const {
+    const int G = (int)gridDim.x, c = (int)blockIdx.x;
+    const int i = round * G + ((round & 1) ? G - 1 - c : c);
+    if (i >= total) return false;
+    const int t = tiles - 1 - i / N;
+    it.n = i % N;
+    it.q0 = t * kBM;
+    it.nk = causal ? min(2 * t + 2, nkv) : nkv;
+    return true;
+  }
+};
+
+template <bool F16>
+__global__ void __launch_bounds__(kThreads256, 1)
+    attn_tc256_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                      const __grid_constant__ CUtensorMap tmv, uint8_t* __restrict__ out, float* __restrict__ lse,
+                      int N, int S, int causal, float scale_log2, unsigned long long limit) {
+  using C = Tc256;
+  constexpr uint32_t kAB = F16 ? 0u : 1u;
+  constexpr uint32_t IDESC_QK = ptx::f16_idesc(kBM, kBN256, kAB, 0);
+  constexpr uint32_t IDESC_PV = ptx::f16_idesc(kBM, C::D, kAB, 1);
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* sm = smem_raw + (base - raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::OFF_MISC + 4);
+  auto bar = [&](int i) -> uint32_t { return base + C::OFF_BAR + 8u * (uint32_t)i; };
+
+  const Schedule256 sched(N, S, causal);
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    ptx::mbar_init(bar(C::B_Q), 1);
+    for (int s = 0; s < C::KS; ++s) {
+      ptx::mbar_init(bar(C::B_KFULL + s), 1);
+      ptx::mbar_init(bar(C::B_KEMPTY + s), 1);
+    }
+    for (int s = 0; s < C::VS; ++s) {
+      ptx::mbar_init(bar(C::B_VFULL + s), 1);
+      ptx::mbar_init(bar(C::B_VEMPTY + s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(bar(C::B_SFULL + b), 1);
+      ptx::mbar_init(bar(C::B_PFULL + b), 4 * 32);
+    }
+    ptx::mbar_init(bar(C::B_PVDONE), 1);
+    ptx::mbar_init(bar(C::B_OFINAL), 1);
+    ptx::mbar_init(bar(C::B_OFREE), 4 * 32);
+    ptx::mbar_init(bar(C::B_QFREE), 1);
+    ptx::mbar_init(bar(C::B_DRAIN), 1);
+    ptx::fence_mbar_init();
+  }
+  if (warp == kWarpMMA256) {
+    ptx::tmem_alloc(base + C::OFF_MISC, kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + C::OFF_MISC);
+
+  if (warp == kWarpTMA256) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      ptx::tma_prefetch_desc(&tmq);
+      ptx::tma_prefetch_desc(&tmk);
+      ptx::tma_prefetch_desc(&tmv);
+      int kdone = 0, vdone = 0, items = 0;
+      bool ok = true;
+      Item256 it;
+      for (int round = 0; ok && sched.get(round, it); ++round) {
+        if (items > 0) ok = wait_bar(bar(C::B_QFREE), (items - 1) & 1, abort_flag, limit, true);
+        if (!ok) break;
+        ptx::mbar_arrive_expect_tx(bar(C::B_Q), C::QTILE);
+        for (int b = 0; b < 4; ++b)
+          ptx::tma_load_3d(base + C::OFF_Q + b * C::QBLK, &tmq, bar(C::B_Q), b * 64, it.q0, it.n);
+        for (int j = 0; j < it.nk && ok; ++j) {
+          const int ks = kdone % C::KS, vs = vdone % C::VS;
+          if (kdone >= C::KS) ok = wait_bar(bar(C::B_KEMPTY + ks), ((kdone / C::KS) & 1) ^ 1, abort_flag, limit, true);
+          if (!ok) break;
+          ptx::mbar_arrive_expect_tx(bar(C::B_KFULL + ks), C::KTILE);
+          for (int b = 0; b < 4; ++b)
+            ptx::tma_load_3d(base + C::OFF_K + ks * C::KTILE + b * C::KBLK, &tmk, bar(C::B_KFULL + ks), b * 64,
+                             j * kBN256, it.n);
+          ++kdone;
+          if (vdone >= C::VS) ok = wait_bar(bar(C::B_VEMPTY + vs), ((vdone / C::VS) & 1) ^ 1, abort_flag, limit, true);
+          if (!ok) break;
+          ptx::mbar_arrive_expect_tx(bar(C::B_VFULL + vs), C::KTILE);
+          for (int b = 0; b < 4; ++b)
+            ptx::tma_load_3d(base + C::OFF_V + vs * C::KTILE + b * C::KBLK, &tmv, bar(C::B_VFULL + vs), b * 64,
+                             j * kBN256, it.n);
+          ++vdone;
+        }
+        ++items;
+      }
+      if (items > 0) wait_bar(bar(C::B_Q), (items - 1) & 1, abort_flag, limit, false);
+      for (int x = kdone - C::KS < 0 ? 0 : kdone - C::KS; x < kdone; ++x)
+        wait_bar(bar(C::B_KFULL + x % C::KS), (x / C::KS) & 1, abort_flag, limit, false);
+      for (int x = vdone - C::VS < 0 ? 0 : vdone - C::VS; x < vdone; ++x)
+        wait_bar(bar(C::B_VFULL + x % C::VS), (x / C::VS) & 1, abort_flag, limit, false);
+    }
+    __syncwarp();
+  } else if (warp == kWarpMMA256) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      // S(buffer b) = Q K^T: 16 k-steps of 16 features; both operands K-major
+      auto issue_s = [&](int b, int ks) {
+        const uint64_t a0 = ptx::sw128_desc(base + C::OFF_Q, 16, 1024);
+        const uint64_t b0 = ptx::sw128_desc(base + C::OFF_K + ks * C::KTILE, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < C::D / 16; ++kk) {
+          const uint32_t offa = ((kk >> 2) * C::QBLK + (kk & 3) * 32) >> 4;
+          const uint32_t offb = ((kk >> 2) * C::KBLK + (kk & 3) * 32) >> 4;
+          ptx::mma_f16_ss(tmem + 64u * (uint32_t)b, a0 + offa, b0 + offb, IDESC_QK, kk > 0 ? 1u : 0u);
+        }
+        ptx::mma_commit(bar(C::B_SFULL + b));
+      };
+      // O += P(buffer b) V: 4 k-steps of 16 keys; V MN-major, column blocks KBLK apart
+      auto issue_pv = [&](int b, int vs, bool first) {
+        const uint64_t b0 = ptx::sw128_desc(base + C::OFF_V + vs * C::KTILE, C::KBLK, 1024);
+#pragma unroll
+        for (int kk = 0; kk < kBN256 / 16; ++kk)
+          ptx::mma_f16_ts(tmem + C::TM_O, tmem + 64u * (uint32_t)b + kk * 8, b0 + ((kk * 16 * 128) >> 4), IDESC_PV,
+                          (!first || kk > 0) ? 1u : 0u);
+      };
+      bool ok = true;
+      int kcons = 0, vcons = 0, scnt = 0, pcnt = 0;
+      Item256 it;
+      for (int item = 0; ok && sched.get(item, it); ++item) {
+        const int nk = it.nk;
+        ok = wait_bar(bar(C::B_Q), item & 1, abort_flag, limit, true);
+        // S(0) and S(1)
+        for (int j = 0; j < 2 && j < nk && ok; ++j) {
+          const int ks = kcons % C::KS;
+          ok = wait_bar(bar(C::B_KFULL + ks), (kcons / C::KS) & 1, abort_flag, limit, true);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          issue_s(scnt & 1, ks);
+          ptx::mma_commit(bar(C::B_KEMPTY + ks));
+          if (j == nk - 1) ptx::mma_commit(bar(C::B_QFREE));
+          ++kcons;
+          ++scnt;
+        }
+        for (int j = 0; j < nk && ok; ++j) {
+          const int vs = vcons % C::VS;
+          ok = wait_bar(bar(C::B_VFULL + vs), (vcons / C::VS) & 1, abort_flag, limit, true);
+          if (ok) ok = wait_bar(bar(C::B_PFULL + (pcnt & 1)), (pcnt >> 1) & 1, abort_flag, limit, true);
+          if (ok && j == 0 && item > 0) ok = wait_bar(bar(C::B_OFREE), (item - 1) & 1, abort_flag, limit, true);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          issue_pv(pcnt & 1, vs, j == 0);
+          ptx::mma_commit(bar(C::B_PVDONE));
+          ptx::mma_commit(bar(C::B_VEMPTY + vs));
+          ++vcons;
+          ++pcnt;
+          if (j + 2 < nk) {
+            const int ks = kcons % C::KS;
+            ok = wait_bar(bar(C::B_KFULL + ks), (kcons / C::KS) & 1, abort_flag, limit, true);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            issue_s(scnt & 1, ks);
+            ptx::mma_commit(bar(C::B_KEMPTY + ks));
+            if (j + 2 == nk - 1) ptx::mma_commit(bar(C::B_QFREE));
+            ++kcons;
+            ++scnt;
+          }
+        }
+        if (ok) ptx::mma_commit(bar(C::B_OFINAL));
+      }
+      ptx::mma_commit(bar(C::B_DRAIN));
+      wait_bar(bar(C::B_DRAIN), 0, abort_flag, limit, false);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax, warps 0-3
+    const int r = warp * 32 + lane;
+    const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
+    const uint32_t to = tl + C::TM_O;
+    int scnt = 0;  // score tiles consumed (global)
+    bool ok = true;
+    Item256 it;
+    for (int item = 0; ok && sched.get(item, it); ++item) {
+      const int row = it.q0 + r;
+      float m_run = -INFINITY, l_run = 0.f;
+      for (int j = 0; j < it.nk; ++j) {
+        const int b = scnt & 1;
+        if (!(ok = warp_wait(bar(C::B_SFULL + b), (scnt >> 1) & 1, abort_flag, limit))) break;
+        ptx::tc_fence_after();
+        const uint32_t ts = tl + 64u * (uint32_t)b;
+        float s[kBN256];
+        {
+          uint32_t u0[32], u1[32];
+          ptx::tmem_ld32(ts + 0, u0);
+          ptx::tmem_ld32(ts + 32, u1);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            s[e] = __uint_as_float(u0[e]);
+            s[32 + e] = __uint_as_float(u1[e]);
+          }
+        }
+        const int k0 = j * kBN256;
+        if ((causal && k0 + kBN256 - 1 > it.q0) || k0 + kBN256 > S) {
+          const int lim = min(causal ? row - k0 : kBN256 - 1, S - 1 - k0);  // last visible column
+#pragma unroll
+          for (int c = 0; c < kBN256; ++c)
+            if (c > lim) s[c] = -INFINITY;
+        }
+        float mx[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mx[e] = fmaxf(s[e], s[8 + e]);
+#pragma unroll
+        for (int c = 16; c < kBN256; c += 16)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) mx[e] = ptx::max3(mx[e], s[c + e], s[c + 8 + e]);
+        const float m_tile =
+            fmaxf(ptx::max3(mx[0], mx[1], mx[2]), ptx::max3(mx[3], mx[4], ptx::max3(mx[5], mx[6], mx[7]))) *
+            scale_log2;
+        float alpha = 1.f;
+        bool corr = false;
+        if (j == 0) {
+          m_run = m_tile == -INFINITY ? 0.f : m_tile;
+        } else if (m_tile > m_run + 8.0f) {
+          alpha = ptx::ex2(m_run - m_tile);
+          m_run = m_tile;
+          l_run *= alpha;
+          corr = true;
+        }
+        const float2 sl2 = make_float2(scale_log2, scale_log2);
+        const float2 nm2 = make_float2(-m_run, -m_run);
+        float2 sum2[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sum2[e] = make_float2(0.f, 0.f);
+        {
+          uint32_t pk[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const float2 x = ptx::fma2(make_float2(s[2 * c], s[2 * c + 1]), sl2, nm2);
+            const float2 pv = make_float2(ptx::ex2(x.x), ptx::ex2(x.y));
+            sum2[c & 3] = ptx::add2(sum2[c & 3], pv);
+            pk[c] = pack2<F16>(pv.x, pv.y);
+          }
+          ptx::tmem_st32(ts, pk);
+        }
+        const float2 t2 = ptx::add2(ptx::add2(sum2[0], sum2[1]), ptx::add2(sum2[2], sum2[3]));
+        l_run += t2.x + t2.y;
+        if (__any_sync(0xffffffffu, corr)) {
+          // O must hold exactly the tiles before j: wait for P V of tile j-1
+          // (global index scnt - 1). Its phase is unambiguous: S of this tile
+          // was issued after P V of tile j-2, so that one has completed.
+          if (!(ok = warp_wait(bar(C::B_PVDONE), (scnt - 1) & 1, abort_flag, limit))) break;
+          ptx::tc_fence_after();
+          uint32_t u[32];
+#pragma unroll 1
+          for (int cb = 0; cb < C::D / 32; ++cb) {
+            ptx::tmem_ld32(to + cb * 32, u);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * alpha);
+            ptx::tmem_st32(to + cb * 32, u);
+          }
+        }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(C::B_PFULL + b));
+        ++scnt;
+      }
+      if (ok) ok = warp_wait(bar(C::B_OFINAL), item & 1, abort_flag, limit);
+      if (ok) {
+        ptx::tc_fence_after();
+        const float inv = 1.0f / l_run;
+        if (lse != nullptr && row < S) lse[(size_t)it.n * S + row] = (m_run + log2f(l_run)) * 0.6931471805599453f;
+        uint8_t* orow = out + ((size_t)it.n * S + row) * (size_t)C::D * 2;
+        uint32_t u[32];
+#pragma unroll 1
+        for (int cb = 0; cb < C::D / 32; ++cb) {
+          ptx::tmem_ld32(to + cb * 32, u);
+          ptx::tmem_wait_ld();
+          if (cb == C::D / 32 - 1) {
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(C::B_OFREE));
+          }
+          if (row < S) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint4 w;
+              w.x = pack2<F16>(__uint_as_float(u[q * 8 + 0]) * inv, __uint_as_float(u[q * 8 + 1]) * inv);
+              w.y = pack2<F16>(__uint_as_float(u[q * 8 + 2]) * inv, __uint_as_float(u[q * 8 + 3]) * inv);
+              w.z = pack2<F16>(__uint_as_float(u[q * 8 + 4]) * inv, __uint_as_float(u[q * 8 + 5]) * inv);
+              w.w = pack2<F16>(__uint_as_float(u[q * 8 + 6]) * inv, __uint_as_float(u[q * 8 + 7]) * inv);
+              *reinterpret_cast<uint4*>(orow + cb * 64 + q * 16) = w;
+            }
+          }
+        }
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMMA256) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
 // One thread waits on an mbarrier nothing will complete; the bounded wait must
 // record a timeout and return.
 __global__ void selftest_timeout_kernel(unsigned long long limit) {
@@ -528,13 +897,13 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// [N, S, d] row-major 16-bit tensor, boxes of 64 features x 128 rows x 1 head.
-bool make_map(CUtensorMap* m, const void* ptr, int64_t N, int S, int d, bool f16) {
+// [N, S, d] row-major 16-bit tensor, boxes of 64 features x `rows` rows x 1 head.
+bool make_map(CUtensorMap* m, const void* ptr, int64_t N, int S, int d, bool f16, int rows = kBM) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)S, (cuuint64_t)N};
   const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)S * d * 2};
-  const cuuint32_t box[3] = {64, (cuuint32_t)kBM, 1};
+  const cuuint32_t box[3] = {64, (cuuint32_t)rows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                   const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -563,17 +932,37 @@ cudaError_t tc_launch(const AttnProblem& p, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+template <bool F16>
+cudaError_t tc256_launch(const AttnProblem& p, cudaStream_t st) {
+  using C = Tc256;
+  cudaError_t e = cudaFuncSetAttribute(attn_tc256_kernel<F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, p.q, p.N, p.S, C::D, F16, kBM) || !make_map(&mk, p.k, p.N, p.S, C::D, F16, kBN256) ||
+      !make_map(&mv, p.v, p.N, p.S, C::D, F16, kBN256))
+    return cudaErrorInvalidValue;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const int64_t items = (int64_t)((p.S + kBM - 1) / kBM) * p.N;
+  const int64_t grid = items < sms ? items : sms;
+  attn_tc256_kernel<F16><<<(unsigned)grid, kThreads256, C::SMEM, st>>>(
+      mq, mk, mv, static_cast<uint8_t*>(p.o), p.lse, (int)p.N, p.S, p.causal, p.scale * 1.4426950408889634f,
+      kDefaultWaitLimitNs);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 int tc_check(int S, int d, int dtype) {
   (void)S;
-  if (d != 64 && d != 128) return KB_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128 && d != 256) return KB_ERR_UNSUPPORTED;
   if (dtype != KB_BF16 && dtype != KB_F16) return KB_ERR_UNSUPPORTED;
   int dev = 0, optin = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KB_ERR_NO_DEVICE;
   if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
     return KB_ERR_CUDA;
-  const int need = d == 128 ? TcCfg<128>::SMEM : TcCfg<64>::SMEM;
+  const int need = d == 256 ? Tc256::SMEM : (d == 128 ? TcCfg<128>::SMEM : TcCfg<64>::SMEM);
   return need <= optin ? KB_OK : KB_ERR_UNSUPPORTED;
 }
 
@@ -581,6 +970,7 @@ cudaError_t launch_tc(const AttnProblem& p, cudaStream_t st) {
   const bool f16 = p.dtype == KB_F16;
   if (p.d == 128) return f16 ? tc_launch<128, true>(p, st) : tc_launch<128, false>(p, st);
   if (p.d == 64) return f16 ? tc_launch<64, true>(p, st) : tc_launch<64, false>(p, st);
+  if (p.d == 256) return f16 ? tc256_launch<true>(p, st) : tc256_launch<false>(p, st);
   return cudaErrorInvalidValue;
 }
 

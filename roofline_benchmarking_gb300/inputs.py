@@ -69,6 +69,9 @@ BF16_CAUSAL_S4096 = Workload("bf16_causal_b4h16s4096d128", 4, 16, 4096, 128, Tru
 BF16_S2048_D64 = Workload("bf16_b16h12s2048d64", 16, 12, 2048, 64, False, "bf16", 3, "normal")
 BF16_CAUSAL_S16384 = Workload("bf16_causal_b1h32s16384d128_sharp", 1, 32, 16384, 128, True, "bf16", 4,
                               "normal", sigma_qk=3.0, sigma_v=1.0)
+# Head dimension 256 (not among the pages' workloads): the tensor-core path's
+# one-query-tile-per-CTA layout, at the bench workload's sequence length.
+BF16_CAUSAL_D256 = Workload("bf16_causal_b2h16s4096d256", 2, 16, 4096, 256, True, "bf16", 6, "normal")
 
 # The Q15 fixed-point model runs on the fp32 workloads' shapes and draws.
 Q15_SINGLE_HEAD = SINGLE_HEAD_F32.with_(name="q15_b1h1s64d32", dtype="q15")
@@ -76,7 +79,7 @@ Q15_S1024 = F32_S1024.with_(name="q15_b1h8s1024d64", dtype="q15")
 Q15_S1024_CAUSAL = F32_S1024_CAUSAL.with_(name="q15_b1h8s1024d64_causal", dtype="q15")
 
 WORKLOADS = {w.name: w for w in (SINGLE_HEAD_F32, F32_S1024, F32_S1024_CAUSAL,
-                                 BF16_CAUSAL_S4096, BF16_S2048_D64, BF16_CAUSAL_S16384,
+                                 BF16_CAUSAL_S4096, BF16_S2048_D64, BF16_CAUSAL_S16384, BF16_CAUSAL_D256,
                                  Q15_SINGLE_HEAD, Q15_S1024, Q15_S1024_CAUSAL)}
 
 # STREAM Triad working set: three fp32 arrays of 2 GiB each.

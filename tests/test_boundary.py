@@ -83,7 +83,8 @@ def attn(q=FAKE, k=FAKE, v=FAKE, o=FAKE, B=1, H=1, S=64, d=64, causal=0, scale=0
     (dict(B=1 << 15, H=1 << 15, S=1 << 30, d=128), Status.INVALID_ARG),  # bytes overflow int64
     (dict(B=2, H=1, S=(1 << 31) - 1, d=32, variant=Variant.NAIVE), Status.UNSUPPORTED),  # score grid
     (dict(d=48), Status.UNSUPPORTED),
-    (dict(d=256), Status.UNSUPPORTED),
+    (dict(d=256), Status.UNSUPPORTED),                                  # fp32 at d = 256: tensor cores only
+    (dict(d=512, dtype=DType.BF16, variant=Variant.TC), Status.UNSUPPORTED),
     (dict(dtype=DType.F32, variant=Variant.TC), Status.UNSUPPORTED),
     (dict(dtype=DType.BF16, variant=Variant.FLASH), Status.UNSUPPORTED),
     (dict(dtype=DType.F16, variant=Variant.NAIVE), Status.UNSUPPORTED),

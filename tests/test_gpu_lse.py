@@ -27,6 +27,7 @@ CASES = [  # (B, H, S, d, causal, dtype, variant, tol)
     (2, 1, 513, 64, True, "f16", Variant.TC, 1e-3), (1, 3, 1024, 64, False, "bf16", Variant.TC, 1e-3),
     (1, 2, 130, 64, True, "f32", Variant.FLASH, 1e-4), (2, 2, 64, 32, False, "f32", Variant.FLASH, 1e-4),
     (1, 1, 1, 128, True, "bf16", Variant.TC, 1e-3),
+    (1, 2, 200, 256, True, "bf16", Variant.TC, 1e-3), (1, 1, 130, 256, False, "f16", Variant.TC, 1e-3),
 ]
 
 

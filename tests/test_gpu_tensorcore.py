@@ -37,6 +37,9 @@ SMALL = [  # (B, H, S, d, causal): one tile, several tiles, ragged tails, S = 1
     (1, 1, 128, 128, False), (1, 1, 128, 128, True), (1, 1, 128, 64, False), (1, 2, 256, 128, True),
     (1, 2, 256, 64, True), (2, 1, 300, 128, False), (1, 1, 1, 128, True), (1, 1, 1, 64, False),
     (1, 2, 77, 64, False), (1, 1, 513, 64, True), (1, 3, 640, 128, True), (2, 2, 383, 128, False),
+    # d = 256: one query tile per CTA, 64-key tiles, two score buffers
+    (1, 1, 1, 256, True), (1, 1, 64, 256, False), (1, 2, 65, 256, True), (1, 1, 128, 256, True),
+    (2, 1, 200, 256, False), (1, 2, 300, 256, True), (1, 1, 513, 256, True), (1, 1, 1024, 256, False),
 ]
 
 
@@ -52,9 +55,10 @@ def test_small_shapes_match_oracle(oracle, shape, dtype):
     assert mx <= MAX_TOL and mean <= MEAN_TOL, (mx, mean)
 
 
-def test_sharp_softmax_rescale_path(oracle):
+@pytest.mark.parametrize("d", [128, 256])
+def test_sharp_softmax_rescale_path(oracle, d):
     """Scores spread over tens of units force repeated O rescaling in TMEM."""
-    w = inputs.Workload("sharp", 1, 2, 1024, 128, True, "bf16", 9, "normal", sigma_qk=3.0)
+    w = inputs.Workload("sharp", 1, 2, 1024, d, True, "bf16", 9, "normal", sigma_qk=3.0)
     q, k, v = inputs.make_qkv(w)
     got = run_tc(q, k, v, True, w.scale).float().cpu().numpy()
     want = oracle.attn(q, k, v, True, w.scale)
@@ -62,9 +66,10 @@ def test_sharp_softmax_rescale_path(oracle):
     assert mx <= MAX_TOL and mean <= MEAN_TOL, (mx, mean)
 
 
-def test_increasing_scores_rescale_every_tile(oracle):
+@pytest.mark.parametrize("d", [64, 256])
+def test_increasing_scores_rescale_every_tile(oracle, d):
     """Keys whose scores grow with position make the row max rise in every tile."""
-    S, d = 1024, 64
+    S = 1024
     q = torch.zeros(1, 1, S, d)
     q[..., 0] = 1.0
     k = torch.zeros(1, 1, S, d)
@@ -86,8 +91,8 @@ def test_constant_values_give_constant_output():
     assert torch.equal(got, torch.full_like(got, 0.75))
 
 
-@pytest.mark.parametrize("w", [inputs.BF16_CAUSAL_S4096, inputs.BF16_S2048_D64, inputs.BF16_CAUSAL_S16384],
-                         ids=lambda w: w.name)
+@pytest.mark.parametrize("w", [inputs.BF16_CAUSAL_S4096, inputs.BF16_S2048_D64, inputs.BF16_CAUSAL_S16384,
+                               inputs.BF16_CAUSAL_D256], ids=lambda w: w.name)
 def test_full_size_workloads_on_sampled_rows(oracle, w):
     q, k, v = inputs.make_qkv(w)
     got = run_tc(q, k, v, w.causal, w.scale)
@@ -102,8 +107,9 @@ def test_full_size_workloads_on_sampled_rows(oracle, w):
     assert float(got.abs().max()) <= float(v.abs().max()) + 1e-2
 
 
-def test_repeat_calls_are_deterministic():
-    w = inputs.Workload("det", 2, 2, 512, 128, True, "bf16", 13, "normal")
+@pytest.mark.parametrize("d", [128, 256])
+def test_repeat_calls_are_deterministic(d):
+    w = inputs.Workload("det", 2, 2, 512, d, True, "bf16", 13, "normal")
     q, k, v = (t.cuda() for t in inputs.make_qkv(w))
     a = kbattn.kb_attn_fwd(q, k, v, causal=True, variant=Variant.TC)
     b = kbattn.kb_attn_fwd(q, k, v, causal=True, variant=Variant.TC)
