@@ -319,96 +319,163 @@ __global__ void __launch_bounds__(kThreads) naive_pv_kernel(const float* __restr
 }
 
 // ---------------------------------------------------------------------------
-// fused: one block per (head, query row); the score row lives in shared memory.
-// Key tiles of 64 rows are staged in shared memory with coalesced loads and
-// each dot product is split over 4 threads, thread q of a key taking float4
-// q, q + 4, ...; rows are padded by 16 floats so that the 8 threads of one
-// 128-bit load phase (2 keys x 4 parts) touch 8 distinct bank groups.
+// fused: the S-length score rows live in shared memory, one pass over the keys
+// (kbench, "The three GPU kernels": one block per query row, shared memory
+// O(S)). A block takes R consecutive query rows of one head (R = 4 where their
+// R score rows fit in shared memory and the grid keeps two blocks per SM, else
+// 2 or 1 -- R = 1 is the page's layout and sets the same S cap), so every K and
+// V element read from L2 serves R rows. Key tiles of 64 keys are staged in shared memory with coalesced
+// loads; each dot product is split over 4 threads, thread q of a key taking
+// float4 q, q + 4, ...; rows are padded by 16 floats so that the 8 threads of
+// one 128-bit load phase (2 keys x 4 parts) touch 8 distinct bank groups.
+// Masked keys (past a row's causal limit) hold -inf, so every row of the block
+// runs over the same key range and gets probability 0 there.
 // ---------------------------------------------------------------------------
 constexpr int kFusedThreads = 256;
 constexpr int kFusedKeys = 64;  // keys per staged tile
+constexpr int kFusedWarps = kFusedThreads / 32;
 
-template <int D>
+// Per-row maxima (MAX) or sums over the block for R values per thread; every
+// thread receives the results. Uses red[kFusedWarps * R]; contains barriers.
+template <int R, bool MAX>
+__device__ __forceinline__ void block_rows(float (&v)[R], float* red) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    float x = v[r];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float y = __shfl_xor_sync(0xffffffffu, x, o);
+      x = MAX ? fmaxf(x, y) : x + y;
+    }
+    if (lane == 0) red[warp * R + r] = x;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    float x = red[r];
+#pragma unroll
+    for (int w = 1; w < kFusedWarps; ++w) x = MAX ? fmaxf(x, red[w * R + r]) : x + red[w * R + r];
+    v[r] = x;
+  }
+  __syncthreads();  // red may be reused
+}
+
+template <int D, int R>
 __global__ void __launch_bounds__(kFusedThreads) fused_row_f32_kernel(const float* __restrict__ Q,
                                                                       const float* __restrict__ K,
                                                                       const float* __restrict__ V,
                                                                       float* __restrict__ O, int S, int causal,
                                                                       float scale_log2) {
   constexpr int LDK = D + 16;
+  constexpr int G = kFusedThreads / D;  // key groups of the P V pass
   extern __shared__ float4 smem4[];
   float* Ks = reinterpret_cast<float*>(smem4);  // [kFusedKeys][LDK]
-  float* qs = Ks + kFusedKeys * LDK;             // [D]
-  float* red = qs + D;                           // [32]
-  float* part = red + 32;                        // [kFusedThreads]
-  float* sc = part + kFusedThreads;              // [S]
-  const int64_t b = blockIdx.x;
-  const int64_t n = b / S;
-  const int i = (int)(b % S);
+  float* qs = Ks + kFusedKeys * LDK;             // [R][D]
+  float* red = qs + R * D;                       // [kFusedWarps * R]
+  float* part = red + kFusedWarps * R;           // [R][kFusedThreads]
+  float* sc = part + R * kFusedThreads;          // [R][S]
+  const int tiles = (S + R - 1) / R;
+  const int64_t n = blockIdx.x / tiles;
+  const int i0 = (int)(blockIdx.x % tiles) * R;
   const int tid = threadIdx.x;
-  const int last = causal ? i : S - 1;
+  const int last_block = causal ? min(i0 + R - 1, S - 1) : S - 1;  // keys any row of the block sees
   const float* Kh = K + n * S * D;
   const float* Vh = V + n * S * D;
 
-  for (int c = tid; c < D; c += kFusedThreads) qs[c] = Q[(n * S + i) * D + c] * scale_log2;
+  for (int f = tid; f < R * D; f += kFusedThreads) {
+    const int r = f / D, c = f % D;
+    qs[f] = i0 + r < S ? Q[(n * S + i0 + r) * D + c] * scale_log2 : 0.f;
+  }
 
-  // scores: thread tid works on key tid / 4 of the tile, float4 (tid % 4) + 4 t
+  // scores: thread tid works on key tid / 4 of the tile, float4 (tid % 4) + 4 t, for all R rows
   const int kl = tid >> 2, qp = tid & 3;
-  float tmax = -INFINITY;
-  for (int k0 = 0; k0 <= last; k0 += kFusedKeys) {
+  float tmax[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) tmax[r] = -INFINITY;
+  for (int k0 = 0; k0 <= last_block; k0 += kFusedKeys) {
     __syncthreads();  // the previous tile is no longer read (and qs is written)
     for (int f = tid; f < kFusedKeys * (D / 4); f += kFusedThreads) {
       const int r = f / (D / 4), c4 = f % (D / 4);
       float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (k0 + r <= last) x = ld4(Kh + (int64_t)(k0 + r) * D + 4 * c4);
+      if (k0 + r <= last_block) x = ld4(Kh + (int64_t)(k0 + r) * D + 4 * c4);
       *reinterpret_cast<float4*>(Ks + r * LDK + 4 * c4) = x;
     }
     __syncthreads();
-    float dot = 0.f;
+    float dot[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) dot[r] = 0.f;
 #pragma unroll
     for (int c = 4 * qp; c < D; c += 16) {
       const float4 kv = ld4(Ks + kl * LDK + c);
-      const float4 qv = ld4(qs + c);
-      dot = fmaf(qv.x, kv.x, dot);
-      dot = fmaf(qv.y, kv.y, dot);
-      dot = fmaf(qv.z, kv.z, dot);
-      dot = fmaf(qv.w, kv.w, dot);
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const float4 qv = ld4(qs + r * D + c);
+        dot[r] = fmaf(qv.x, kv.x, dot[r]);
+        dot[r] = fmaf(qv.y, kv.y, dot[r]);
+        dot[r] = fmaf(qv.z, kv.z, dot[r]);
+        dot[r] = fmaf(qv.w, kv.w, dot[r]);
+      }
     }
-    dot += __shfl_xor_sync(0xffffffffu, dot, 1);
-    dot += __shfl_xor_sync(0xffffffffu, dot, 2);
     const int key = k0 + kl;
-    if (qp == 0 && key <= last) {
-      sc[key] = dot;
-      tmax = fmaxf(tmax, dot);
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      float x = dot[r];
+      x += __shfl_xor_sync(0xffffffffu, x, 1);
+      x += __shfl_xor_sync(0xffffffffu, x, 2);
+      const int last_r = causal ? min(i0 + r, S - 1) : S - 1;
+      if (qp == 0 && key <= last_block) {
+        const float sv = key <= last_r ? x : -INFINITY;
+        sc[r * S + key] = sv;
+        tmax[r] = fmaxf(tmax[r], sv);
+      }
     }
   }
-  const float m = block_max(tmax, red);  // its barriers also publish sc[]
-  float tsum = 0.f;
-  for (int j = tid; j <= last; j += kFusedThreads) {
-    const float p = exp2f(sc[j] - m);
-    sc[j] = p;
-    tsum += p;
+  block_rows<R, true>(tmax, red);  // its barriers also publish sc[]
+  float tsum[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    tsum[r] = 0.f;
+    for (int j = tid; j <= last_block; j += kFusedThreads) {
+      const float p = exp2f(sc[r * S + j] - tmax[r]);
+      sc[r * S + j] = p;
+      tsum[r] += p;
+    }
   }
-  const float l = block_sum(tsum, red);  // its barriers also publish the new sc[]
+  block_rows<R, false>(tsum, red);  // its barriers also publish the new sc[]
 
-  constexpr int R = kFusedThreads / D;  // key groups
   const int c = tid % D, g = tid / D;
-  float acc = 0.f;
-  for (int j = g; j <= last; j += R) acc = fmaf(sc[j], Vh[(int64_t)j * D + c], acc);
-  part[tid] = acc;
+  float acc[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) acc[r] = 0.f;
+  for (int j = g; j <= last_block; j += G) {
+    const float v = Vh[(int64_t)j * D + c];
+#pragma unroll
+    for (int r = 0; r < R; ++r) acc[r] = fmaf(sc[r * S + j], v, acc[r]);
+  }
+#pragma unroll
+  for (int r = 0; r < R; ++r) part[r * kFusedThreads + tid] = acc[r];
+  if (tid == 0) {
+#pragma unroll
+    for (int r = 0; r < R; ++r) red[r] = tsum[r];  // row sums, indexed by a runtime row below
+  }
   __syncthreads();
-  if (g == 0) {
+  for (int f = tid; f < R * D; f += kFusedThreads) {
+    const int r = f / D, cc = f % D;
+    if (i0 + r >= S) continue;
     float t = 0.f;
 #pragma unroll
-    for (int r = 0; r < R; ++r) t += part[r * D + c];
-    O[(n * S + i) * D + c] = t / l;
+    for (int gg = 0; gg < G; ++gg) t += part[r * kFusedThreads + gg * D + cc];
+    O[(n * S + i0 + r) * D + cc] = t / red[r];
   }
 }
 
 size_t flash_smem(int d) { return sizeof(float) * (size_t)(2 * d * kLD + kBC * d + kBC * kLD); }
 size_t naive_scores_smem(int d) { return sizeof(float) * (size_t)(2 * d * kLD); }
 size_t naive_pv_smem(int d) { return sizeof(float) * (size_t)(kBC * kLD + kBC * d); }
-size_t fused_smem(int S, int d) {
-  return sizeof(float) * (size_t)(kFusedKeys * (d + 16) + d + 32 + kFusedThreads + S);
+size_t fused_smem(int S, int d, int rows = 1) {
+  return sizeof(float) * (size_t)(kFusedKeys * (d + 16) + rows * d + kFusedWarps * rows + rows * kFusedThreads +
+                                  (size_t)rows * S);
 }
 
 template <typename F>
@@ -446,14 +513,30 @@ cudaError_t naive_launch(const AttnProblem& p, float* scores, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-template <int D>
-cudaError_t fused_launch(const AttnProblem& p, cudaStream_t st) {
-  const size_t smem = fused_smem(p.S, D);
-  cudaError_t e = set_smem(fused_row_f32_kernel<D>, smem);
+template <int D, int R>
+cudaError_t fused_launch_rows(const AttnProblem& p, size_t smem, cudaStream_t st) {
+  cudaError_t e = set_smem(fused_row_f32_kernel<D, R>, smem);
   if (e != cudaSuccess) return e;
-  fused_row_f32_kernel<D><<<(unsigned)(p.N * p.S), kFusedThreads, smem, st>>>(
+  const int64_t blocks = p.N * ((p.S + R - 1) / R);
+  fused_row_f32_kernel<D, R><<<(unsigned)blocks, kFusedThreads, smem, st>>>(
       (const float*)p.q, (const float*)p.k, (const float*)p.v, (float*)p.o, p.S, p.causal, p.scale * kLog2e);
   return cudaGetLastError();
+}
+
+// R = 4 query rows per block where their score rows fit in shared memory and
+// the grid still has at least two blocks per SM, else 2, else 1.
+template <int D>
+cudaError_t fused_launch(const AttnProblem& p, cudaStream_t st) {
+  int dev = 0, optin = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int64_t rows = p.N * p.S;
+  auto fits = [&](int r) { return fused_smem(p.S, D, r) <= (size_t)optin && rows / r >= 2 * (int64_t)sms; };
+  if (fits(4)) return fused_launch_rows<D, 4>(p, fused_smem(p.S, D, 4), st);
+  if (fits(2)) return fused_launch_rows<D, 2>(p, fused_smem(p.S, D, 2), st);
+  return fused_launch_rows<D, 1>(p, fused_smem(p.S, D, 1), st);
 }
 
 }  // namespace
