@@ -59,6 +59,10 @@ def parse_args(argv=None):
     p.add_argument("--no-triad", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--oracle-table", action="store_true",
+                   help="time the CPU oracle on every workload (bounded row samples, one thread and all "
+                        "host threads) and print a Markdown table instead of the JSON line")
+    p.add_argument("--oracle-seconds", type=float, default=10.0, help="oracle time budget per workload and mode")
     return p.parse_args(argv)
 
 
@@ -186,6 +190,83 @@ def oracle_sample(w, q64, k64, v64, seconds: float, seed: int = 0, gpu_out=None)
         diff = np.abs(got - np.concatenate(outs))
         parity = {"rows": int(done), "max_abs": float(diff.max()), "mean_abs": float(diff.mean())}
     return flops, elapsed, int(done), parity
+
+
+def oracle_threads_rate(w, q64, k64, v64, seconds: float, threads: int, seed: int = 0):
+    """The oracle on the same seeded row sample, split over `threads` host
+    threads (the oracle's ctypes calls release the GIL). Returns (flops, wall
+    seconds, rows)."""
+    import concurrent.futures as cf
+
+    import numpy as np
+    import torch
+
+    import oracle
+    from roofline_benchmarking_gb300 import inputs
+
+    heads, rows = inputs.sample_rows(w, per_head=min(w.S, 512), seed=seed)
+    perm = torch.randperm(len(heads), generator=torch.Generator().manual_seed(seed))
+    heads, rows = heads[perm].numpy(), rows[perm].numpy()
+    orc = oracle.get()
+    parts = [(heads[t::threads], rows[t::threads]) for t in range(threads)]
+    chunk = max(4, int(4e6 / (4.0 * w.S * w.d)))  # rows per call: a few MFLOP, so Python overhead stays small
+
+    def work(part):
+        h_all, r_all = part
+        done, flops, t0 = 0, 0.0, time.perf_counter()
+        while done < len(h_all) and time.perf_counter() - t0 < seconds:
+            h, r = h_all[done:done + chunk], r_all[done:done + chunk]
+            orc.attn_rows(q64, k64, v64, w.causal, w.scale, h, r)
+            vis = (r + 1) if w.causal else np.full(len(r), w.S)
+            flops += float(np.sum(4.0 * vis * w.d))
+            done += len(h)
+        return flops, done
+
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        res = list(ex.map(work, parts))
+    wall = time.perf_counter() - t0
+    return sum(f for f, _ in res), wall, sum(n for _, n in res)
+
+
+def oracle_table(args) -> int:
+    """The CPU oracle's rate on every workload: a time-bounded seeded row sample
+    on one thread and on all host threads, with the full-problem time
+    extrapolated by the exact FLOP count of the visible keys."""
+    import numpy as np
+
+    import oracle
+    from roofline_benchmarking_gb300 import inputs
+
+    threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    print(f"Host CPU: {host_cpu_model()}; {threads} threads available; budget {args.oracle_seconds:g} s per "
+          f"workload and mode.\n")
+    print("| workload | rows evaluated (1 thread) | of all rows | 1 thread GFLOP/s | full problem, 1 thread (s) | "
+          f"{threads} threads GFLOP/s | full problem, {threads} threads (s) |")
+    print("|---|---|---|---|---|---|---|")
+    for w in (inputs.SINGLE_HEAD_F32, inputs.F32_S1024, inputs.F32_S1024_CAUSAL, inputs.BF16_CAUSAL_S4096,
+              inputs.BF16_S2048_D64, inputs.BF16_CAUSAL_S16384, inputs.BF16_CAUSAL_D256):
+        q64, k64, v64 = widen(*inputs.make_qkv(w))
+        vis_total = w.N * (w.S * (w.S + 1) / 2 if w.causal else float(w.S) * w.S)
+        full_flops = 4.0 * w.d * vis_total
+        f1, t1, n1, _ = oracle_sample(w, q64, k64, v64, args.oracle_seconds, seed=7)
+        fm, tm, _ = oracle_threads_rate(w, q64, k64, v64, args.oracle_seconds, threads, seed=7)
+        r1, rm = f1 / t1, fm / tm
+        print(f"| {w.name} | {n1} | {n1 / (w.N * w.S):.2%} | {r1 / 1e9:.2f} | {full_flops / r1:.1f} | "
+              f"{rm / 1e9:.2f} | {full_flops / rm:.1f} |", flush=True)
+    # the Q15 fixed-point model, whole problem, one thread
+    orc = oracle.get()
+    for w in (inputs.Q15_SINGLE_HEAD, inputs.Q15_S1024, inputs.Q15_S1024_CAUSAL):
+        q, k, v = inputs.make_qkv(w)
+        t0 = time.perf_counter()
+        orc.attn_q15(q, k, v, w.causal, w.scale)
+        t = time.perf_counter() - t0
+        vis_total = w.N * (w.S * (w.S + 1) / 2 if w.causal else float(w.S) * w.S)
+        ops = 4.0 * w.d * vis_total
+        print(f"| {w.name} (Q15 model, integer ops) | {w.N * w.S} | 100.00% | {ops / t / 1e9:.2f} | {t:.2f} | - | - |",
+              flush=True)
+    del np
+    return 0
 
 
 # ----------------------------------------------------------------------------- reference arm
@@ -440,6 +521,8 @@ def e2e_rate(args, w, qh, kh, vh, q, k, v, o, variant, stream, d: Dist) -> dict:
 
 def main(argv=None):
     args = parse_args(argv)
+    if args.oracle_table:
+        return oracle_table(args)
     d = Dist()
     if args.impl == "reference":
         return run_reference(args, d)

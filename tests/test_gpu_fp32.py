@@ -108,3 +108,18 @@ def test_graph_replay_matches_oracle(oracle, variant):
     want = oracle.attn(*inputs.make_qkv(w), w.causal, w.scale)
     mx, _, _ = errors(got, want)
     assert mx <= (F32_TOL if variant != Variant.TC else 2e-2), mx
+
+
+@pytest.mark.parametrize("shape", [(1, 8, 1023, 64, False), (1, 8, 1021, 64, True), (2, 4, 777, 32, True),
+                                   (1, 4, 513, 128, False), (1, 3, 1030, 128, True)],
+                         ids=lambda s: "b{}h{}s{}d{}{}".format(*s[:4], "c" if s[4] else ""))
+def test_fused_four_rows_per_block_with_ragged_tails(oracle, shape):
+    """Grids large enough that the fused-row kernel takes four query rows per
+    block, with S not a multiple of four (the last block of each head is
+    partial) and causal rows whose key ranges differ within a block."""
+    B, H, S, d, causal = shape
+    w = inputs.Workload("t", B, H, S, d, causal, "f32", 500 + S, "uniform")
+    got = run(w, Variant.FUSED)
+    want = oracle.attn(*inputs.make_qkv(w), causal, w.scale)
+    mx, mean, _ = errors(got, want)
+    assert mx <= F32_TOL, (mx, mean)
