@@ -49,7 +49,7 @@ int validate(const void* q, const void* k, const void* v, const void* o, int B, 
   if (var == KB_FIXEDPOINT) {
     // keeps every fixed-point intermediate inside 64 bits
     if (S > 65536 || !q15_scale_ok(scale)) return KB_ERR_INVALID_ARG;
-    if (N * ((S + 31) / 32) > std::numeric_limits<int32_t>::max()) return KB_ERR_UNSUPPORTED;
+    if (N * ((S + 15) / 16) > std::numeric_limits<int32_t>::max()) return KB_ERR_UNSUPPORTED;  // 16-row blocks
   }
   // one block per query row (fused) or per 64-row tile (flash, naive)
   const int64_t grid_limit = std::numeric_limits<int32_t>::max();

@@ -19,11 +19,13 @@
 //   output  acc_c / l rounded to nearest, halves away from zero, saturated.
 // Every step is integer arithmetic, so the result is defined bit for bit.
 //
-// GPU layout: one block per 32 query rows of one head, 256 threads, 8 per
-// row. Per 32-key tile the block stages K and V in shared memory; thread g of
-// a row computes the scores of keys g, g+8, g+16, g+24, the row's 8 threads
-// combine the tile maximum and the weight sum with shuffles, and each thread
-// accumulates d/8 contiguous output channels in 64-bit registers. The tiles
+// GPU layout: one block per ROWS query rows of one head (32 rows; 16 under
+// the causal mask, where short blocks balance the triangle), 8 threads per
+// row. Per 32-key tile the block stages K (split into low and high bytes) and
+// V (split and transposed to channel-major) in shared memory; thread g of a
+// row computes the scores of keys g, g+8, g+16, g+24 with dp2a, the row's 8
+// threads combine the tile maximum and the weight sum with shuffles, and each
+// thread accumulates channels g, g+8, ... in 64-bit registers. The tiles
 // are the model's tiles, and the block's rows all use the same tile bounds, so
 // the sequence of rescales is exactly the model's.
 #include <cuda_runtime.h>
@@ -35,9 +37,7 @@
 namespace kb {
 namespace {
 
-constexpr int kRows = 32;     // query rows per block
 constexpr int kTile = 32;     // keys per tile
-constexpr int kThreads = 256; // 8 threads per query row
 constexpr double kLog2e = 1.4426950408889634074;
 
 struct Q15Params {
@@ -57,62 +57,136 @@ __device__ __forceinline__ long long round_div(long long a, long long b) {
   return a >= 0 ? (a + b / 2) / b : -((-a + b / 2) / b);
 }
 
-__device__ __forceinline__ int lo16(int w) { return (int)(short)(w & 0xffff); }
-__device__ __forceinline__ int hi16(int w) { return w >> 16; }  // arithmetic shift keeps the sign
+// Two-way 16-bit x 8-bit dot products (dp2a): d = c + a.h0 * b.byte(2s) + a.h1 * b.byte(2s+1),
+// s = 0 (.lo) or 1 (.hi); the first type names a's halves, the second b's bytes.
+__device__ __forceinline__ int dp2a_lo_su(int a, unsigned b, int c) {
+  int d;
+  asm("dp2a.lo.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ int dp2a_hi_su(int a, unsigned b, int c) {
+  int d;
+  asm("dp2a.hi.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ int dp2a_lo_ss(int a, unsigned b, int c) {
+  int d;
+  asm("dp2a.lo.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ int dp2a_hi_ss(int a, unsigned b, int c) {
+  int d;
+  asm("dp2a.hi.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ unsigned dp2a_lo_uu(unsigned a, unsigned b, unsigned c) {
+  unsigned d;
+  asm("dp2a.lo.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ unsigned dp2a_hi_uu(unsigned a, unsigned b, unsigned c) {
+  unsigned d;
+  asm("dp2a.hi.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ int dp2a_lo_us(unsigned a, unsigned b, int c) {
+  int d;
+  asm("dp2a.lo.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ int dp2a_hi_us(unsigned a, unsigned b, int c) {
+  int d;
+  asm("dp2a.hi.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
 
-template <int D>
-__global__ void __launch_bounds__(kThreads) q15_attn_kernel(const short* __restrict__ Q,
+// Four int16 values (packed as two words) split into their low bytes
+// (unsigned, x & 255) and high bytes (signed, x >> 8): x = 256 * hi + lo.
+__device__ __forceinline__ void split4(int2 x, unsigned& lo, unsigned& hi) {
+  const int a = (int)(short)(x.x & 0xffff), b = x.x >> 16, c = (int)(short)(x.y & 0xffff), d = x.y >> 16;
+  lo = (unsigned)(a & 255) | ((unsigned)(b & 255) << 8) | ((unsigned)(c & 255) << 16) | ((unsigned)(d & 255) << 24);
+  hi = (unsigned)((a >> 8) & 255) | ((unsigned)((b >> 8) & 255) << 8) | ((unsigned)((c >> 8) & 255) << 16) |
+       ((unsigned)((d >> 8) & 255) << 24);
+}
+
+// The integer products are formed with dp2a: a key k = 256 kh + kl splits into
+// a signed high byte and an unsigned low byte, so q . k = 256 (q . kh) + q . kl
+// with both partial sums exact in 32 bits (|q kh| <= 2^22, 0 <= ... q kl < 2^23,
+// at most 128 terms); likewise each tile's sum over 32 keys of p v (p <= 2^15).
+template <int D, int ROWS>
+__global__ void __launch_bounds__(8 * ROWS) q15_attn_kernel(const short* __restrict__ Q,
                                                            const short* __restrict__ K,
                                                            const short* __restrict__ V, short* __restrict__ O,
                                                            int S, int tiles_per_head, int causal,
                                                            const Q15Params prm) {
-  constexpr int LD = D + 8;        // int16 per staged row: 16-byte pad, 8 rows of one load hit distinct banks
-  constexpr int VPR = D / 8;       // 16-byte vectors per row
-  constexpr int CH = D / 8;        // output channels per thread
-  __shared__ __align__(16) short Qs[kRows][LD];
-  __shared__ __align__(16) short Ks[kTile][LD];
+  constexpr int QW = D / 2;       // words (int16 pairs) of a query row
+  constexpr int KW = D / 4;       // words (byte quads) of a split key row
+  constexpr int KLD = KW + 4;     // padded: the 8 rows read by one load phase fall in distinct banks
+  constexpr int VLD = kTile / 4 + 4;  // words of a split value column (32 keys), padded likewise
+  constexpr int CH = D / 8;       // output channels per thread: g, g + 8, ...
+  constexpr int kThreads = 8 * ROWS;
+  __shared__ __align__(16) int Qw[ROWS][QW];
+  __shared__ __align__(16) unsigned Kl[kTile][KLD], Kh[kTile][KLD];
   __shared__ __align__(16) short Vs[kTile][D];
-  __shared__ int Ps[kRows][kTile + 1];
+  __shared__ __align__(16) unsigned Vl[D][VLD], Vh[D][VLD];
+  __shared__ __align__(16) unsigned Pw[ROWS][kTile / 2];
   __shared__ unsigned short tab[64];
 
   const int tid = threadIdx.x;
   const int r = tid >> 3, g = tid & 7;
   const long long n = blockIdx.x / tiles_per_head;
-  const int i0 = (int)(blockIdx.x % tiles_per_head) * kRows;
+  const int i0 = (int)(blockIdx.x % tiles_per_head) * ROWS;
   const int i = i0 + r;
   const short* Qh = Q + n * S * D;
-  const short* Kh = K + n * S * D;
-  const short* Vh = V + n * S * D;
+  const short* Kg = K + n * S * D;
+  const short* Vg = V + n * S * D;
 
   if (tid < 64) tab[tid] = prm.t[tid];
-  for (int f = tid; f < kRows * VPR; f += kThreads) {
-    const int rr = f / VPR, c8 = f % VPR;
+  for (int f = tid; f < ROWS * (D / 8); f += kThreads) {
+    const int rr = f / (D / 8), c8 = f % (D / 8);
     int4 x = make_int4(0, 0, 0, 0);
     if (i0 + rr < S) x = *reinterpret_cast<const int4*>(Qh + (long long)(i0 + rr) * D + 8 * c8);
-    *reinterpret_cast<int4*>(&Qs[rr][8 * c8]) = x;
+    *reinterpret_cast<int4*>(&Qw[rr][4 * c8]) = x;
   }
 
-  // rows past S (the ragged tail) run on zeros and are not stored
   const int my_last = causal ? min(i, S - 1) : S - 1;
-  const int block_last = causal ? min(i0 + kRows - 1, S - 1) : S - 1;
+  const int block_last = causal ? min(i0 + ROWS - 1, S - 1) : S - 1;
   long long m = 0, l = 0, acc[CH];
   bool have_m = false;
 #pragma unroll
   for (int c = 0; c < CH; ++c) acc[c] = 0;
 
   for (int t0 = 0; t0 <= block_last; t0 += kTile) {
-    __syncthreads();  // the previous tile is no longer read
-    for (int f = tid; f < kTile * VPR; f += kThreads) {
-      const int rr = f / VPR, c8 = f % VPR;
-      int4 kx = make_int4(0, 0, 0, 0), vx = kx;
-      if (t0 + rr < S) {
-        kx = *reinterpret_cast<const int4*>(Kh + (long long)(t0 + rr) * D + 8 * c8);
-        vx = *reinterpret_cast<const int4*>(Vh + (long long)(t0 + rr) * D + 8 * c8);
-      }
-      *reinterpret_cast<int4*>(&Ks[rr][8 * c8]) = kx;
-      *reinterpret_cast<int4*>(&Vs[rr][8 * c8]) = vx;
+    __syncthreads();  // the previous tile is no longer read (and Qw is written)
+    // K: split each quad of features into low and high bytes
+    for (int f = tid; f < kTile * KW; f += kThreads) {
+      const int j = f / KW, w = f % KW;
+      int2 x = make_int2(0, 0);
+      if (t0 + j < S) x = *reinterpret_cast<const int2*>(Kg + (long long)(t0 + j) * D + 4 * w);
+      unsigned lo, hi;
+      split4(x, lo, hi);
+      Kl[j][w] = lo;
+      Kh[j][w] = hi;
+    }
+    // V: staged as is (coalesced), then split and transposed below
+    for (int f = tid; f < kTile * (D / 8); f += kThreads) {
+      const int j = f / (D / 8), c8 = f % (D / 8);
+      int4 x = make_int4(0, 0, 0, 0);
+      if (t0 + j < S) x = *reinterpret_cast<const int4*>(Vg + (long long)(t0 + j) * D + 8 * c8);
+      *reinterpret_cast<int4*>(&Vs[j][8 * c8]) = x;
     }
     __syncthreads();
+    for (int f = tid; f < D * (kTile / 4); f += kThreads) {
+      const int c = f / (kTile / 4), kq = f % (kTile / 4);
+      const int2 x = make_int2((int)((unsigned)(unsigned short)Vs[4 * kq][c] |
+                                     ((unsigned)(unsigned short)Vs[4 * kq + 1][c] << 16)),
+                               (int)((unsigned)(unsigned short)Vs[4 * kq + 2][c] |
+                                     ((unsigned)(unsigned short)Vs[4 * kq + 3][c] << 16)));
+      unsigned lo, hi;
+      split4(x, lo, hi);
+      Vl[c][kq] = lo;
+      Vh[c][kq] = hi;
+    }
 
     // scores of keys g, g+8, g+16, g+24 of the tile
     long long z[4];
@@ -122,17 +196,24 @@ __global__ void __launch_bounds__(kThreads) q15_attn_kernel(const short* __restr
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int kk = g + 8 * u;
-      long long dot = 0;
+      int accl = 0, acch = 0;
 #pragma unroll
-      for (int c8 = 0; c8 < VPR; ++c8) {
-        const int4 a = *reinterpret_cast<const int4*>(&Qs[r][8 * c8]);
-        const int4 b = *reinterpret_cast<const int4*>(&Ks[kk][8 * c8]);
-        dot += (long long)(lo16(a.x) * lo16(b.x)) + (long long)(hi16(a.x) * hi16(b.x));
-        dot += (long long)(lo16(a.y) * lo16(b.y)) + (long long)(hi16(a.y) * hi16(b.y));
-        dot += (long long)(lo16(a.z) * lo16(b.z)) + (long long)(hi16(a.z) * hi16(b.z));
-        dot += (long long)(lo16(a.w) * lo16(b.w)) + (long long)(hi16(a.w) * hi16(b.w));
+      for (int w = 0; w < KW; w += 4) {
+        const uint4 kl = *reinterpret_cast<const uint4*>(&Kl[kk][w]);
+        const uint4 kh = *reinterpret_cast<const uint4*>(&Kh[kk][w]);
+        const int4 qa = *reinterpret_cast<const int4*>(&Qw[r][2 * w]);
+        const int4 qb = *reinterpret_cast<const int4*>(&Qw[r][2 * w + 4]);
+        accl = dp2a_lo_su(qa.x, kl.x, accl); accl = dp2a_hi_su(qa.y, kl.x, accl);
+        acch = dp2a_lo_ss(qa.x, kh.x, acch); acch = dp2a_hi_ss(qa.y, kh.x, acch);
+        accl = dp2a_lo_su(qa.z, kl.y, accl); accl = dp2a_hi_su(qa.w, kl.y, accl);
+        acch = dp2a_lo_ss(qa.z, kh.y, acch); acch = dp2a_hi_ss(qa.w, kh.y, acch);
+        accl = dp2a_lo_su(qb.x, kl.z, accl); accl = dp2a_hi_su(qb.y, kl.z, accl);
+        acch = dp2a_lo_ss(qb.x, kh.z, acch); acch = dp2a_hi_ss(qb.y, kh.z, acch);
+        accl = dp2a_lo_su(qb.z, kl.w, accl); accl = dp2a_hi_su(qb.w, kl.w, accl);
+        acch = dp2a_lo_ss(qb.z, kh.w, acch); acch = dp2a_hi_ss(qb.w, kh.w, acch);
       }
-      z[u] = ((dot >> 14) * prm.C) >> 16;  // arithmetic shifts: floor
+      const long long dot = (long long)acch * 256 + accl;  // the exact sum of the d products
+      z[u] = ((dot >> 14) * prm.C) >> 16;                   // arithmetic shifts: floor
       ok[u] = t0 + kk <= my_last;
       if (ok[u] && (!any || z[u] > mt)) mt = z[u];
       any = any || ok[u];
@@ -160,51 +241,67 @@ __global__ void __launch_bounds__(kThreads) q15_attn_kernel(const short* __restr
     long long psum = 0;
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      const long long p = (any && ok[u]) ? pow2_neg(m - z[u], tab) : 0;
-      Ps[r][g + 8 * u] = (int)p;
+      const unsigned p = (any && ok[u]) ? (unsigned)pow2_neg(m - z[u], tab) : 0u;  // <= 2^15
       psum += p;
+      // weights of keys 2m and 2m+1 share a word: even threads take their odd neighbour's
+      const unsigned pn = __shfl_down_sync(0xffffffffu, p, 1);
+      if ((g & 1) == 0) Pw[r][(g + 8 * u) >> 1] = p | (pn << 16);
     }
 #pragma unroll
     for (int s = 1; s < 8; s <<= 1) psum += __shfl_xor_sync(0xffffffffu, psum, s);
     l += psum;
-    __syncwarp();  // the row's weights are written by, and read by, this warp only
+    __syncthreads();  // Vl / Vh complete; the row's weights written
 
-    // acc_c += p_j * v_jc over the tile; this thread owns channels g*CH .. g*CH+CH-1
-#pragma unroll 4
-    for (int kk = 0; kk < kTile; ++kk) {
-      const int p = Ps[r][kk];
-      const short* vrow = &Vs[kk][g * CH];
+    // acc_c += sum_j p_j v_jc over the tile for channels c = g + 8 i
+    uint4 pw[kTile / 8];
 #pragma unroll
-      for (int c2 = 0; c2 < CH; c2 += 2) {
-        const int w = *reinterpret_cast<const int*>(vrow + c2);
-        acc[c2] += (long long)(p * lo16(w));
-        acc[c2 + 1] += (long long)(p * hi16(w));
+    for (int q4 = 0; q4 < kTile / 8; ++q4) pw[q4] = *reinterpret_cast<const uint4*>(&Pw[r][4 * q4]);
+#pragma unroll
+    for (int ci = 0; ci < CH; ++ci) {
+      const int c = g + 8 * ci;
+      unsigned al = 0;
+      int ah = 0;
+#pragma unroll
+      for (int q4 = 0; q4 < kTile / 16; ++q4) {
+        const uint4 vl = *reinterpret_cast<const uint4*>(&Vl[c][4 * q4]);
+        const uint4 vh = *reinterpret_cast<const uint4*>(&Vh[c][4 * q4]);
+        const uint4 pa = pw[2 * q4], pb = pw[2 * q4 + 1];  // keys 16 q4 .. 16 q4 + 15 as 8 pairs
+        al = dp2a_lo_uu(pa.x, vl.x, al); al = dp2a_hi_uu(pa.y, vl.x, al);
+        ah = dp2a_lo_us(pa.x, vh.x, ah); ah = dp2a_hi_us(pa.y, vh.x, ah);
+        al = dp2a_lo_uu(pa.z, vl.y, al); al = dp2a_hi_uu(pa.w, vl.y, al);
+        ah = dp2a_lo_us(pa.z, vh.y, ah); ah = dp2a_hi_us(pa.w, vh.y, ah);
+        al = dp2a_lo_uu(pb.x, vl.z, al); al = dp2a_hi_uu(pb.y, vl.z, al);
+        ah = dp2a_lo_us(pb.x, vh.z, ah); ah = dp2a_hi_us(pb.y, vh.z, ah);
+        al = dp2a_lo_uu(pb.z, vl.w, al); al = dp2a_hi_uu(pb.w, vl.w, al);
+        ah = dp2a_lo_us(pb.z, vh.w, ah); ah = dp2a_hi_us(pb.w, vh.w, ah);
       }
+      acc[ci] += (long long)ah * 256 + (long long)al;
     }
   }
 
   if (i < S) {
-    __align__(8) short out[CH];
+    short* dst = O + (n * S + i) * D;
 #pragma unroll
-    for (int c = 0; c < CH; ++c) {
-      long long x = round_div(acc[c], l);
+    for (int ci = 0; ci < CH; ++ci) {
+      long long x = round_div(acc[ci], l);
       x = x > 32767 ? 32767 : (x < -32768 ? -32768 : x);
-      out[c] = (short)x;
+      dst[g + 8 * ci] = (short)x;
     }
-    short* dst = O + (n * S + i) * D + g * CH;
-#pragma unroll
-    for (int c = 0; c < CH; c += 4)
-      *reinterpret_cast<int2*>(dst + c) = *reinterpret_cast<const int2*>(out + c);
   }
+}
+
+template <int D, int ROWS>
+cudaError_t q15_launch_rows(const AttnProblem& p, const Q15Params& prm, cudaStream_t st) {
+  const int tiles = (p.S + ROWS - 1) / ROWS;
+  q15_attn_kernel<D, ROWS><<<(unsigned)(p.N * tiles), 8 * ROWS, 0, st>>>(
+      static_cast<const short*>(p.q), static_cast<const short*>(p.k), static_cast<const short*>(p.v),
+      static_cast<short*>(p.o), p.S, tiles, p.causal, prm);
+  return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t q15_launch(const AttnProblem& p, const Q15Params& prm, cudaStream_t st) {
-  const int tiles = (p.S + kRows - 1) / kRows;
-  q15_attn_kernel<D><<<(unsigned)(p.N * tiles), kThreads, 0, st>>>(
-      static_cast<const short*>(p.q), static_cast<const short*>(p.k), static_cast<const short*>(p.v),
-      static_cast<short*>(p.o), p.S, tiles, p.causal, prm);
-  return cudaGetLastError();
+  return p.causal ? q15_launch_rows<D, 16>(p, prm, st) : q15_launch_rows<D, 32>(p, prm, st);
 }
 
 }  // namespace
