@@ -101,6 +101,12 @@ class Dist:
             dist.destroy_process_group()
 
 
+def aggregate_tflops(flops_per_replica: float, world: int, ms_per_step: float) -> float:
+    """Whole-job rate: every rank runs the whole workload (replicas), and the
+    step time is the maximum over ranks."""
+    return flops_per_replica * world / (ms_per_step * 1e-3) / 1e12
+
+
 # ----------------------------------------------------------------------------- clocks
 from roofline_benchmarking_gb300.clocks import ClockSampler, gpu_id_for_smi  # noqa: E402
 
@@ -398,7 +404,7 @@ def run_ours(args, d: Dist):
 
     total_ms = d.max(total_ms)
     ms_per_step = total_ms / K
-    value = w.flops * d.world / (ms_per_step * 1e-3) / 1e12
+    value = aggregate_tflops(w.flops, d.world, ms_per_step)
 
     peaks, src = rf.load_measured_peaks()
     mean_launch_s = statistics.mean(launch_ms) * 1e-3
@@ -513,7 +519,7 @@ def e2e_rate(args, w, qh, kh, vh, q, k, v, o, variant, stream, d: Dist) -> dict:
     same = bool(torch.equal(op[(K - 1) % 2], o_ref.cpu()))
     h2d = sum(t.numel() * t.element_size() for t in (qp, kp, vp))
     d2h = op[0].numel() * op[0].element_size()
-    return {"value": w.flops * d.world / (ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+    return {"value": aggregate_tflops(w.flops, d.world, ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": K, "host_buffers": "pinned",
             "pipelining": "2 buffer sets; input copy, kernel and output copy of neighbouring steps overlap",
             "output_equals_device_run": same}
