@@ -500,15 +500,17 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
 // score buffers (the scores of key tile j+1 are computed while the softmax
 // works on tile j) and the 128 x 256 O. Key tiles are 64 keys; K and V rings
 // of two 32 KB stages each plus the 64 KB Q tile use 192 KB of shared memory.
-// Warps 0-3 run the softmax (thread = row = TMEM lane), warp 4 drives TMA,
-// warp 5 issues the MMAs. MMA order per item: S(0), S(1), then for each j:
+// Warps 0-3 run the softmax (thread = row = TMEM lane), warp 4 loads Q and K
+// with TMA, warp 6 loads V (so K tiles are not held behind V's ring), warp 5
+// issues the MMAs. MMA order per item: S(0), S(1), then for each j:
 // PV(j), S(j+2). S(j+2) reuses the buffer of P(j) only after PV(j) read it
 // (in-order execution); since PV(j) is no longer ordered before S(j+1), a
 // softmax that must rescale O first waits for the PVDONE commit of PV(j-1).
 // ---------------------------------------------------------------------------
-constexpr int kThreads256 = 192;
-constexpr int kWarpTMA256 = 4;
+constexpr int kThreads256 = 224;
+constexpr int kWarpTMA256 = 4;   // Q and K tiles
 constexpr int kWarpMMA256 = 5;
+constexpr int kWarpTMAV256 = 6;  // V tiles: a producer of its own, so K loads run ahead of V's
 constexpr int kBN256 = 64;
 
 struct Tc256 {
@@ -619,12 +621,11 @@ __global__ void __launch_bounds__(kThreads256, 1)
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + C::OFF_MISC);
 
   if (warp == kWarpTMA256) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ TMA producer: Q and K
     if (lane == 0) {
       ptx::tma_prefetch_desc(&tmq);
       ptx::tma_prefetch_desc(&tmk);
-      ptx::tma_prefetch_desc(&tmv);
-      int kdone = 0, vdone = 0, items = 0;
+      int kdone = 0, items = 0;
       bool ok = true;
       Item256 it;
       for (int round = 0; ok && sched.get(round, it); ++round) {
@@ -634,7 +635,7 @@ __global__ void __launch_bounds__(kThreads256, 1)
         for (int b = 0; b < 4; ++b)
           ptx::tma_load_3d(base + C::OFF_Q + b * C::QBLK, &tmq, bar(C::B_Q), b * 64, it.q0, it.n);
         for (int j = 0; j < it.nk && ok; ++j) {
-          const int ks = kdone % C::KS, vs = vdone % C::VS;
+          const int ks = kdone % C::KS;
           if (kdone >= C::KS) ok = wait_bar(bar(C::B_KEMPTY + ks), ((kdone / C::KS) & 1) ^ 1, abort_flag, limit, true);
           if (!ok) break;
           ptx::mbar_arrive_expect_tx(bar(C::B_KFULL + ks), C::KTILE);
@@ -642,6 +643,24 @@ __global__ void __launch_bounds__(kThreads256, 1)
             ptx::tma_load_3d(base + C::OFF_K + ks * C::KTILE + b * C::KBLK, &tmk, bar(C::B_KFULL + ks), b * 64,
                              j * kBN256, it.n);
           ++kdone;
+        }
+        ++items;
+      }
+      if (items > 0) wait_bar(bar(C::B_Q), (items - 1) & 1, abort_flag, limit, false);
+      for (int x = kdone - C::KS < 0 ? 0 : kdone - C::KS; x < kdone; ++x)
+        wait_bar(bar(C::B_KFULL + x % C::KS), (x / C::KS) & 1, abort_flag, limit, false);
+    }
+    __syncwarp();
+  } else if (warp == kWarpTMAV256) {
+    // ------------------------------------------------------------ TMA producer: V
+    if (lane == 0) {
+      ptx::tma_prefetch_desc(&tmv);
+      int vdone = 0;
+      bool ok = true;
+      Item256 it;
+      for (int round = 0; ok && sched.get(round, it); ++round) {
+        for (int j = 0; j < it.nk && ok; ++j) {
+          const int vs = vdone % C::VS;
           if (vdone >= C::VS) ok = wait_bar(bar(C::B_VEMPTY + vs), ((vdone / C::VS) & 1) ^ 1, abort_flag, limit, true);
           if (!ok) break;
           ptx::mbar_arrive_expect_tx(bar(C::B_VFULL + vs), C::KTILE);
@@ -650,11 +669,7 @@ __global__ void __launch_bounds__(kThreads256, 1)
                              j * kBN256, it.n);
           ++vdone;
         }
-        ++items;
       }
-      if (items > 0) wait_bar(bar(C::B_Q), (items - 1) & 1, abort_flag, limit, false);
-      for (int x = kdone - C::KS < 0 ? 0 : kdone - C::KS; x < kdone; ++x)
-        wait_bar(bar(C::B_KFULL + x % C::KS), (x / C::KS) & 1, abort_flag, limit, false);
       for (int x = vdone - C::VS < 0 ? 0 : vdone - C::VS; x < vdone; ++x)
         wait_bar(bar(C::B_VFULL + x % C::VS), (x / C::VS) & 1, abort_flag, limit, false);
     }
