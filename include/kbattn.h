@@ -123,13 +123,15 @@ typedef struct {
  *   o       : device pointer, [B, H, S, d] of `dtype`, written in full
  *             (bf16/f16 outputs are rounded to nearest even from fp32)
  *   B, H, S : >= 1; B*H*S*d must fit in int64 and B*H in int32
- *   d       : head dimension, one of 32, 64, 128 (others -> UNSUPPORTED)
+ *   d       : head dimension: 32, 64 or 128, and 256 for KB_TC (others -> UNSUPPORTED)
  *   causal  : 0 or 1
  *   scale   : finite and > 0 (callers normally pass 1/sqrt(d))
  *   dtype   : kb_dtype of q, k, v and o
  *   variant : kb_variant; see the support matrix above
  *   stream  : cudaStream_t or NULL
- * KB_TC supports d = 64 and 128 (d = 32 -> UNSUPPORTED).
+ * KB_TC supports d = 32 (run by the d = 64 kernel on tiles whose features
+ * 32-63 are zero-filled by TMA), 64, 128 and 256 (one 128-row query tile per
+ * CTA); KB_NAIVE, KB_FUSED and KB_FLASH support d = 32, 64 and 128.
  * KB_NAIVE needs N*S*S*4 bytes of workspace: this call takes it from a
  * per-device cache that it grows with cudaMalloc, synchronising the device
  * first when it replaces a smaller buffer (so it may allocate and block);
