@@ -168,8 +168,10 @@ struct Schedule {
 template <int D, bool F16>
 __global__ void __launch_bounds__(kThreadsTC, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                   const __grid_constant__ CUtensorMap tmv, uint8_t* __restrict__ out, float* __restrict__ lse, int N,
-                   int S, int causal, float scale_log2, unsigned long long limit) {
+                   const __grid_constant__ CUtensorMap tmv, uint8_t* __restrict__ out, float* __restrict__ lse,
+                   int dout, int N, int S, int causal, float scale_log2, unsigned long long limit) {
+  // dout: output columns per row (D, or 32 when a d = 32 problem runs on the 64-wide kernel
+  // with its tiles zero-filled by TMA past column 32)
   using C = TcCfg<D>;
   constexpr uint32_t kAB = F16 ? 0u : 1u;
   constexpr uint32_t IDESC_QK = ptx::f16_idesc(kBM, kBN, kAB, 0);
@@ -459,7 +461,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         const float inv = 1.0f / l_run;
         // natural log of sum_j exp(score): the scores sum to 2^m_run * l_run in base 2
         if (lse != nullptr && row < S) lse[(size_t)it.n * S + row] = (m_run + log2f(l_run)) * 0.6931471805599453f;
-        uint8_t* orow = out + ((size_t)it.n * S + row) * (size_t)D * 2;
+        uint8_t* orow = out + ((size_t)it.n * S + row) * (size_t)dout * 2;
         uint32_t u[32];
 #pragma unroll 1
         for (int cb = 0; cb < D / 32; ++cb) {
@@ -470,7 +472,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar(C::B_OFREE + g));
           }
-          if (row < S) {
+          if (row < S && cb * 32 < dout) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               uint4 w;
@@ -926,15 +928,19 @@ bool make_map(CUtensorMap* m, const void* ptr, int64_t N, int S, int d, bool f16
   return r == CUDA_SUCCESS;
 }
 
+// d = 32 runs on the 64-wide kernel: the tensor maps describe the real
+// 32-feature rows, TMA fills features 32-63 of every box with zeros (they add
+// nothing to Q K^T and give O columns that are never stored).
 template <int D, bool F16>
 cudaError_t tc_launch(const AttnProblem& p, cudaStream_t st) {
   using C = TcCfg<D>;
   // per-device attribute, so it is set on every launch
   cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
+  const int dreal = p.d;  // D, or 32 with D = 64
   CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, p.q, p.N, p.S, D, F16) || !make_map(&mk, p.k, p.N, p.S, D, F16) ||
-      !make_map(&mv, p.v, p.N, p.S, D, F16))
+  if (!make_map(&mq, p.q, p.N, p.S, dreal, F16) || !make_map(&mk, p.k, p.N, p.S, dreal, F16) ||
+      !make_map(&mv, p.v, p.N, p.S, dreal, F16))
     return cudaErrorInvalidValue;
   int dev = 0, sms = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
@@ -942,8 +948,8 @@ cudaError_t tc_launch(const AttnProblem& p, cudaStream_t st) {
   const int64_t items = (int64_t)((p.S + kPairRows - 1) / kPairRows) * p.N;
   const int64_t grid = items < sms ? items : sms;  // persistent: at most one CTA per SM
   attn_tc_kernel<D, F16><<<(unsigned)grid, kThreadsTC, C::SMEM, st>>>(
-      mq, mk, mv, static_cast<uint8_t*>(p.o), p.lse, (int)p.N, p.S, p.causal, p.scale * 1.4426950408889634f,
-      kDefaultWaitLimitNs);
+      mq, mk, mv, static_cast<uint8_t*>(p.o), p.lse, dreal, (int)p.N, p.S, p.causal,
+      p.scale * 1.4426950408889634f, kDefaultWaitLimitNs);
   return cudaGetLastError();
 }
 
@@ -971,20 +977,20 @@ cudaError_t tc256_launch(const AttnProblem& p, cudaStream_t st) {
 
 int tc_check(int S, int d, int dtype) {
   (void)S;
-  if (d != 64 && d != 128 && d != 256) return KB_ERR_UNSUPPORTED;
+  if (d != 32 && d != 64 && d != 128 && d != 256) return KB_ERR_UNSUPPORTED;
   if (dtype != KB_BF16 && dtype != KB_F16) return KB_ERR_UNSUPPORTED;
   int dev = 0, optin = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KB_ERR_NO_DEVICE;
   if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
     return KB_ERR_CUDA;
-  const int need = d == 256 ? Tc256::SMEM : (d == 128 ? TcCfg<128>::SMEM : TcCfg<64>::SMEM);
+  const int need = d == 256 ? Tc256::SMEM : (d == 128 ? TcCfg<128>::SMEM : TcCfg<64>::SMEM);  // d = 32: the 64 kernel
   return need <= optin ? KB_OK : KB_ERR_UNSUPPORTED;
 }
 
 cudaError_t launch_tc(const AttnProblem& p, cudaStream_t st) {
   const bool f16 = p.dtype == KB_F16;
   if (p.d == 128) return f16 ? tc_launch<128, true>(p, st) : tc_launch<128, false>(p, st);
-  if (p.d == 64) return f16 ? tc_launch<64, true>(p, st) : tc_launch<64, false>(p, st);
+  if (p.d == 64 || p.d == 32) return f16 ? tc_launch<64, true>(p, st) : tc_launch<64, false>(p, st);
   if (p.d == 256) return f16 ? tc256_launch<true>(p, st) : tc256_launch<false>(p, st);
   return cudaErrorInvalidValue;
 }

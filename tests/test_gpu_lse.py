@@ -28,6 +28,7 @@ CASES = [  # (B, H, S, d, causal, dtype, variant, tol)
     (1, 2, 130, 64, True, "f32", Variant.FLASH, 1e-4), (2, 2, 64, 32, False, "f32", Variant.FLASH, 1e-4),
     (1, 1, 1, 128, True, "bf16", Variant.TC, 1e-3),
     (1, 2, 200, 256, True, "bf16", Variant.TC, 1e-3), (1, 1, 130, 256, False, "f16", Variant.TC, 1e-3),
+    (1, 2, 257, 32, True, "bf16", Variant.TC, 1e-3),
 ]
 
 

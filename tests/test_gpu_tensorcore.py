@@ -37,6 +37,8 @@ SMALL = [  # (B, H, S, d, causal): one tile, several tiles, ragged tails, S = 1
     (1, 1, 128, 128, False), (1, 1, 128, 128, True), (1, 1, 128, 64, False), (1, 2, 256, 128, True),
     (1, 2, 256, 64, True), (2, 1, 300, 128, False), (1, 1, 1, 128, True), (1, 1, 1, 64, False),
     (1, 2, 77, 64, False), (1, 1, 513, 64, True), (1, 3, 640, 128, True), (2, 2, 383, 128, False),
+    # d = 32: the d = 64 kernel on tiles zero-filled past feature 32
+    (1, 1, 1, 32, True), (1, 1, 64, 32, False), (1, 2, 300, 32, True), (2, 1, 129, 32, False),
     # d = 256: one query tile per CTA, 64-key tiles, two score buffers
     (1, 1, 1, 256, True), (1, 1, 64, 256, False), (1, 2, 65, 256, True), (1, 1, 128, 256, True),
     (2, 1, 200, 256, False), (1, 2, 300, 256, True), (1, 1, 513, 256, True), (1, 1, 1024, 256, False),
@@ -118,6 +120,6 @@ def test_repeat_calls_are_deterministic(d):
 
 
 def test_tc_rejects_unsupported_head_dim():
-    st = kbattn.kb_attn_fwd_ptr(1 << 20, 1 << 20, 1 << 20, 1 << 20, 1, 1, 128, 32, False, 0.17,
+    st = kbattn.kb_attn_fwd_ptr(1 << 20, 1 << 20, 1 << 20, 1 << 20, 1, 1, 128, 96, False, 0.17,
                                 kbattn.DType.BF16, Variant.TC, 0)
     assert st == kbattn.Status.UNSUPPORTED
