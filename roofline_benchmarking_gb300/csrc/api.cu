@@ -46,6 +46,9 @@ int validate(const void* q, const void* k, const void* v, const void* o, int B, 
   if (dtype == KB_F32 && var == KB_TC) return KB_ERR_UNSUPPORTED;
   if ((dtype == KB_BF16 || dtype == KB_F16) && var != KB_TC) return KB_ERR_UNSUPPORTED;
   if (d == 256 && var != KB_TC) return KB_ERR_UNSUPPORTED;  // d = 256: tensor-core path only
+  // the tensor-core kernels index their work items (256-row pairs, 128-row tiles at d = 256) in 32 bits
+  if (var == KB_TC && N * ((S + (d == 256 ? 127 : 255)) / (d == 256 ? 128 : 256)) > std::numeric_limits<int32_t>::max())
+    return KB_ERR_UNSUPPORTED;
   if (var == KB_FIXEDPOINT) {
     // keeps every fixed-point intermediate inside 64 bits
     if (S > 65536 || !q15_scale_ok(scale)) return KB_ERR_INVALID_ARG;

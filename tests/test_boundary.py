@@ -85,6 +85,8 @@ def attn(q=FAKE, k=FAKE, v=FAKE, o=FAKE, B=1, H=1, S=64, d=64, causal=0, scale=0
     (dict(d=48), Status.UNSUPPORTED),
     (dict(d=256), Status.UNSUPPORTED),                                  # fp32 at d = 256: tensor cores only
     (dict(d=512, dtype=DType.BF16, variant=Variant.TC), Status.UNSUPPORTED),
+    (dict(B=1 << 15, H=1 << 15, S=1 << 11, d=32, dtype=DType.BF16, variant=Variant.TC),
+     Status.UNSUPPORTED),  # 2^30 heads x 8 pairs: work items overflow int32
     (dict(dtype=DType.F32, variant=Variant.TC), Status.UNSUPPORTED),
     (dict(dtype=DType.BF16, variant=Variant.FLASH), Status.UNSUPPORTED),
     (dict(dtype=DType.F16, variant=Variant.NAIVE), Status.UNSUPPORTED),
