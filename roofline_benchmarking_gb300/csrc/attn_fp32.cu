@@ -39,8 +39,9 @@ __device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast
 // Consecutive threads take consecutive rows so that the shared stores do not
 // conflict; the strided global reads are served from L1 across the k loop.
 template <int D>
-__device__ __forceinline__ void load_transposed(float* dst, const float* src, int r0, int S, float mul) {
-  for (int f = threadIdx.x; f < kBR * (D / 4); f += kThreads) {
+__device__ __forceinline__ void load_transposed(float* dst, const float* src, int r0, int S, float mul,
+                                                int tid, int nthreads) {
+  for (int f = tid; f < kBR * (D / 4); f += nthreads) {
     const int r = f % kBR, k4 = f / kBR;
     float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
     if (r0 + r < S) x = ld4(src + (int64_t)(r0 + r) * D + 4 * k4);
@@ -51,10 +52,20 @@ __device__ __forceinline__ void load_transposed(float* dst, const float* src, in
   }
 }
 
+template <int D>
+__device__ __forceinline__ void load_transposed(float* dst, const float* src, int r0, int S, float mul) {
+  load_transposed<D>(dst, src, r0, S, mul, threadIdx.x, kThreads);
+}
+
 // Loads rows [r0, r0+64) x D of a [S, D] matrix into dst[r * D + k] (row-major).
 template <int D>
-__device__ __forceinline__ void load_rows(float* dst, const float* src, int r0, int S) {
-  for (int f = threadIdx.x; f < kBC * (D / 4); f += kThreads) {
+__device__ __forceinline__ void load_rows(float* dst, const float* src, int r0, int S, int tid = 0,
+                                          int nthreads = 0) {
+  if (nthreads == 0) {
+    tid = threadIdx.x;
+    nthreads = kThreads;
+  }
+  for (int f = tid; f < kBC * (D / 4); f += nthreads) {
     const int r = f / (D / 4), k4 = f % (D / 4);
     float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
     if (r0 + r < S) x = ld4(src + (int64_t)(r0 + r) * D + 4 * k4);
@@ -112,18 +123,30 @@ __device__ __forceinline__ void qk_tile(float (&s)[4][4], const float* Qs, const
 
 // ---------------------------------------------------------------------------
 // flash: one block per (head, 64-row query tile); grid.x = tiles * N with the
-// heaviest causal tiles scheduled first.
+// heaviest causal tiles scheduled first. The block's 512 threads form two
+// groups of 256 (each synchronised by its own named barrier) that take the
+// even and the odd key tiles with their own K/V/P buffers and their own
+// running max, sum and O, and are merged at the end -- twice the warps per
+// query tile, so that small grids still hide the latency of shared memory.
 // ---------------------------------------------------------------------------
+constexpr int kFlashThreads = 2 * kThreads;
+
+__device__ __forceinline__ void group_bar(int grp) {
+  asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "r"(kThreads) : "memory");
+}
+
 template <int D>
-__global__ void __launch_bounds__(kThreads) flash_f32_kernel(const float* __restrict__ Q,
-                                                             const float* __restrict__ K,
-                                                             const float* __restrict__ V,
-                                                             float* __restrict__ O, float* __restrict__ lse,
-                                                             int64_t N, int S, int causal, float scale_log2) {
+__global__ void __launch_bounds__(kFlashThreads, 1) flash_f32_kernel(const float* __restrict__ Q,
+                                                                  const float* __restrict__ K,
+                                                                  const float* __restrict__ V,
+                                                                  float* __restrict__ O, float* __restrict__ lse,
+                                                                  int64_t N, int S, int causal, float scale_log2) {
   using C = Cols<D>;
+  constexpr int GROUP = D * kLD + kBC * D + kBC * kLD;  // floats of one group's K, V and P buffers
   extern __shared__ float4 smem4[];
-  float* Qs = reinterpret_cast<float*>(smem4);  // [D][kLD]
-  float* Ks = Qs + D * kLD;                      // [D][kLD]
+  float* Qs = reinterpret_cast<float*>(smem4);  // [D][kLD], both groups
+  const int grp = threadIdx.x / kThreads, ltid = threadIdx.x % kThreads;
+  float* Ks = Qs + D * kLD + grp * GROUP;        // [D][kLD]
   float* Vs = Ks + D * kLD;                      // [kBC][D]
   float* Ps = Vs + kBC * D;                      // [kBC][kLD]
 
@@ -131,12 +154,13 @@ __global__ void __launch_bounds__(kThreads) flash_f32_kernel(const float* __rest
   const int64_t n = blockIdx.x % N;
   const int qt = ntiles - 1 - (int)(blockIdx.x / N);
   const int q0 = qt * kBR;
-  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  const int tx = ltid & 15, ty = ltid >> 4;
   const float* Qh = Q + n * S * D;
   const float* Kh = K + n * S * D;
   const float* Vh = V + n * S * D;
 
-  load_transposed<D>(Qs, Qh, q0, S, scale_log2);
+  load_transposed<D>(Qs, Qh, q0, S, scale_log2, threadIdx.x, kFlashThreads);
+  __syncthreads();
 
   float m[4], l[4], acc[4][D / 16];
 #pragma unroll
@@ -148,12 +172,12 @@ __global__ void __launch_bounds__(kThreads) flash_f32_kernel(const float* __rest
   }
 
   const int kt_last = causal ? qt : ntiles - 1;
-  for (int kt = 0; kt <= kt_last; ++kt) {
+  for (int kt = grp; kt <= kt_last; kt += 2) {
     const int k0 = kt * kBC;
-    __syncthreads();  // previous tile's Ks, Vs, Ps are no longer read
-    load_transposed<D>(Ks, Kh, k0, S, 1.0f);
-    load_rows<D>(Vs, Vh, k0, S);
-    __syncthreads();
+    group_bar(grp);  // the group's previous Ks, Vs, Ps are no longer read
+    load_transposed<D>(Ks, Kh, k0, S, 1.0f, ltid, kThreads);
+    load_rows<D>(Vs, Vh, k0, S, ltid, kThreads);
+    group_bar(grp);
 
     float s[4][4];
     qk_tile<D>(s, Qs, Ks, ty, tx);
@@ -188,22 +212,47 @@ __global__ void __launch_bounds__(kThreads) flash_f32_kernel(const float* __rest
 #pragma unroll
     for (int b = 0; b < 4; ++b)
       *reinterpret_cast<float4*>(Ps + (tx * 4 + b) * kLD + ty * 4) = make_float4(s[0][b], s[1][b], s[2][b], s[3][b]);
-    __syncthreads();
+    group_bar(grp);
     pv_accumulate<D>(acc, Ps, Vs, ty, tx, kBC);
   }
 
+  // merge: group 1 publishes its state (field-major, one column per thread) in
+  // its own buffers, group 0 combines the two online softmaxes and writes O
+  constexpr int F = 8 + 4 * (D / 16);  // m[4], l[4], acc[4][D/16]
+  float* X = Qs + D * kLD + GROUP;     // group 1's buffers
+  __syncthreads();
+  if (grp == 1) {
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      X[a * kThreads + ltid] = m[a];
+      X[(4 + a) * kThreads + ltid] = l[a];
+#pragma unroll
+      for (int c = 0; c < D / 16; ++c) X[(8 + a * (D / 16) + c) * kThreads + ltid] = acc[a][c];
+    }
+  }
+  __syncthreads();
+  if (grp == 1) return;
+  static_assert(F * kThreads <= GROUP, "merge state fits in one group's buffers");
 #pragma unroll
   for (int a = 0; a < 4; ++a) {
     const int row = q0 + ty * 4 + a;
+    const float m1 = X[a * kThreads + ltid], l1 = X[(4 + a) * kThreads + ltid];
+    const float mm = fmaxf(m[a], m1);  // group 0 always sees key 0, so m[a] and mm are finite
+    const float s0 = exp2f(m[a] - mm);
+    const float s1 = m1 == -INFINITY ? 0.f : exp2f(m1 - mm);
+    const float lt = l[a] * s0 + l1 * s1;
     if (row >= S) continue;
-    const float inv = 1.0f / l[a];
-    // natural log of sum_j exp(score): the scores sum to 2^m * l in base 2
-    if (lse != nullptr && tx == 0) lse[n * S + row] = (m[a] + log2f(l[a])) * 0.6931471805599453f;
+    const float inv = 1.0f / lt;
+    // natural log of sum_j exp(score): the scores sum to 2^mm * lt in base 2
+    if (lse != nullptr && tx == 0) lse[n * S + row] = (mm + log2f(lt)) * 0.6931471805599453f;
     float* orow = O + (n * S + row) * D;
 #pragma unroll
     for (int g = 0; g < C::G; ++g)
 #pragma unroll
-      for (int e = 0; e < C::W; ++e) orow[g * 16 * C::W + tx * C::W + e] = acc[a][g * C::W + e] * inv;
+      for (int e = 0; e < C::W; ++e) {
+        const float a1 = X[(8 + a * (D / 16) + g * C::W + e) * kThreads + ltid];
+        orow[g * 16 * C::W + tx * C::W + e] = (acc[a][g * C::W + e] * s0 + a1 * s1) * inv;
+      }
   }
 }
 
@@ -470,7 +519,7 @@ __global__ void __launch_bounds__(kFusedThreads) fused_row_f32_kernel(const floa
   }
 }
 
-size_t flash_smem(int d) { return sizeof(float) * (size_t)(2 * d * kLD + kBC * d + kBC * kLD); }
+size_t flash_smem(int d) { return sizeof(float) * (size_t)(d * kLD + 2 * (d * kLD + kBC * d + kBC * kLD)); }
 size_t naive_scores_smem(int d) { return sizeof(float) * (size_t)(2 * d * kLD); }
 size_t naive_pv_smem(int d) { return sizeof(float) * (size_t)(kBC * kLD + kBC * d); }
 size_t fused_smem(int S, int d, int rows = 1) {
@@ -489,7 +538,7 @@ cudaError_t flash_launch(const AttnProblem& p, cudaStream_t st) {
   cudaError_t e = set_smem(flash_f32_kernel<D>, smem);
   if (e != cudaSuccess) return e;
   const int64_t tiles = (p.S + kBR - 1) / kBR;
-  flash_f32_kernel<D><<<(unsigned)(tiles * p.N), kThreads, smem, st>>>(
+  flash_f32_kernel<D><<<(unsigned)(tiles * p.N), kFlashThreads, smem, st>>>(
       (const float*)p.q, (const float*)p.k, (const float*)p.v, (float*)p.o, p.lse, p.N, p.S, p.causal,
       p.scale * kLog2e);
   return cudaGetLastError();
