@@ -318,20 +318,25 @@ __global__ void __launch_bounds__(kThreads) naive_softmax_kernel(float* __restri
   for (int j = lane; j < len; j += 32) row[j] = exp2f(row[j] * kLog2e - mw) * inv;
 }
 
-// naive pass 3: O = P V as a tiled GEMM over the visible key tiles.
+// naive pass 3: O = P V as a tiled GEMM over the visible key tiles. As in the
+// flash kernel, two groups of 256 threads take the even and the odd key tiles
+// with their own P and V buffers; group 0 adds group 1's partial sums.
 template <int D>
-__global__ void __launch_bounds__(kThreads) naive_pv_kernel(const float* __restrict__ Sc,
-                                                            const float* __restrict__ V, float* __restrict__ O,
-                                                            int64_t N, int S, int causal) {
+__global__ void __launch_bounds__(kFlashThreads, 1) naive_pv_kernel(const float* __restrict__ Sc,
+                                                                    const float* __restrict__ V,
+                                                                    float* __restrict__ O, int64_t N, int S,
+                                                                    int causal) {
   using C = Cols<D>;
+  constexpr int GROUP = kBC * kLD + kBC * D;  // floats of one group's P and V buffers
   extern __shared__ float4 smem4[];
-  float* Ps = reinterpret_cast<float*>(smem4);  // [kBC][kLD] (key-major)
-  float* Vs = Ps + kBC * kLD;                    // [kBC][D]
+  const int grp = threadIdx.x / kThreads, ltid = threadIdx.x % kThreads;
+  float* Ps = reinterpret_cast<float*>(smem4) + grp * GROUP;  // [kBC][kLD] (key-major)
+  float* Vs = Ps + kBC * kLD;                                  // [kBC][D]
   const int ntiles = (S + kBR - 1) / kBR;
   const int64_t n = blockIdx.x % N;
   const int qt = ntiles - 1 - (int)(blockIdx.x / N);
   const int q0 = qt * kBR;
-  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  const int tx = ltid & 15, ty = ltid >> 4;
   const float* Sh = Sc + n * (int64_t)S * S;
   float acc[4][D / 16];
 #pragma unroll
@@ -340,21 +345,32 @@ __global__ void __launch_bounds__(kThreads) naive_pv_kernel(const float* __restr
     for (int c = 0; c < D / 16; ++c) acc[a][c] = 0.f;
 
   const int kt_last = causal ? qt : ntiles - 1;
-  for (int kt = 0; kt <= kt_last; ++kt) {
+  for (int kt = grp; kt <= kt_last; kt += 2) {
     const int k0 = kt * kBC;
-    __syncthreads();
+    group_bar(grp);
     // P tile, transposed to Ps[key][row]; masked and out-of-range entries are 0
-    for (int f = tid; f < kBR * kBC; f += kThreads) {
+    for (int f = ltid; f < kBR * kBC; f += kThreads) {
       const int key = f % kBC, r = f / kBC;
       const int row = q0 + r, col = k0 + key;
       float p = 0.f;
       if (row < S && col < S && !(causal && col > row)) p = Sh[(int64_t)row * S + col];
       Ps[key * kLD + r] = p;
     }
-    load_rows<D>(Vs, V + n * S * D, k0, S);
-    __syncthreads();
+    load_rows<D>(Vs, V + n * S * D, k0, S, ltid, kThreads);
+    group_bar(grp);
     pv_accumulate<D>(acc, Ps, Vs, ty, tx, kBC);
   }
+  float* X = reinterpret_cast<float*>(smem4) + GROUP;  // group 1's buffers hold its partial sums
+  static_assert(4 * (D / 16) * kThreads <= GROUP, "partial sums fit in one group's buffers");
+  __syncthreads();
+  if (grp == 1) {
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int c = 0; c < D / 16; ++c) X[(a * (D / 16) + c) * kThreads + ltid] = acc[a][c];
+  }
+  __syncthreads();
+  if (grp == 1) return;
 #pragma unroll
   for (int a = 0; a < 4; ++a) {
     const int row = q0 + ty * 4 + a;
@@ -363,7 +379,9 @@ __global__ void __launch_bounds__(kThreads) naive_pv_kernel(const float* __restr
 #pragma unroll
     for (int g = 0; g < C::G; ++g)
 #pragma unroll
-      for (int e = 0; e < C::W; ++e) orow[g * 16 * C::W + tx * C::W + e] = acc[a][g * C::W + e];
+      for (int e = 0; e < C::W; ++e)
+        orow[g * 16 * C::W + tx * C::W + e] =
+            acc[a][g * C::W + e] + X[(a * (D / 16) + g * C::W + e) * kThreads + ltid];
   }
 }
 
@@ -521,7 +539,7 @@ __global__ void __launch_bounds__(kFusedThreads) fused_row_f32_kernel(const floa
 
 size_t flash_smem(int d) { return sizeof(float) * (size_t)(d * kLD + 2 * (d * kLD + kBC * d + kBC * kLD)); }
 size_t naive_scores_smem(int d) { return sizeof(float) * (size_t)(2 * d * kLD); }
-size_t naive_pv_smem(int d) { return sizeof(float) * (size_t)(kBC * kLD + kBC * d); }
+size_t naive_pv_smem(int d) { return sizeof(float) * (size_t)(2 * (kBC * kLD + kBC * d)); }
 size_t fused_smem(int S, int d, int rows = 1) {
   return sizeof(float) * (size_t)(kFusedKeys * (d + 16) + rows * d + kFusedWarps * rows + rows * kFusedThreads +
                                   (size_t)rows * S);
@@ -557,7 +575,7 @@ cudaError_t naive_launch(const AttnProblem& p, float* scores, cudaStream_t st) {
   naive_softmax_kernel<<<(unsigned)((rows + kThreads / 32 - 1) / (kThreads / 32)), kThreads, 0, st>>>(
       scores, rows, p.S, p.causal);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  naive_pv_kernel<D><<<(unsigned)(tiles * p.N), kThreads, naive_pv_smem(D), st>>>(
+  naive_pv_kernel<D><<<(unsigned)(tiles * p.N), kFlashThreads, naive_pv_smem(D), st>>>(
       scores, (const float*)p.v, (float*)p.o, p.N, p.S, p.causal);
   return cudaGetLastError();
 }
