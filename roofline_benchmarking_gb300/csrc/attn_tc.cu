@@ -14,7 +14,8 @@
 //    its first P V waits only for the current epilogue to have read O;
 //  * warp 8 (one lane) stages both Q tiles and rings of K and V tiles with TMA
 //    (128-byte swizzle, 3-D tensor maps [N, S, d], rows past S zero-filled);
-//  * warp 9 (one lane) issues the tcgen05 MMAs: S = Q K^T from shared memory
+//  * warp 9 issues the tcgen05 MMAs, the whole warp running the issue loop and
+//    one elected lane issuing each instruction: S = Q K^T from shared memory
 //    into a 128x128 fp32 TMEM tile per query tile, and O += P V with P read
 //    from TMEM and V from shared memory into a 128 x d fp32 TMEM accumulator
 //    per query tile; completion is signalled by tcgen05.commit on mbarriers;
@@ -54,12 +55,12 @@ constexpr int kPairRows = 2 * kBM;
 // Three warpgroups: 0 and 1 run the softmax of tiles A and B; in the third,
 // warp 8 drives TMA and warp 9 issues MMAs (warps 10 and 11 only hand their
 // registers over). Launch budget 384 x 168 = 64512 registers, rebalanced as
-// 2 x 128 x 208 + 128 x 88 = 64512.
+// 2 x 128 x 200 + 128 x 104 = 64512.
 constexpr int kThreadsTC = 384;
 constexpr int kWarpTMA = 8;
 constexpr int kWarpMMA = 9;
-constexpr int kRegsSoftmax = 208;
-constexpr int kRegsControl = 88;
+constexpr int kRegsSoftmax = 200;
+constexpr int kRegsControl = 104;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColBlock = 16384;  // one 128-row x 128-byte swizzled block
 constexpr unsigned long long kDefaultWaitLimitNs = 1000000000ull;
@@ -120,6 +121,13 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           unsigned long long limit) {
   const bool ok = wait_bar(bar, parity, abort_flag, limit, true);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Warp-wide wait that can ignore the abort flag (used to drain copies and MMAs in flight).
+__device__ __forceinline__ bool warp_wait_all(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                              unsigned long long limit, bool honor_abort) {
+  const bool ok = wait_bar(bar, parity, abort_flag, limit, honor_abort);
   return __all_sync(0xffffffffu, ok);
 }
 
@@ -266,7 +274,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       __syncwarp();
     } else if (warp == kWarpMMA) {
       // ------------------------------------------------------------ MMA issuer
-      if (lane == 0) {
+      // The whole warp runs the issue loop (descriptors and waits are warp-uniform);
+      // one elected lane issues each MMA and commit.
+      {
         // S_g = Q_g K_j^T (K-major operands, both from shared memory)
         auto issue_s = [&](int g, int ks) {
           // descriptors of k-step 0; a k-step moves the start address field (bytes >> 4)
@@ -275,16 +285,16 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = ((kk >> 2) * kColBlock + (kk & 3) * 32) >> 4;
-            ptx::mma_f16_ss(tmem + C::tm_s(g), a0 + off, b0 + off, IDESC_QK, kk > 0 ? 1u : 0u);
+            ptx::mma_f16_ss_elect(tmem + C::tm_s(g), a0 + off, b0 + off, IDESC_QK, kk > 0 ? 1u : 0u);
           }
-          ptx::mma_commit(bar(C::B_SFULL + g));
+          ptx::mma_commit_elect(bar(C::B_SFULL + g));
         };
         // O_g += P_g V_j (P from TMEM, V MN-major from shared memory)
         auto issue_pv = [&](int g, int vs, bool first) {
           const uint64_t b0 = ptx::sw128_desc(base + C::OFF_V + vs * C::TILE, kColBlock, 1024);
 #pragma unroll
           for (int kk = 0; kk < kBN / 16; ++kk)  // a k-step is 16 keys = 16 rows of 128 bytes
-            ptx::mma_f16_ts(tmem + C::tm_o(g), tmem + C::tm_s(g) + kk * 8, b0 + ((kk * 16 * 128) >> 4), IDESC_PV,
+            ptx::mma_f16_ts_elect(tmem + C::tm_o(g), tmem + C::tm_s(g) + kk * 8, b0 + ((kk * 16 * 128) >> 4), IDESC_PV,
                             (!first || kk > 0) ? 1u : 0u);
         };
         bool ok = true;
@@ -293,63 +303,62 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         Item it;
         for (int item = 0; ok && sched.get(item, it); ++item) {
           const int nA = it.nA, nB = it.nB;
-          ok = wait_bar(bar(C::B_Q), item & 1, abort_flag, limit, true);
+          ok = warp_wait(bar(C::B_Q), item & 1, abort_flag, limit);
           const int ks0 = kbase % C::KS;
-          if (ok) ok = wait_bar(bar(C::B_KFULL + ks0), (kbase / C::KS) & 1, abort_flag, limit, true);
+          if (ok) ok = warp_wait(bar(C::B_KFULL + ks0), (kbase / C::KS) & 1, abort_flag, limit);
           if (!ok) break;
           ptx::tc_fence_after();
           issue_s(0, ks0);
           issue_s(1, ks0);
-          ptx::mma_commit(bar(C::B_KEMPTY + ks0));
-          if (nB == 1) ptx::mma_commit(bar(C::B_QFREE));
+          ptx::mma_commit_elect(bar(C::B_KEMPTY + ks0));
+          if (nB == 1) ptx::mma_commit_elect(bar(C::B_QFREE));
           for (int j = 0; j < nB && ok; ++j) {
             const int vp = vbase + j, vs = vp % C::VS;
             const int jn = j + 1, kpn = kbase + jn, ksn = kpn % C::KS;
-            ok = wait_bar(bar(C::B_VFULL + vs), (vp / C::VS) & 1, abort_flag, limit, true);
+            ok = warp_wait(bar(C::B_VFULL + vs), (vp / C::VS) & 1, abort_flag, limit);
             if (ok && j < nA) {  // tile A
-              ok = wait_bar(bar(C::B_PFULL + 0), pa & 1, abort_flag, limit, true);
-              if (ok && j == 0 && item > 0) ok = wait_bar(bar(C::B_OFREE + 0), (item - 1) & 1, abort_flag, limit, true);
+              ok = warp_wait(bar(C::B_PFULL + 0), pa & 1, abort_flag, limit);
+              if (ok && j == 0 && item > 0) ok = warp_wait(bar(C::B_OFREE + 0), (item - 1) & 1, abort_flag, limit);
               if (ok) {
                 ++pa;
                 ptx::tc_fence_after();
                 issue_pv(0, vs, j == 0);
                 if (jn < nA) {
-                  ok = wait_bar(bar(C::B_KFULL + ksn), (kpn / C::KS) & 1, abort_flag, limit, true);
+                  ok = warp_wait(bar(C::B_KFULL + ksn), (kpn / C::KS) & 1, abort_flag, limit);
                   if (ok) {
                     ptx::tc_fence_after();
                     issue_s(0, ksn);
                   }
                 } else {
-                  ptx::mma_commit(bar(C::B_OFINAL + 0));
+                  ptx::mma_commit_elect(bar(C::B_OFINAL + 0));
                 }
               }
             }
-            if (ok) ok = wait_bar(bar(C::B_PFULL + 1), pb & 1, abort_flag, limit, true);
-            if (ok && j == 0 && item > 0) ok = wait_bar(bar(C::B_OFREE + 1), (item - 1) & 1, abort_flag, limit, true);
+            if (ok) ok = warp_wait(bar(C::B_PFULL + 1), pb & 1, abort_flag, limit);
+            if (ok && j == 0 && item > 0) ok = warp_wait(bar(C::B_OFREE + 1), (item - 1) & 1, abort_flag, limit);
             if (!ok) break;
             ++pb;
             ptx::tc_fence_after();
             issue_pv(1, vs, j == 0);  // tile B
-            ptx::mma_commit(bar(C::B_VEMPTY + vs));
+            ptx::mma_commit_elect(bar(C::B_VEMPTY + vs));
             if (jn < nB) {
-              ok = wait_bar(bar(C::B_KFULL + ksn), (kpn / C::KS) & 1, abort_flag, limit, true);
+              ok = warp_wait(bar(C::B_KFULL + ksn), (kpn / C::KS) & 1, abort_flag, limit);
               if (!ok) break;
               ptx::tc_fence_after();
               issue_s(1, ksn);
-              ptx::mma_commit(bar(C::B_KEMPTY + ksn));
-              if (jn == nB - 1) ptx::mma_commit(bar(C::B_QFREE));  // the item's last score MMA
+              ptx::mma_commit_elect(bar(C::B_KEMPTY + ksn));
+              if (jn == nB - 1) ptx::mma_commit_elect(bar(C::B_QFREE));  // the item's last score MMA
             } else {
-              ptx::mma_commit(bar(C::B_OFINAL + 1));
+              ptx::mma_commit_elect(bar(C::B_OFINAL + 1));
             }
           }
           kbase += nB;
           vbase += nB;
         }
         // No MMA may still be running when the tensor memory is released.
-        ptx::mma_commit(bar(C::B_DRAIN));
-        wait_bar(bar(C::B_DRAIN), 0, abort_flag, limit, false);
+        ptx::mma_commit_elect(bar(C::B_DRAIN));
+        warp_wait_all(bar(C::B_DRAIN), 0, abort_flag, limit, false);
       }
-      __syncwarp();
     }
   } else {
     ptx::regs_increase<kRegsSoftmax>();
