@@ -687,7 +687,8 @@ __global__ void __launch_bounds__(kThreads256, 1)
     __syncwarp();
   } else if (warp == kWarpMMA256) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the issue loop; one elected lane issues each MMA and commit.
+    {
       // S(buffer b) = Q K^T: 16 k-steps of 16 features; both operands K-major
       auto issue_s = [&](int b, int ks) {
         const uint64_t a0 = ptx::sw128_desc(base + C::OFF_Q, 16, 1024);
@@ -696,16 +697,16 @@ __global__ void __launch_bounds__(kThreads256, 1)
         for (int kk = 0; kk < C::D / 16; ++kk) {
           const uint32_t offa = ((kk >> 2) * C::QBLK + (kk & 3) * 32) >> 4;
           const uint32_t offb = ((kk >> 2) * C::KBLK + (kk & 3) * 32) >> 4;
-          ptx::mma_f16_ss(tmem + 64u * (uint32_t)b, a0 + offa, b0 + offb, IDESC_QK, kk > 0 ? 1u : 0u);
+          ptx::mma_f16_ss_elect(tmem + 64u * (uint32_t)b, a0 + offa, b0 + offb, IDESC_QK, kk > 0 ? 1u : 0u);
         }
-        ptx::mma_commit(bar(C::B_SFULL + b));
+        ptx::mma_commit_elect(bar(C::B_SFULL + b));
       };
       // O += P(buffer b) V: 4 k-steps of 16 keys; V MN-major, column blocks KBLK apart
       auto issue_pv = [&](int b, int vs, bool first) {
         const uint64_t b0 = ptx::sw128_desc(base + C::OFF_V + vs * C::KTILE, C::KBLK, 1024);
 #pragma unroll
         for (int kk = 0; kk < kBN256 / 16; ++kk)
-          ptx::mma_f16_ts(tmem + C::TM_O, tmem + 64u * (uint32_t)b + kk * 8, b0 + ((kk * 16 * 128) >> 4), IDESC_PV,
+          ptx::mma_f16_ts_elect(tmem + C::TM_O, tmem + 64u * (uint32_t)b + kk * 8, b0 + ((kk * 16 * 128) >> 4), IDESC_PV,
                           (!first || kk > 0) ? 1u : 0u);
       };
       bool ok = true;
@@ -713,49 +714,48 @@ __global__ void __launch_bounds__(kThreads256, 1)
       Item256 it;
       for (int item = 0; ok && sched.get(item, it); ++item) {
         const int nk = it.nk;
-        ok = wait_bar(bar(C::B_Q), item & 1, abort_flag, limit, true);
+        ok = warp_wait(bar(C::B_Q), item & 1, abort_flag, limit);
         // S(0) and S(1)
         for (int j = 0; j < 2 && j < nk && ok; ++j) {
           const int ks = kcons % C::KS;
-          ok = wait_bar(bar(C::B_KFULL + ks), (kcons / C::KS) & 1, abort_flag, limit, true);
+          ok = warp_wait(bar(C::B_KFULL + ks), (kcons / C::KS) & 1, abort_flag, limit);
           if (!ok) break;
           ptx::tc_fence_after();
           issue_s(scnt & 1, ks);
-          ptx::mma_commit(bar(C::B_KEMPTY + ks));
-          if (j == nk - 1) ptx::mma_commit(bar(C::B_QFREE));
+          ptx::mma_commit_elect(bar(C::B_KEMPTY + ks));
+          if (j == nk - 1) ptx::mma_commit_elect(bar(C::B_QFREE));
           ++kcons;
           ++scnt;
         }
         for (int j = 0; j < nk && ok; ++j) {
           const int vs = vcons % C::VS;
-          ok = wait_bar(bar(C::B_VFULL + vs), (vcons / C::VS) & 1, abort_flag, limit, true);
-          if (ok) ok = wait_bar(bar(C::B_PFULL + (pcnt & 1)), (pcnt >> 1) & 1, abort_flag, limit, true);
-          if (ok && j == 0 && item > 0) ok = wait_bar(bar(C::B_OFREE), (item - 1) & 1, abort_flag, limit, true);
+          ok = warp_wait(bar(C::B_VFULL + vs), (vcons / C::VS) & 1, abort_flag, limit);
+          if (ok) ok = warp_wait(bar(C::B_PFULL + (pcnt & 1)), (pcnt >> 1) & 1, abort_flag, limit);
+          if (ok && j == 0 && item > 0) ok = warp_wait(bar(C::B_OFREE), (item - 1) & 1, abort_flag, limit);
           if (!ok) break;
           ptx::tc_fence_after();
           issue_pv(pcnt & 1, vs, j == 0);
-          ptx::mma_commit(bar(C::B_PVDONE));
-          ptx::mma_commit(bar(C::B_VEMPTY + vs));
+          ptx::mma_commit_elect(bar(C::B_PVDONE));
+          ptx::mma_commit_elect(bar(C::B_VEMPTY + vs));
           ++vcons;
           ++pcnt;
           if (j + 2 < nk) {
             const int ks = kcons % C::KS;
-            ok = wait_bar(bar(C::B_KFULL + ks), (kcons / C::KS) & 1, abort_flag, limit, true);
+            ok = warp_wait(bar(C::B_KFULL + ks), (kcons / C::KS) & 1, abort_flag, limit);
             if (!ok) break;
             ptx::tc_fence_after();
             issue_s(scnt & 1, ks);
-            ptx::mma_commit(bar(C::B_KEMPTY + ks));
-            if (j + 2 == nk - 1) ptx::mma_commit(bar(C::B_QFREE));
+            ptx::mma_commit_elect(bar(C::B_KEMPTY + ks));
+            if (j + 2 == nk - 1) ptx::mma_commit_elect(bar(C::B_QFREE));
             ++kcons;
             ++scnt;
           }
         }
-        if (ok) ptx::mma_commit(bar(C::B_OFINAL));
+        if (ok) ptx::mma_commit_elect(bar(C::B_OFINAL));
       }
-      ptx::mma_commit(bar(C::B_DRAIN));
-      wait_bar(bar(C::B_DRAIN), 0, abort_flag, limit, false);
+      ptx::mma_commit_elect(bar(C::B_DRAIN));
+      warp_wait_all(bar(C::B_DRAIN), 0, abort_flag, limit, false);
     }
-    __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax, warps 0-3
     const int r = warp * 32 + lane;
