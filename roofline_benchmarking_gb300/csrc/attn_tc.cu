@@ -471,24 +471,24 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         // natural log of sum_j exp(score): the scores sum to 2^m_run * l_run in base 2
         if (lse != nullptr && row < S) lse[(size_t)it.n * S + row] = (m_run + log2f(l_run)) * 0.6931471805599453f;
         uint8_t* orow = out + ((size_t)it.n * S + row) * (size_t)dout * 2;
-        uint32_t u[32];
-#pragma unroll 1
+        // the whole O row in one round trip to TMEM (the score registers are free by now);
+        // then the accumulator may take the next item while this one is scaled and stored
+        uint32_t u[D / 32][32];
+#pragma unroll
+        for (int cb = 0; cb < D / 32; ++cb) ptx::tmem_ld32(to + cb * 32, u[cb]);
+        ptx::tmem_wait_ld();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(C::B_OFREE + g));
+#pragma unroll
         for (int cb = 0; cb < D / 32; ++cb) {
-          ptx::tmem_ld32(to + cb * 32, u);
-          ptx::tmem_wait_ld();
-          if (cb == D / 32 - 1) {
-            // all of O is in registers: the accumulator may take the next item
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(bar(C::B_OFREE + g));
-          }
           if (row < S && cb * 32 < dout) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               uint4 w;
-              w.x = pack2<F16>(__uint_as_float(u[q * 8 + 0]) * inv, __uint_as_float(u[q * 8 + 1]) * inv);
-              w.y = pack2<F16>(__uint_as_float(u[q * 8 + 2]) * inv, __uint_as_float(u[q * 8 + 3]) * inv);
-              w.z = pack2<F16>(__uint_as_float(u[q * 8 + 4]) * inv, __uint_as_float(u[q * 8 + 5]) * inv);
-              w.w = pack2<F16>(__uint_as_float(u[q * 8 + 6]) * inv, __uint_as_float(u[q * 8 + 7]) * inv);
+              w.x = pack2<F16>(__uint_as_float(u[cb][q * 8 + 0]) * inv, __uint_as_float(u[cb][q * 8 + 1]) * inv);
+              w.y = pack2<F16>(__uint_as_float(u[cb][q * 8 + 2]) * inv, __uint_as_float(u[cb][q * 8 + 3]) * inv);
+              w.z = pack2<F16>(__uint_as_float(u[cb][q * 8 + 4]) * inv, __uint_as_float(u[cb][q * 8 + 5]) * inv);
+              w.w = pack2<F16>(__uint_as_float(u[cb][q * 8 + 6]) * inv, __uint_as_float(u[cb][q * 8 + 7]) * inv);
               *reinterpret_cast<uint4*>(orow + cb * 64 + q * 16) = w;
             }
           }
