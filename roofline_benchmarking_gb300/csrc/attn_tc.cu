@@ -37,7 +37,16 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <cmath>
+#include <functional>
+#include <map>
+#include <memory>
 #include <mutex>
+#include <queue>
+#include <tuple>
+#include <utility>
+#include <vector>
 
 #include "internal.h"
 #include "tc_ptx.cuh"
@@ -142,7 +151,23 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   }
 }
 
-// The persistent schedule. Work item i (0 <= i < N * pairs) is query rows
+// Per-CTA work lists built on the host (passed by value as a kernel parameter):
+// CTA c runs units item[start[c]], item[start[c] + 1], ... < start[c + 1], an
+// entry holding head << 16 | unit. The lists come from list scheduling over
+// the heads in groups whose K and V fit in L2 (each group's units heaviest
+// first): the CTAs work on one group's heads at a time, so every K/V tile is
+// fetched from DRAM about once and shared in L2 by all the units of its head,
+// while the per-CTA totals stay within a few per cent of each other. count = 0
+// (more units than the table holds) selects the snake order below.
+constexpr int kSchedMaxGrid = 256;
+constexpr int kSchedMaxItems = 4096;
+struct SchedTable {
+  int count;
+  unsigned short start[kSchedMaxGrid + 1];
+  unsigned int item[kSchedMaxItems];
+};
+
+// Snake order (the fallback). Work item i (0 <= i < N * pairs) is query rows
 // [256 t, 256 t + 256) of head n with t = pairs - 1 - i / N, so the heaviest
 // causal items come first. CTA c takes, in round r, item r G + c when r is
 // even and item r G + G - 1 - c when r is odd: a snake over the list sorted
@@ -153,7 +178,9 @@ struct Item {
 
 struct Schedule {
   int N, S, causal, pairs, nkv, total;
-  __device__ Schedule(int N_, int S_, int causal_) : N(N_), S(S_), causal(causal_) {
+  const SchedTable* tab;
+  __device__ Schedule(int N_, int S_, int causal_, const SchedTable* tab_)
+      : N(N_), S(S_), causal(causal_), tab(tab_) {
     pairs = (S + kPairRows - 1) / kPairRows;
     nkv = (S + kBN - 1) / kBN;
     total = N * pairs;
@@ -161,11 +188,20 @@ struct Schedule {
   // Item of this CTA's round `round`; false once the list is exhausted (the
   // index grows with the round, so every later round is exhausted too).
   __device__ bool get(int round, Item& it) const {
-    const int G = (int)gridDim.x, c = (int)blockIdx.x;
-    const int i = round * G + ((round & 1) ? G - 1 - c : c);
-    if (i >= total) return false;
-    it.n = i % N;
-    it.t = pairs - 1 - i / N;
+    const int c = (int)blockIdx.x;
+    if (tab->count > 0) {
+      const int k = (int)tab->start[c] + round;
+      if (k >= (int)tab->start[c + 1]) return false;
+      const unsigned int e = tab->item[k];
+      it.n = (int)(e >> 16);
+      it.t = (int)(e & 0xFFFFu);
+    } else {
+      const int G = (int)gridDim.x;
+      const int i = round * G + ((round & 1) ? G - 1 - c : c);
+      if (i >= total) return false;
+      it.n = i % N;
+      it.t = pairs - 1 - i / N;
+    }
     it.q0 = it.t * kPairRows;
     it.nA = causal ? min(2 * it.t + 1, nkv) : nkv;
     it.nB = causal ? min(2 * it.t + 2, nkv) : nkv;  // never shorter than nA
@@ -176,8 +212,9 @@ struct Schedule {
 template <int D, bool F16>
 __global__ void __launch_bounds__(kThreadsTC, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                   const __grid_constant__ CUtensorMap tmv, uint8_t* __restrict__ out, float* __restrict__ lse,
-                   int dout, int N, int S, int causal, float scale_log2, unsigned long long limit) {
+                   const __grid_constant__ CUtensorMap tmv, const __grid_constant__ SchedTable tab,
+                   uint8_t* __restrict__ out, float* __restrict__ lse, int dout, int N, int S, int causal,
+                   float scale_log2, unsigned long long limit) {
   // dout: output columns per row (D, or 32 when a d = 32 problem runs on the 64-wide kernel
   // with its tiles zero-filled by TMA past column 32)
   using C = TcCfg<D>;
@@ -193,7 +230,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::OFF_MISC + 4);
   auto bar = [&](int i) -> uint32_t { return base + C::OFF_BAR + 8u * (uint32_t)i; };
 
-  const Schedule sched(N, S, causal);
+  const Schedule sched(N, S, causal, &tab);
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -556,24 +593,37 @@ struct Tc256 {
   static constexpr uint32_t TM_O = 256;  // O in columns 256-511; score buffer b in 64 b .. 64 b + 63
 };
 
-// One query tile per item; heaviest (causal) first, dealt in a snake order.
+// One query tile per item: from the host's work lists (same construction as for
+// the pair kernel), or heaviest (causal) first in a snake order.
 struct Item256 {
   int n, q0, nk;  // head, first row, key tiles
 };
 
 struct Schedule256 {
   int N, S, causal, tiles, nkv, total;
-  __device__ Schedule256(int N_, int S_, int causal_) : N(N_), S(S_), causal(causal_) {
+  const SchedTable* tab;
+  __device__ Schedule256(int N_, int S_, int causal_, const SchedTable* tab_)
+      : N(N_), S(S_), causal(causal_), tab(tab_) {
     tiles = (S + kBM - 1) / kBM;
     nkv = (S + kBN256 - 1) / kBN256;
     total = N * tiles;
   }
   __device__ bool get(int round, Item256& it) const {
-    const int G = (int)gridDim.x, c = (int)blockIdx.x;
-    const int i = round * G + ((round & 1) ? G - 1 - c : c);
-    if (i >= total) return false;
-    const int t = tiles - 1 - i / N;
-    it.n = i % N;
+    const int c = (int)blockIdx.x;
+    int t;
+    if (tab->count > 0) {
+      const int k = (int)tab->start[c] + round;
+      if (k >= (int)tab->start[c + 1]) return false;
+      const unsigned int e = tab->item[k];
+      it.n = (int)(e >> 16);
+      t = (int)(e & 0xFFFFu);
+    } else {
+      const int G = (int)gridDim.x;
+      const int i = round * G + ((round & 1) ? G - 1 - c : c);
+      if (i >= total) return false;
+      t = tiles - 1 - i / N;
+      it.n = i % N;
+    }
     it.q0 = t * kBM;
     it.nk = causal ? min(2 * t + 2, nkv) : nkv;
     return true;
@@ -583,8 +633,9 @@ struct Schedule256 {
 template <bool F16>
 __global__ void __launch_bounds__(kThreads256, 1)
     attn_tc256_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                      const __grid_constant__ CUtensorMap tmv, uint8_t* __restrict__ out, float* __restrict__ lse,
-                      int N, int S, int causal, float scale_log2, unsigned long long limit) {
+                      const __grid_constant__ CUtensorMap tmv, const __grid_constant__ SchedTable tab,
+                      uint8_t* __restrict__ out, float* __restrict__ lse, int N, int S, int causal,
+                      float scale_log2, unsigned long long limit) {
   using C = Tc256;
   constexpr uint32_t kAB = F16 ? 0u : 1u;
   constexpr uint32_t IDESC_QK = ptx::f16_idesc(kBM, kBN256, kAB, 0);
@@ -598,7 +649,7 @@ __global__ void __launch_bounds__(kThreads256, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::OFF_MISC + 4);
   auto bar = [&](int i) -> uint32_t { return base + C::OFF_BAR + 8u * (uint32_t)i; };
 
-  const Schedule256 sched(N, S, causal);
+  const Schedule256 sched(N, S, causal, &tab);
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -923,6 +974,65 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// K and V bytes that one head group may keep in L2: about a quarter of the
+// 129 MB, leaving room for the Q, O and next-group traffic around them.
+constexpr double kGroupKvBytes = 32.0 * 1024 * 1024;
+
+// Work lists for `grid` persistent CTAs over N heads x `units` query units. A
+// unit t costs min(2 t + 2, nkv) key tiles when causal (nkv otherwise) plus one
+// for its pipeline fill and epilogue. Heads are split into contiguous groups
+// whose K and V fit kGroupKvBytes; within a group the units go heaviest first,
+// and each goes to the CTA with the least work so far (lowest index on ties).
+void build_table(SchedTable& tab, int64_t N, int units, int nkv, bool causal, int grid, double kv_bytes_per_head) {
+  tab.count = 0;
+  const int64_t total = N * units;
+  if (grid <= 0 || grid > kSchedMaxGrid || total <= grid || total > kSchedMaxItems || N > 65535 || units > 65535)
+    return;
+  int groups = (int)std::ceil((double)N * kv_bytes_per_head / kGroupKvBytes);
+  groups = std::max(1, std::min(groups, (int)N));
+  std::vector<std::vector<unsigned int>> lists((size_t)grid);
+  using Slot = std::pair<double, int>;  // work so far, CTA
+  std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
+  for (int c = 0; c < grid; ++c) heap.push({0.0, c});
+  for (int g = 0; g < groups; ++g) {
+    const int64_t h0 = N * g / groups, h1 = N * (g + 1) / groups;
+    for (int t = units - 1; t >= 0; --t) {
+      const double cost = (causal ? std::min(2 * t + 2, nkv) : nkv) + 1.0;
+      for (int64_t n = h0; n < h1; ++n) {
+        const Slot s = heap.top();
+        heap.pop();
+        lists[(size_t)s.second].push_back((unsigned int)(n << 16) | (unsigned int)t);
+        heap.push({s.first + cost, s.second});
+      }
+    }
+  }
+  int k = 0;
+  for (int c = 0; c < grid; ++c) {
+    tab.start[c] = (unsigned short)k;
+    for (unsigned int e : lists[(size_t)c]) tab.item[k++] = e;
+  }
+  tab.start[grid] = (unsigned short)k;
+  tab.count = k;
+}
+
+// The table for one problem shape, built once and kept (a few shapes at most in
+// practice; the cache is emptied if it ever grows past 64 entries).
+SchedTable sched_table(int64_t N, int units, int nkv, bool causal, int grid, double kv_bytes_per_head) {
+  using Key = std::tuple<int64_t, int, int, int, int, double>;
+  static std::mutex mu;
+  static std::map<Key, std::unique_ptr<SchedTable>> cache;
+  const Key key{N, units, nkv, (int)causal, grid, kv_bytes_per_head};
+  std::lock_guard<std::mutex> lock(mu);
+  auto f = cache.find(key);
+  if (f == cache.end()) {
+    if (cache.size() >= 64) cache.clear();
+    auto t = std::make_unique<SchedTable>();
+    build_table(*t, N, units, nkv, causal, grid, kv_bytes_per_head);
+    f = cache.emplace(key, std::move(t)).first;
+  }
+  return *f->second;
+}
+
 // [N, S, d] row-major 16-bit tensor, boxes of 64 features x `rows` rows x 1 head.
 bool make_map(CUtensorMap* m, const void* ptr, int64_t N, int S, int d, bool f16, int rows = kBM) {
   EncodeTiledFn fn = encode_fn();
@@ -954,10 +1064,13 @@ cudaError_t tc_launch(const AttnProblem& p, cudaStream_t st) {
   int dev = 0, sms = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-  const int64_t items = (int64_t)((p.S + kPairRows - 1) / kPairRows) * p.N;
+  const int units = (p.S + kPairRows - 1) / kPairRows;
+  const int64_t items = (int64_t)units * p.N;
   const int64_t grid = items < sms ? items : sms;  // persistent: at most one CTA per SM
+  const SchedTable tab = sched_table(p.N, units, (p.S + kBN - 1) / kBN, p.causal != 0, (int)grid,
+                                     2.0 * p.S * dreal * 2.0);
   attn_tc_kernel<D, F16><<<(unsigned)grid, kThreadsTC, C::SMEM, st>>>(
-      mq, mk, mv, static_cast<uint8_t*>(p.o), p.lse, dreal, (int)p.N, p.S, p.causal,
+      mq, mk, mv, tab, static_cast<uint8_t*>(p.o), p.lse, dreal, (int)p.N, p.S, p.causal,
       p.scale * 1.4426950408889634f, kDefaultWaitLimitNs);
   return cudaGetLastError();
 }
@@ -974,10 +1087,13 @@ cudaError_t tc256_launch(const AttnProblem& p, cudaStream_t st) {
   int dev = 0, sms = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-  const int64_t items = (int64_t)((p.S + kBM - 1) / kBM) * p.N;
+  const int units = (p.S + kBM - 1) / kBM;
+  const int64_t items = (int64_t)units * p.N;
   const int64_t grid = items < sms ? items : sms;
+  const SchedTable tab = sched_table(p.N, units, (p.S + kBN256 - 1) / kBN256, p.causal != 0, (int)grid,
+                                     2.0 * p.S * C::D * 2.0);
   attn_tc256_kernel<F16><<<(unsigned)grid, kThreads256, C::SMEM, st>>>(
-      mq, mk, mv, static_cast<uint8_t*>(p.o), p.lse, (int)p.N, p.S, p.causal, p.scale * 1.4426950408889634f,
+      mq, mk, mv, tab, static_cast<uint8_t*>(p.o), p.lse, (int)p.N, p.S, p.causal, p.scale * 1.4426950408889634f,
       kDefaultWaitLimitNs);
   return cudaGetLastError();
 }
