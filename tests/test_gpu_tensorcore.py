@@ -123,3 +123,29 @@ def test_tc_rejects_unsupported_head_dim():
     st = kbattn.kb_attn_fwd_ptr(1 << 20, 1 << 20, 1 << 20, 1 << 20, 1, 1, 128, 96, False, 0.17,
                                 kbattn.DType.BF16, Variant.TC, 0)
     assert st == kbattn.Status.UNSUPPORTED
+
+
+@pytest.mark.parametrize("d,dtype", [(64, "bf16"), (128, "f16"), (256, "bf16")])
+def test_work_list_schedule_direct_and_graph(oracle, d, dtype):
+    """More query units than CTAs, so the host-built per-CTA work lists (a
+    grid-constant kernel parameter) drive the kernel: every unit is computed
+    exactly once (sampled rows of every head against the oracle, the canaries
+    intact), and replaying 20 captured launches in a CUDA graph leaves the same
+    bits as one direct launch."""
+    S = 2048 if d < 256 else 1024
+    w = inputs.Workload("t", 2, 12 if d < 256 else 24, S, d, True, dtype, 31 + d, "normal")
+    q, k, v = inputs.make_qkv(w)
+    direct = run_tc(q, k, v, w.causal, w.scale)
+    g = Guarded(q.shape, q.dtype)
+    ms = kbattn.kb_attn_bench_graph(q.cuda(), k.cuda(), v.cuda(), g.out, causal=w.causal, scale=w.scale,
+                                    variant=Variant.TC, launches=20, warmup=1, iters=2)
+    assert kbattn.kb_check_device_error() == kbattn.Status.OK
+    assert len(ms) == 2 and all(x > 0 for x in ms)
+    assert torch.equal(g.check(), direct)
+    N = w.B * w.H
+    heads = torch.arange(N).repeat_interleave(3)
+    rows = torch.tensor([0, S // 2 + 77, S - 1] * N)
+    got = direct.reshape(N, S, d)[heads.cuda(), rows.cuda()].float().cpu().numpy()
+    want = oracle.attn_rows(q, k, v, w.causal, w.scale, heads.numpy(), rows.numpy())
+    mx, mean, _ = errors(got, want)
+    assert mx <= MAX_TOL and mean <= MEAN_TOL, (mx, mean)
