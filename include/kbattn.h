@@ -294,6 +294,28 @@ KB_API int kb_attn_fwd_naive_noalloc(const void* q, const void* k, const void* v
                                      int B, int H, int S, int d, int causal, float scale,
                                      void* stream);
 
+/*
+ * kb_attn_work_lists -- the per-CTA work lists the KB_TC path launches with, for
+ * inspection (host only, no CUDA call). A unit is query rows [256 u, 256 u + 256)
+ * of one head (d <= 128: the two 128-row tiles of a work item) or [128 u, 128 u +
+ * 128) (d = 256). The heads are split into contiguous groups whose K and V fit
+ * 32 MB of L2; within a group the units go heaviest first (causal: most key
+ * tiles), each to the CTA with the least modelled work so far (key tiles + 1).
+ * The kernel runs CTA c's units in list order. The lists are deterministic.
+ *   N      : heads (B * H), > 0;  S > 0;  d : 32, 64, 128 or 256
+ *   grid   : persistent CTAs (the launch uses min(units, SMs))
+ *   start  : host array of grid + 1 ints; CTA c runs items[start[c] .. start[c + 1])
+ *   items  : host array of `cap` entries, head << 16 | unit
+ *   count  : receives the number of entries; 0 means the kernel orders the units
+ *            itself (heaviest first, a snake over the CTAs): more than 4096
+ *            units, no more units than CTAs, or more than 256 CTAs; start and
+ *            items are then left untouched
+ * Returns KB_ERR_INVALID_ARG for null pointers, non-positive sizes, another d,
+ * or cap smaller than the count (which is then still stored in *count).
+ */
+KB_API int kb_attn_work_lists(long long N, int S, int d, int causal, int grid, int* start, unsigned int* items,
+                              int cap, int* count);
+
 /* Human-readable name of a kb_status (static storage, never NULL). */
 KB_API const char* kb_status_string(int status);
 

@@ -230,6 +230,13 @@ int kb_q15_exp_table(unsigned short* out64) {
   return kb::q15_exp_table(out64);
 }
 
+int kb_attn_work_lists(long long N, int S, int d, int causal, int grid, int* start, unsigned int* items, int cap,
+                       int* count) {
+  if (N <= 0 || S <= 0 || grid <= 0 || cap < 0 || !start || !items || !count) return KB_ERR_INVALID_ARG;
+  if (d != 32 && d != 64 && d != 128 && d != 256) return KB_ERR_INVALID_ARG;
+  return kb::tc_work_lists(N, S, d, causal != 0, grid, start, items, cap, count);
+}
+
 int kb_attn_fwd(const void* q, const void* k, const void* v, void* o, int B, int H, int S, int d, int causal,
                 float scale, int dtype, int variant, void* stream) {
   return run_attention(q, k, v, o, B, H, S, d, causal, scale, dtype, variant, stream, nullptr, 0, false);

@@ -1112,6 +1112,21 @@ int tc_check(int S, int d, int dtype) {
   return need <= optin ? KB_OK : KB_ERR_UNSUPPORTED;
 }
 
+// The work lists tc_launch / tc256_launch build for these arguments (host only).
+int tc_work_lists(int64_t N, int S, int d, bool causal, int grid, int* start, unsigned int* items, int cap,
+                  int* count) {
+  const bool wide = d == 256;
+  const int units = wide ? (S + kBM - 1) / kBM : (S + kPairRows - 1) / kPairRows;
+  const int nkv = wide ? (S + kBN256 - 1) / kBN256 : (S + kBN - 1) / kBN;
+  const SchedTable tab = sched_table(N, units, nkv, causal, grid, 2.0 * S * d * 2.0);
+  *count = tab.count;
+  if (tab.count == 0) return KB_OK;
+  if (cap < tab.count) return KB_ERR_INVALID_ARG;
+  for (int c = 0; c <= grid; ++c) start[c] = tab.start[c];
+  for (int k = 0; k < tab.count; ++k) items[k] = tab.item[k];
+  return KB_OK;
+}
+
 cudaError_t launch_tc(const AttnProblem& p, cudaStream_t st) {
   const bool f16 = p.dtype == KB_F16;
   if (p.d == 128) return f16 ? tc_launch<128, true>(p, st) : tc_launch<128, false>(p, st);

@@ -35,6 +35,10 @@ int fused_f32_check(int S, int d);
 
 cudaError_t launch_tc(const AttnProblem& p, cudaStream_t st);
 int tc_check(int S, int d, int dtype);
+// The per-CTA work lists of the tensor-core path (host only); *count = 0 when
+// the kernel falls back to its snake order.
+int tc_work_lists(int64_t N, int S, int d, bool causal, int grid, int* start, unsigned int* items, int cap,
+                  int* count);
 
 // Q15 fixed-point path: launcher, the scale limit (scale*log2(e)*2^16 <= 2^30)
 // and the 64-entry exp table it uses.

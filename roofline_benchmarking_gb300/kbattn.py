@@ -95,6 +95,8 @@ SIGNATURES = {
     "kb_last_cuda_error": (_I, []),
     "kb_version": (_I, []),
     "kb_q15_exp_table": (_I, [ctypes.POINTER(ctypes.c_uint16)]),
+    "kb_attn_work_lists": (_I, [ctypes.c_longlong, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_int),
+                                ctypes.POINTER(ctypes.c_uint32), _I, ctypes.POINTER(ctypes.c_int)]),
     "kb_attn_fwd_naive_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]),
     "kb_hbm_copy": (_I, [_P, _P, _SZ, _I, _P]),
     "kb_hbm_write": (_I, [_P, _F, _SZ, _I, _P]),
@@ -276,6 +278,21 @@ def kb_q15_exp_table() -> list[int]:
     out = (ctypes.c_uint16 * 64)()
     _check(load().kb_q15_exp_table(out), "kb_q15_exp_table")
     return list(out)
+
+
+def kb_attn_work_lists(N: int, S: int, d: int, causal: bool, grid: int):
+    """The tensor-core path's per-CTA work lists: a list of ``grid`` lists of
+    (head, unit) pairs in run order, or None when the kernel orders the units
+    itself (see include/kbattn.h)."""
+    cap = 4096
+    start = (ctypes.c_int * (grid + 1))()
+    items = (ctypes.c_uint32 * cap)()
+    count = ctypes.c_int(0)
+    _check(load().kb_attn_work_lists(N, S, d, int(bool(causal)), grid, start, items, cap, ctypes.byref(count)),
+           "kb_attn_work_lists")
+    if count.value == 0:
+        return None
+    return [[(items[k] >> 16, items[k] & 0xFFFF) for k in range(start[c], start[c + 1])] for c in range(grid)]
 
 
 def kb_attn_bench_graph(q, k, v, o, causal: bool, scale: float | None = None, variant: int = Variant.AUTO,
