@@ -135,6 +135,94 @@ __device__ __forceinline__ void group_bar(int grp) {
   asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "r"(kThreads) : "memory");
 }
 
+// Asynchronous global -> shared copies (cp.async): `bytes` (4 or 16) from src,
+// or zeros when !valid (no byte is read then; src is still a mapped address).
+template <int BYTES>
+__device__ __forceinline__ void cp_async(float* dst, const float* src, bool valid) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+  if constexpr (BYTES == 16)
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(valid ? 16 : 0) : "memory");
+  else
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(d), "l"(src), "r"(valid ? 4 : 0) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Wait until at most N of this thread's committed groups are still in flight.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Row stride of the flash kernel's row-major K tile: D + 4 floats, so that the
+// rows a thread reads (consecutive keys across the 16 threads of a row group)
+// fall in different 16-byte bank groups.
+template <int D>
+constexpr int flash_ldk() { return D + 4; }
+
+// One group's copies of key tile [k0, k0 + 64): K row-major into Kr[r * (D + 4) + k]
+// and V row-major into Vr[r * D + c], 16-byte copies; rows >= S are zero-filled.
+template <int D>
+__device__ __forceinline__ void flash_issue_kv(float* Kr, float* Vr, const float* Kh, const float* Vh, int k0, int S,
+                                               int tid) {
+  for (int f = tid; f < kBC * (D / 4); f += kThreads) {
+    const int r = f / (D / 4), c4 = f % (D / 4);
+    const bool ok = k0 + r < S;
+    cp_async<16>(Kr + r * flash_ldk<D>() + 4 * c4, Kh + (int64_t)(ok ? k0 + r : 0) * D + 4 * c4, ok);
+  }
+  for (int f = tid; f < kBC * (D / 4); f += kThreads) {
+    const int r = f / (D / 4), c4 = f % (D / 4);
+    const bool ok = k0 + r < S;
+    cp_async<16>(Vr + r * D + 4 * c4, Vh + (int64_t)(ok ? k0 + r : 0) * D + 4 * c4, ok);
+  }
+}
+
+// At d <= 64 each group double-buffers its K and V tiles: the copies of its next
+// tile (cp.async) are in flight while it computes the current one. At d = 128
+// two buffers per group do not fit in shared memory; the loads stay synchronous.
+template <int D>
+constexpr bool flash_double_buffer() { return D <= 64; }
+template <int D>
+constexpr int flash_group_floats() {
+  return (flash_double_buffer<D>() ? 2 : 1) * (kBC * flash_ldk<D>() + kBC * D) + kBC * kLD;
+}
+
+// s[a][b] = sum_k Qs[k][ty*4+a] * K[tx+16b][k]: Q transposed (Qs[k * kLD + r]), K
+// row-major (Kr[key * (D + 4) + k]); the thread's keys are tx, tx+16, tx+32, tx+48.
+template <int D>
+__device__ __forceinline__ void qk_tile_rowk(float (&s)[4][4], const float* Qs, const float* Kr, int ty, int tx) {
+  constexpr int LDK = flash_ldk<D>();
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int b = 0; b < 4; ++b) s[a][b] = 0.f;
+#pragma unroll 2
+  for (int k = 0; k < D; k += 4) {
+    float4 q[4], kv[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) q[i] = ld4(Qs + (k + i) * kLD + ty * 4);
+#pragma unroll
+    for (int b = 0; b < 4; ++b) kv[b] = ld4(Kr + (tx + 16 * b) * LDK + k);
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      s[0][b] = fmaf(q[0].x, kv[b].x, s[0][b]);
+      s[1][b] = fmaf(q[0].y, kv[b].x, s[1][b]);
+      s[2][b] = fmaf(q[0].z, kv[b].x, s[2][b]);
+      s[3][b] = fmaf(q[0].w, kv[b].x, s[3][b]);
+      s[0][b] = fmaf(q[1].x, kv[b].y, s[0][b]);
+      s[1][b] = fmaf(q[1].y, kv[b].y, s[1][b]);
+      s[2][b] = fmaf(q[1].z, kv[b].y, s[2][b]);
+      s[3][b] = fmaf(q[1].w, kv[b].y, s[3][b]);
+      s[0][b] = fmaf(q[2].x, kv[b].z, s[0][b]);
+      s[1][b] = fmaf(q[2].y, kv[b].z, s[1][b]);
+      s[2][b] = fmaf(q[2].z, kv[b].z, s[2][b]);
+      s[3][b] = fmaf(q[2].w, kv[b].z, s[3][b]);
+      s[0][b] = fmaf(q[3].x, kv[b].w, s[0][b]);
+      s[1][b] = fmaf(q[3].y, kv[b].w, s[1][b]);
+      s[2][b] = fmaf(q[3].z, kv[b].w, s[2][b]);
+      s[3][b] = fmaf(q[3].w, kv[b].w, s[3][b]);
+    }
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kFlashThreads, 1) flash_f32_kernel(const float* __restrict__ Q,
                                                                   const float* __restrict__ K,
@@ -142,13 +230,14 @@ __global__ void __launch_bounds__(kFlashThreads, 1) flash_f32_kernel(const float
                                                                   float* __restrict__ O, float* __restrict__ lse,
                                                                   int64_t N, int S, int causal, float scale_log2) {
   using C = Cols<D>;
-  constexpr int GROUP = D * kLD + kBC * D + kBC * kLD;  // floats of one group's K, V and P buffers
+  constexpr bool DB = flash_double_buffer<D>();
+  constexpr int GROUP = flash_group_floats<D>();  // floats of one group's K, V and P buffers
+  constexpr int KV = kBC * flash_ldk<D>() + kBC * D;  // one K + V buffer pair
   extern __shared__ float4 smem4[];
   float* Qs = reinterpret_cast<float*>(smem4);  // [D][kLD], both groups
   const int grp = threadIdx.x / kThreads, ltid = threadIdx.x % kThreads;
-  float* Ks = Qs + D * kLD + grp * GROUP;        // [D][kLD]
-  float* Vs = Ks + D * kLD;                      // [kBC][D]
-  float* Ps = Vs + kBC * D;                      // [kBC][kLD]
+  float* KV0 = Qs + D * kLD + grp * GROUP;       // buffer b: K [kBC][D + 4] at KV0 + b KV, V [kBC][D] after it
+  float* Ps = KV0 + (DB ? 2 : 1) * KV;           // [kBC][kLD]
 
   const int ntiles = (S + kBR - 1) / kBR;
   const int64_t n = blockIdx.x % N;
@@ -172,15 +261,31 @@ __global__ void __launch_bounds__(kFlashThreads, 1) flash_f32_kernel(const float
   }
 
   const int kt_last = causal ? qt : ntiles - 1;
-  for (int kt = grp; kt <= kt_last; kt += 2) {
+  if constexpr (DB) {
+    if (grp <= kt_last) flash_issue_kv<D>(KV0, KV0 + kBC * flash_ldk<D>(), Kh, Vh, grp * kBC, S, ltid);
+    cp_async_commit();
+  }
+  for (int kt = grp, it = 0; kt <= kt_last; kt += 2, ++it) {
     const int k0 = kt * kBC;
-    group_bar(grp);  // the group's previous Ks, Vs, Ps are no longer read
-    load_transposed<D>(Ks, Kh, k0, S, 1.0f, ltid, kThreads);
-    load_rows<D>(Vs, Vh, k0, S, ltid, kThreads);
+    float* Ks = KV0 + (DB ? (it & 1) * KV : 0);  // [kBC][D + 4]
+    float* Vs = Ks + kBC * flash_ldk<D>();        // [kBC][D]
+    group_bar(grp);  // the group's previous K, V (other buffer) and P are no longer read
+    if constexpr (DB) {
+      if (kt + 2 <= kt_last) {
+        float* Kn = KV0 + ((it + 1) & 1) * KV;
+        flash_issue_kv<D>(Kn, Kn + kBC * flash_ldk<D>(), Kh, Vh, k0 + 2 * kBC, S, ltid);
+      }
+      cp_async_commit();
+      cp_async_wait<1>();  // this thread's copies of tile kt have landed
+    } else {
+      flash_issue_kv<D>(Ks, Vs, Kh, Vh, k0, S, ltid);
+      cp_async_commit();
+      cp_async_wait<0>();
+    }
     group_bar(grp);
 
     float s[4][4];
-    qk_tile<D>(s, Qs, Ks, ty, tx);
+    qk_tile_rowk<D>(s, Qs, Ks, ty, tx);
 
     // mask, then the online-softmax update for each of the thread's 4 rows
 #pragma unroll
@@ -189,7 +294,7 @@ __global__ void __launch_bounds__(kFlashThreads, 1) flash_f32_kernel(const float
       float tmax = -INFINITY;
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
-        const int key = k0 + tx * 4 + b;
+        const int key = k0 + tx + 16 * b;
         if (key >= S || (causal && key > row)) s[a][b] = -INFINITY;
         tmax = fmaxf(tmax, s[a][b]);
       }
@@ -211,7 +316,7 @@ __global__ void __launch_bounds__(kFlashThreads, 1) flash_f32_kernel(const float
     }
 #pragma unroll
     for (int b = 0; b < 4; ++b)
-      *reinterpret_cast<float4*>(Ps + (tx * 4 + b) * kLD + ty * 4) = make_float4(s[0][b], s[1][b], s[2][b], s[3][b]);
+      *reinterpret_cast<float4*>(Ps + (tx + 16 * b) * kLD + ty * 4) = make_float4(s[0][b], s[1][b], s[2][b], s[3][b]);
     group_bar(grp);
     pv_accumulate<D>(acc, Ps, Vs, ty, tx, kBC);
   }
@@ -537,7 +642,10 @@ __global__ void __launch_bounds__(kFusedThreads) fused_row_f32_kernel(const floa
   }
 }
 
-size_t flash_smem(int d) { return sizeof(float) * (size_t)(d * kLD + 2 * (d * kLD + kBC * d + kBC * kLD)); }
+size_t flash_smem(int d) {
+  const int group = d == 32 ? flash_group_floats<32>() : d == 64 ? flash_group_floats<64>() : flash_group_floats<128>();
+  return sizeof(float) * (size_t)(d * kLD + 2 * group);
+}
 size_t naive_scores_smem(int d) { return sizeof(float) * (size_t)(2 * d * kLD); }
 size_t naive_pv_smem(int d) { return sizeof(float) * (size_t)(2 * (kBC * kLD + kBC * d)); }
 size_t fused_smem(int S, int d, int rows = 1) {
