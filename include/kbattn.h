@@ -59,7 +59,7 @@ extern "C" {
 typedef enum {
   KB_OK = 0,
   KB_ERR_INVALID_ARG = 1, /* null pointer, non-positive size, bad scale, overflow */
-  KB_ERR_UNSUPPORTED = 2, /* valid request this build has no kernel for */
+  KB_ERR_UNSUPPORTED = 2, /* valid request the library has no kernel for */
   KB_ERR_CUDA = 3,        /* a CUDA runtime call failed; see kb_last_cuda_error() */
   KB_ERR_NO_MEMORY = 4,   /* workspace too small or allocation failed */
   KB_ERR_TIMEOUT = 5,     /* a bounded device-side wait ran out */
