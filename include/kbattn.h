@@ -132,11 +132,13 @@ typedef struct {
  * KB_TC supports d = 32 (run by the d = 64 kernel on tiles whose features
  * 32-63 are zero-filled by TMA), 64, 128 and 256 (one 128-row query tile per
  * CTA); KB_NAIVE, KB_FUSED and KB_FLASH support d = 32, 64 and 128.
- * KB_NAIVE needs N*S*S*4 bytes of workspace: this call takes it from a
- * per-device cache that it grows with cudaMalloc, synchronising the device
- * first when it replaces a smaller buffer (so it may allocate and block);
- * calls on different streams share that cache and must not overlap.
- * kb_attn_fwd_ws lets the caller supply the workspace instead.
+ * KB_NAIVE needs N*S*S*4 bytes of workspace, and a causal KB_FLASH call on a
+ * small grid the partial states of its split query tiles (see
+ * kb_attn_workspace_bytes): this call takes them from a per-device cache that
+ * it grows with cudaMalloc, synchronising the device first when it replaces a
+ * smaller buffer (so it may allocate and block); calls on different streams
+ * share that cache and must not overlap. kb_attn_fwd_ws lets the caller supply
+ * the workspace instead.
  */
 KB_API int kb_attn_fwd(const void* q, const void* k, const void* v, void* o,
                 int B, int H, int S, int d, int causal, float scale,
@@ -156,12 +158,16 @@ KB_API int kb_attn_fwd_lse(const void* q, const void* k, const void* v, void* o,
                            int B, int H, int S, int d, int causal, float scale,
                            int dtype, int variant, void* stream);
 
-/* Workspace bytes kb_attn_fwd_ws needs (0 for every variant but KB_NAIVE,
- * and 0 for an invalid request). */
+/* Workspace bytes kb_attn_fwd_ws uses: KB_NAIVE's N*S*S*4 score matrix; for
+ * KB_FLASH, the partial states of its split causal query tiles (the heavier
+ * half of them runs as two blocks over two key ranges when N * ceil(S/64) is
+ * at most twice the SM count, and a merge kernel combines the halves); 0 for
+ * the other variants and for an invalid request. */
 KB_API size_t kb_attn_workspace_bytes(int B, int H, int S, int d, int dtype, int variant);
 
 /* kb_attn_fwd with a caller-owned device workspace of ws_bytes bytes (16-byte
- * aligned); KB_ERR_NO_MEMORY if ws_bytes < kb_attn_workspace_bytes(...).
+ * aligned). KB_NAIVE: KB_ERR_NO_MEMORY if ws_bytes < kb_attn_workspace_bytes(...).
+ * KB_FLASH: with less (or none), its causal tiles simply run unsplit.
  * The library allocates nothing in this call. */
 KB_API int kb_attn_fwd_ws(const void* q, const void* k, const void* v, void* o,
                    int B, int H, int S, int d, int causal, float scale,

@@ -161,6 +161,18 @@ int run_attention(const void* q, const void* k, const void* v, void* o, int B, i
   } else if ((st = check_device()) != KB_OK) {
     return st;
   }
+  if (var == KB_FLASH && flash_wants_split(p.N, S, causal)) {
+    // split causal tiles need room for their partial states; without it (a caller's
+    // workspace that is absent or too small) the kernel runs every tile whole
+    const size_t need = flash_split_bytes(p.N, S, d);
+    if (caller_ws) {
+      if (workspace && ws_bytes >= need && aligned16(workspace)) p.work = static_cast<float*>(workspace);
+    } else {
+      void* w = nullptr;
+      if ((st = cached_workspace(need, &w)) != KB_OK) return st;
+      p.work = static_cast<float*>(w);
+    }
+  }
   if (var == KB_FUSED && (st = fused_f32_check(S, d)) != KB_OK) return st;
   if (var == KB_TC && (st = tc_check(S, d, dtype)) != KB_OK) return st;
 
@@ -256,7 +268,9 @@ size_t kb_attn_workspace_bytes(int B, int H, int S, int d, int dtype, int varian
   int var = 0;
   const void* dummy = reinterpret_cast<const void*>(static_cast<uintptr_t>(256));
   if (validate(dummy, dummy, dummy, dummy, B, H, S, d, 0, 1.0f, dtype, variant, &var) != KB_OK) return 0;
-  return var == KB_NAIVE ? naive_workspace_bytes((int64_t)B * H, S) : 0;
+  if (var == KB_NAIVE) return naive_workspace_bytes((int64_t)B * H, S);
+  if (var == KB_FLASH) return flash_split_bytes((int64_t)B * H, S, d);  // used by causal calls only
+  return 0;
 }
 
 int kb_attn_fwd_ws(const void* q, const void* k, const void* v, void* o, int B, int H, int S, int d, int causal,

@@ -228,7 +228,12 @@ __global__ void __launch_bounds__(kFlashThreads, 1) flash_f32_kernel(const float
                                                                   const float* __restrict__ K,
                                                                   const float* __restrict__ V,
                                                                   float* __restrict__ O, float* __restrict__ lse,
-                                                                  int64_t N, int S, int causal, float scale_log2) {
+                                                                  int64_t N, int S, int causal, float scale_log2,
+                                                                  float* __restrict__ part, int split_from) {
+  // part / split_from: causal query tiles qt >= split_from are computed by two
+  // blocks, over key tiles [0, h) and [h, qt] with h = ceil((qt + 1) / 2); each
+  // writes its merged online-softmax state (m, l and the unnormalised O rows) to
+  // `part` and flash_merge_kernel combines the two. split_from = tiles: no split.
   using C = Cols<D>;
   constexpr bool DB = flash_double_buffer<D>();
   constexpr int GROUP = flash_group_floats<D>();  // floats of one group's K, V and P buffers
@@ -240,8 +245,21 @@ __global__ void __launch_bounds__(kFlashThreads, 1) flash_f32_kernel(const float
   float* Ps = KV0 + (DB ? 2 : 1) * KV;           // [kBC][kLD]
 
   const int ntiles = (S + kBR - 1) / kBR;
+  const int nsplit = ntiles - split_from;  // split query tiles per head
   const int64_t n = blockIdx.x % N;
-  const int qt = ntiles - 1 - (int)(blockIdx.x / N);
+  const int u = (int)(blockIdx.x / N);  // heaviest units first: the split tiles' parts, then the rest
+  int qt, kb, ke, pt = -1;              // query tile, key tiles [kb, ke], part (-1: whole tile)
+  if (u < 2 * nsplit) {
+    qt = ntiles - 1 - u / 2;
+    pt = u & 1;
+    const int h = (qt + 2) / 2;
+    kb = pt ? h : 0;
+    ke = pt ? qt : h - 1;
+  } else {
+    qt = split_from - 1 - (u - 2 * nsplit);
+    kb = 0;
+    ke = causal ? qt : ntiles - 1;
+  }
   const int q0 = qt * kBR;
   const int tx = ltid & 15, ty = ltid >> 4;
   const float* Qh = Q + n * S * D;
@@ -260,12 +278,12 @@ __global__ void __launch_bounds__(kFlashThreads, 1) flash_f32_kernel(const float
     for (int c = 0; c < D / 16; ++c) acc[a][c] = 0.f;
   }
 
-  const int kt_last = causal ? qt : ntiles - 1;
+  const int kt_last = ke;
   if constexpr (DB) {
-    if (grp <= kt_last) flash_issue_kv<D>(KV0, KV0 + kBC * flash_ldk<D>(), Kh, Vh, grp * kBC, S, ltid);
+    if (kb + grp <= kt_last) flash_issue_kv<D>(KV0, KV0 + kBC * flash_ldk<D>(), Kh, Vh, (kb + grp) * kBC, S, ltid);
     cp_async_commit();
   }
-  for (int kt = grp, it = 0; kt <= kt_last; kt += 2, ++it) {
+  for (int kt = kb + grp, it = 0; kt <= kt_last; kt += 2, ++it) {
     const int k0 = kt * kBC;
     float* Ks = KV0 + (DB ? (it & 1) * KV : 0);  // [kBC][D + 4]
     float* Vs = Ks + kBC * flash_ldk<D>();        // [kBC][D]
@@ -342,11 +360,28 @@ __global__ void __launch_bounds__(kFlashThreads, 1) flash_f32_kernel(const float
   for (int a = 0; a < 4; ++a) {
     const int row = q0 + ty * 4 + a;
     const float m1 = X[a * kThreads + ltid], l1 = X[(4 + a) * kThreads + ltid];
-    const float mm = fmaxf(m[a], m1);  // group 0 always sees key 0, so m[a] and mm are finite
+    // group 0 always sees key kb * 64 <= every row of the tile, so m[a] and mm are finite
+    const float mm = fmaxf(m[a], m1);
     const float s0 = exp2f(m[a] - mm);
     const float s1 = m1 == -INFINITY ? 0.f : exp2f(m1 - mm);
     const float lt = l[a] * s0 + l1 * s1;
     if (row >= S) continue;
+    if (pt >= 0) {  // a part of a split tile: its state, for flash_merge_kernel
+      const int lr = ty * 4 + a;
+      float* st = part + ((n * nsplit + (ntiles - 1 - qt)) * 2 + pt) * (int64_t)(kBR * (D + 2));
+      if (tx == 0) {
+        st[lr] = mm;
+        st[kBR + lr] = lt;
+      }
+#pragma unroll
+      for (int g = 0; g < C::G; ++g)
+#pragma unroll
+        for (int e = 0; e < C::W; ++e) {
+          const float a1 = X[(8 + a * (D / 16) + g * C::W + e) * kThreads + ltid];
+          st[2 * kBR + lr * D + g * 16 * C::W + tx * C::W + e] = acc[a][g * C::W + e] * s0 + a1 * s1;
+        }
+      continue;
+    }
     const float inv = 1.0f / lt;
     // natural log of sum_j exp(score): the scores sum to 2^mm * lt in base 2
     if (lse != nullptr && tx == 0) lse[n * S + row] = (mm + log2f(lt)) * 0.6931471805599453f;
@@ -359,6 +394,35 @@ __global__ void __launch_bounds__(kFlashThreads, 1) flash_f32_kernel(const float
         orow[g * 16 * C::W + tx * C::W + e] = (acc[a][g * C::W + e] * s0 + a1 * s1) * inv;
       }
   }
+}
+
+// Combines the two parts of every split query tile: O = (acc0 s0 + acc1 s1) / l
+// with s_p = 2^(m_p - max(m0, m1)), l = l0 s0 + l1 s1 (two online-softmax states
+// over disjoint key ranges, combined like the flash kernel's own group merge).
+// One block of 256 threads per split tile: thread t takes row t / 4 and the
+// columns c = t % 4 + 4 i.
+template <int D>
+__global__ void __launch_bounds__(256) flash_merge_kernel(const float* __restrict__ part, float* __restrict__ O,
+                                                        float* __restrict__ lse, int S, int nsplit) {
+  const int64_t n = blockIdx.x / nsplit;
+  const int j = (int)(blockIdx.x % nsplit);
+  const int ntiles = (S + kBR - 1) / kBR;
+  const int qt = ntiles - 1 - j;
+  const int lr = threadIdx.x >> 2, c0 = threadIdx.x & 3;
+  const int row = qt * kBR + lr;
+  if (row >= S) return;
+  const float* p0 = part + (n * nsplit + j) * 2 * (int64_t)(kBR * (D + 2));
+  const float* p1 = p0 + kBR * (D + 2);
+  const float m0 = p0[lr], m1 = p1[lr];
+  const float mm = fmaxf(m0, m1);
+  const float s0 = m0 == -INFINITY ? 0.f : exp2f(m0 - mm);
+  const float s1 = m1 == -INFINITY ? 0.f : exp2f(m1 - mm);
+  const float lt = p0[kBR + lr] * s0 + p1[kBR + lr] * s1;
+  const float inv = 1.0f / lt;
+  if (lse != nullptr && c0 == 0) lse[n * S + row] = (mm + log2f(lt)) * 0.6931471805599453f;
+  float* orow = O + (n * S + row) * D;
+  for (int c = c0; c < D; c += 4)
+    orow[c] = (p0[2 * kBR + lr * D + c] * s0 + p1[2 * kBR + lr * D + c] * s1) * inv;
 }
 
 // ---------------------------------------------------------------------------
@@ -663,10 +727,14 @@ cudaError_t flash_launch(const AttnProblem& p, cudaStream_t st) {
   const size_t smem = flash_smem(D);
   cudaError_t e = set_smem(flash_f32_kernel<D>, smem);
   if (e != cudaSuccess) return e;
-  const int64_t tiles = (p.S + kBR - 1) / kBR;
-  flash_f32_kernel<D><<<(unsigned)(tiles * p.N), kFlashThreads, smem, st>>>(
+  const int tiles = (p.S + kBR - 1) / kBR;
+  const int split_from = p.work ? (tiles + 1) / 2 : tiles;
+  const int nsplit = tiles - split_from;
+  flash_f32_kernel<D><<<(unsigned)((tiles + nsplit) * p.N), kFlashThreads, smem, st>>>(
       (const float*)p.q, (const float*)p.k, (const float*)p.v, (float*)p.o, p.lse, p.N, p.S, p.causal,
-      p.scale * kLog2e);
+      p.scale * kLog2e, p.work, split_from);
+  if (nsplit > 0 && (e = cudaGetLastError()) == cudaSuccess)
+    flash_merge_kernel<D><<<(unsigned)(nsplit * p.N), 256, 0, st>>>(p.work, (float*)p.o, p.lse, p.S, nsplit);
   return cudaGetLastError();
 }
 
@@ -726,6 +794,23 @@ cudaError_t launch_flash_f32(const AttnProblem& p, cudaStream_t st) {
 }
 
 size_t naive_workspace_bytes(int64_t N, int S) { return (size_t)N * (size_t)S * (size_t)S * sizeof(float); }
+
+bool flash_wants_split(int64_t N, int S, int causal) {
+  const int tiles = (S + kBR - 1) / kBR;
+  if (!causal || tiles < 4) return false;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  return N * tiles <= 2 * (int64_t)sms;
+}
+
+size_t flash_split_bytes(int64_t N, int S, int d) {
+  const int tiles = (S + kBR - 1) / kBR;
+  const int nsplit = tiles - (tiles + 1) / 2;
+  return (size_t)N * (size_t)nsplit * 2 * kBR * (size_t)(d + 2) * sizeof(float);
+}
 
 cudaError_t launch_naive_f32(const AttnProblem& p, float* scores, cudaStream_t st) {
   switch (p.d) {

@@ -23,6 +23,7 @@ struct AttnProblem {
   float scale;
   int dtype;
   float* lse = nullptr;  // optional [N, S] fp32 log-sum-exp of the score rows
+  float* work = nullptr;  // fp32 flash: the split tiles' partial states (null: no split)
 };
 
 // Launchers return a cudaError_t from the launch (or cudaSuccess).
@@ -30,6 +31,11 @@ cudaError_t launch_flash_f32(const AttnProblem& p, cudaStream_t st);
 cudaError_t launch_fused_f32(const AttnProblem& p, cudaStream_t st);
 cudaError_t launch_naive_f32(const AttnProblem& p, float* scores, cudaStream_t st);
 size_t naive_workspace_bytes(int64_t N, int S);
+// fp32 flash, causal: the heavier half of the query tiles is split over two blocks
+// when the grid is small (a single wave of blocks would otherwise wait on the
+// heaviest tile); these give the decision and the partial-state bytes it needs.
+bool flash_wants_split(int64_t N, int S, int causal);
+size_t flash_split_bytes(int64_t N, int S, int d);
 // 0 if the fused-row kernel can run S keys on the current device, else an error code.
 int fused_f32_check(int S, int d);
 

@@ -111,8 +111,17 @@ def test_valid_request_without_a_device_reports_no_device(lib):
 def test_naive_workspace_contract(lib):
     assert kbattn.kb_attn_workspace_bytes(1, 8, 1024, 64, DType.F32, Variant.NAIVE) == 8 * 1024 * 1024 * 4
     assert kbattn.kb_attn_workspace_bytes(2, 3, 5, 32, DType.F32, Variant.NAIVE) == 6 * 25 * 4
-    for v in (Variant.FLASH, Variant.FUSED, Variant.AUTO):
-        assert kbattn.kb_attn_workspace_bytes(1, 8, 1024, 64, DType.F32, v) == 0
+    assert kbattn.kb_attn_workspace_bytes(1, 8, 1024, 64, DType.F32, Variant.FUSED) == 0
+    # KB_AUTO picks the flash kernel for fp32 inputs, and so its workspace
+    assert (kbattn.kb_attn_workspace_bytes(1, 8, 1024, 64, DType.F32, Variant.AUTO) ==
+            kbattn.kb_attn_workspace_bytes(1, 8, 1024, 64, DType.F32, Variant.FLASH))
+    # fp32 flash: the partial states (m, l and 64 x d O values of 64 rows) of the
+    # two halves of its split causal query tiles, the heavier T - ceil(T / 2) of
+    # the T = ceil(S / 64) tiles of each head
+    for B, H, S, d in ((1, 8, 1024, 64), (2, 3, 300, 128), (1, 1, 64, 32)):
+        T = -(-S // 64)
+        want = B * H * (T - (T + 1) // 2) * 2 * 64 * (d + 2) * 4
+        assert kbattn.kb_attn_workspace_bytes(B, H, S, d, DType.F32, Variant.FLASH) == want
     assert kbattn.kb_attn_workspace_bytes(1, 8, 1024, 64, DType.BF16, Variant.TC) == 0
     assert kbattn.kb_attn_workspace_bytes(0, 8, 1024, 64, DType.F32, Variant.NAIVE) == 0
     # a score matrix too large to address is refused, never a wrapped-around size

@@ -123,3 +123,33 @@ def test_fused_four_rows_per_block_with_ragged_tails(oracle, shape):
     want = oracle.attn(*inputs.make_qkv(w), causal, w.scale)
     mx, mean, _ = errors(got, want)
     assert mx <= F32_TOL, (mx, mean)
+
+
+@pytest.mark.parametrize("shape", [(1, 8, 1024, 64), (1, 3, 700, 128), (2, 2, 333, 32)],
+                         ids=lambda s: "b{}h{}s{}d{}".format(*s))
+def test_flash_causal_split_paths(oracle, shape):
+    """Causal fp32 flash on a small grid runs the heavier half of its query tiles
+    as two blocks over two key ranges (partial states in a workspace, combined by
+    a merge kernel). The library's cached workspace and a caller's full workspace
+    give the same bits; a caller's too-small workspace runs every tile whole; all
+    three are within the fp32 tolerance of the oracle."""
+    B, H, S, d = shape
+    w = inputs.Workload("split", B, H, S, d, True, "f32", 500 + S, "uniform")
+    q, k, v = (t.cuda() for t in inputs.make_qkv(w))
+    want = oracle.attn(*inputs.make_qkv(w), True, w.scale)
+    nbytes = kbattn.kb_attn_workspace_bytes(B, H, S, d, kbattn.DType.F32, Variant.FLASH)
+    assert nbytes > 0
+    outs = []
+    for ws in (None, torch.empty(nbytes, dtype=torch.uint8, device="cuda"),
+               torch.empty(16, dtype=torch.uint8, device="cuda")):
+        g = Guarded(q.shape, torch.float32)
+        if ws is None:
+            kbattn.kb_attn_fwd(q, k, v, g.out, causal=True, scale=w.scale, variant=Variant.FLASH)
+        else:
+            kbattn.kb_attn_fwd_ws(q, k, v, g.out, ws, causal=True, scale=w.scale, variant=Variant.FLASH)
+        assert kbattn.kb_check_device_error() == kbattn.Status.OK
+        got = g.check()
+        mx, _, _ = errors(got.cpu().numpy(), want)
+        assert mx <= F32_TOL, mx
+        outs.append(got)
+    assert torch.equal(outs[0], outs[1])
