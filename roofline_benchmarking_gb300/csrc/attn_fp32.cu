@@ -489,24 +489,92 @@ __global__ void __launch_bounds__(kThreads) naive_softmax_kernel(float* __restri
 
 // naive pass 3: O = P V as a tiled GEMM over the visible key tiles. As in the
 // flash kernel, two groups of 256 threads take the even and the odd key tiles
-// with their own P and V buffers; group 0 adds group 1's partial sums.
+// with their own buffers, and group 0 adds group 1's partial sums. Each group
+// double-buffers its P and V tiles with cp.async; P stays row-major as the
+// softmax pass left it (16-byte copies when S is a multiple of 4, so that every
+// copied row segment is 16-byte aligned, else 4-byte copies), and the entries
+// above the diagonal of the causal diagonal tile (still -inf) are zeroed.
+constexpr int kLDP = kBC + 4;  // row stride of a P tile
+
+template <int D>
+__device__ __forceinline__ void naive_pv_issue(float* Pr, float* Vr, const float* Sh, const float* Vh, int q0, int k0,
+                                               int S, int tid, bool vec16) {
+  if (vec16) {
+    for (int f = tid; f < kBR * (kBC / 4); f += kThreads) {
+      const int r = f / (kBC / 4), c4 = f % (kBC / 4);
+      const int row = q0 + r, col = k0 + 4 * c4;
+      const bool ok = row < S && col < S;  // S % 4 == 0: a 4-key chunk is wholly in or out
+      cp_async<16>(Pr + r * kLDP + 4 * c4, Sh + (ok ? (int64_t)row * S + col : 0), ok);
+    }
+  } else {
+    for (int f = tid; f < kBR * kBC; f += kThreads) {
+      const int r = f / kBC, c = f % kBC;
+      const int row = q0 + r, col = k0 + c;
+      const bool ok = row < S && col < S;
+      cp_async<4>(Pr + r * kLDP + c, Sh + (ok ? (int64_t)row * S + col : 0), ok);
+    }
+  }
+  for (int f = tid; f < kBC * (D / 4); f += kThreads) {
+    const int r = f / (D / 4), c4 = f % (D / 4);
+    const bool ok = k0 + r < S;
+    cp_async<16>(Vr + r * D + 4 * c4, Vh + (int64_t)(ok ? k0 + r : 0) * D + 4 * c4, ok);
+  }
+}
+
+// acc[a][*] += sum_c P[ty*4+a][c] * V[c][col], P row-major (Pr[r * kLDP + c]), four keys per step.
+template <int D>
+__device__ __forceinline__ void pv_accumulate_rowp(float (&acc)[4][D / 16], const float* Pr, const float* Vs, int ty,
+                                                   int tx) {
+  using C = Cols<D>;
+#pragma unroll 2
+  for (int c = 0; c < kBC; c += 4) {
+    float4 p4[4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a) p4[a] = ld4(Pr + (ty * 4 + a) * kLDP + c);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float pr[4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) pr[a] = i == 0 ? p4[a].x : i == 1 ? p4[a].y : i == 2 ? p4[a].z : p4[a].w;
+#pragma unroll
+      for (int g = 0; g < C::G; ++g) {
+        float vv[C::W];
+        const float* vp = Vs + (c + i) * D + g * 16 * C::W + tx * C::W;
+        if constexpr (C::W == 4) {
+          const float4 t = ld4(vp);
+          vv[0] = t.x; vv[1] = t.y; vv[2] = t.z; vv[3] = t.w;
+        } else {
+          const float2 t = *reinterpret_cast<const float2*>(vp);
+          vv[0] = t.x; vv[1] = t.y;
+        }
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int e = 0; e < C::W; ++e) acc[a][g * C::W + e] = fmaf(pr[a], vv[e], acc[a][g * C::W + e]);
+      }
+    }
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kFlashThreads, 1) naive_pv_kernel(const float* __restrict__ Sc,
                                                                     const float* __restrict__ V,
                                                                     float* __restrict__ O, int64_t N, int S,
                                                                     int causal) {
   using C = Cols<D>;
-  constexpr int GROUP = kBC * kLD + kBC * D;  // floats of one group's P and V buffers
+  constexpr int BUF = kBR * kLDP + kBC * D;  // floats of one P + V buffer pair
+  constexpr int GROUP = 2 * BUF;              // a group's two buffer pairs
   extern __shared__ float4 smem4[];
   const int grp = threadIdx.x / kThreads, ltid = threadIdx.x % kThreads;
-  float* Ps = reinterpret_cast<float*>(smem4) + grp * GROUP;  // [kBC][kLD] (key-major)
-  float* Vs = Ps + kBC * kLD;                                  // [kBC][D]
+  float* B0 = reinterpret_cast<float*>(smem4) + grp * GROUP;  // buffer b: P [kBR][kLDP] at B0 + b BUF, V after it
   const int ntiles = (S + kBR - 1) / kBR;
   const int64_t n = blockIdx.x % N;
   const int qt = ntiles - 1 - (int)(blockIdx.x / N);
   const int q0 = qt * kBR;
   const int tx = ltid & 15, ty = ltid >> 4;
   const float* Sh = Sc + n * (int64_t)S * S;
+  const float* Vh = V + n * S * D;
+  const bool vec16 = (S & 3) == 0;
   float acc[4][D / 16];
 #pragma unroll
   for (int a = 0; a < 4; ++a)
@@ -514,20 +582,27 @@ __global__ void __launch_bounds__(kFlashThreads, 1) naive_pv_kernel(const float*
     for (int c = 0; c < D / 16; ++c) acc[a][c] = 0.f;
 
   const int kt_last = causal ? qt : ntiles - 1;
-  for (int kt = grp; kt <= kt_last; kt += 2) {
-    const int k0 = kt * kBC;
-    group_bar(grp);
-    // P tile, transposed to Ps[key][row]; masked and out-of-range entries are 0
-    for (int f = ltid; f < kBR * kBC; f += kThreads) {
-      const int key = f % kBC, r = f / kBC;
-      const int row = q0 + r, col = k0 + key;
-      float p = 0.f;
-      if (row < S && col < S && !(causal && col > row)) p = Sh[(int64_t)row * S + col];
-      Ps[key * kLD + r] = p;
+  if (grp <= kt_last) naive_pv_issue<D>(B0, B0 + kBR * kLDP, Sh, Vh, q0, grp * kBC, S, ltid, vec16);
+  cp_async_commit();
+  for (int kt = grp, it = 0; kt <= kt_last; kt += 2, ++it) {
+    float* Pr = B0 + (it & 1) * BUF;
+    float* Vs = Pr + kBR * kLDP;
+    group_bar(grp);  // the group's other buffer pair is no longer read
+    if (kt + 2 <= kt_last) {
+      float* Pn = B0 + ((it + 1) & 1) * BUF;
+      naive_pv_issue<D>(Pn, Pn + kBR * kLDP, Sh, Vh, q0, (kt + 2) * kBC, S, ltid, vec16);
     }
-    load_rows<D>(Vs, V + n * S * D, k0, S, ltid, kThreads);
+    cp_async_commit();
+    cp_async_wait<1>();  // this thread's copies of tile kt have landed
     group_bar(grp);
-    pv_accumulate<D>(acc, Ps, Vs, ty, tx, kBC);
+    if (causal && kt == qt) {  // the diagonal tile: keys after the row are masked
+      for (int f = ltid; f < kBR * kBC; f += kThreads) {
+        const int r = f / kBC, c = f % kBC;
+        if (c > r) Pr[r * kLDP + c] = 0.f;
+      }
+      group_bar(grp);
+    }
+    pv_accumulate_rowp<D>(acc, Pr, Vs, ty, tx);
   }
   float* X = reinterpret_cast<float*>(smem4) + GROUP;  // group 1's buffers hold its partial sums
   static_assert(4 * (D / 16) * kThreads <= GROUP, "partial sums fit in one group's buffers");
@@ -711,7 +786,7 @@ size_t flash_smem(int d) {
   return sizeof(float) * (size_t)(d * kLD + 2 * group);
 }
 size_t naive_scores_smem(int d) { return sizeof(float) * (size_t)(2 * d * kLD); }
-size_t naive_pv_smem(int d) { return sizeof(float) * (size_t)(2 * (kBC * kLD + kBC * d)); }
+size_t naive_pv_smem(int d) { return sizeof(float) * (size_t)(2 * 2 * (kBR * kLDP + kBC * d)); }
 size_t fused_smem(int S, int d, int rows = 1) {
   return sizeof(float) * (size_t)(kFusedKeys * (d + 16) + rows * d + kFusedWarps * rows + rows * kFusedThreads +
                                   (size_t)rows * S);
