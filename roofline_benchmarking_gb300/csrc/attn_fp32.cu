@@ -101,26 +101,6 @@ __device__ __forceinline__ void pv_accumulate(float (&acc)[4][D / 16], const flo
   }
 }
 
-// s[a][b] = sum_k Qs[k][ty*4+a] * Ks[k][tx*4+b] for the 64 x 64 tile.
-template <int D>
-__device__ __forceinline__ void qk_tile(float (&s)[4][4], const float* Qs, const float* Ks, int ty, int tx) {
-#pragma unroll
-  for (int a = 0; a < 4; ++a)
-#pragma unroll
-    for (int b = 0; b < 4; ++b) s[a][b] = 0.f;
-#pragma unroll 8
-  for (int k = 0; k < D; ++k) {
-    const float4 qa = ld4(Qs + k * kLD + ty * 4);
-    const float4 kb = ld4(Ks + k * kLD + tx * 4);
-    const float qv[4] = {qa.x, qa.y, qa.z, qa.w};
-    const float kv[4] = {kb.x, kb.y, kb.z, kb.w};
-#pragma unroll
-    for (int a = 0; a < 4; ++a)
-#pragma unroll
-      for (int b = 0; b < 4; ++b) s[a][b] = fmaf(qv[a], kv[b], s[a][b]);
-  }
-}
-
 // ---------------------------------------------------------------------------
 // flash: one block per (head, 64-row query tile); grid.x = tiles * N with the
 // heaviest causal tiles scheduled first. The block's 512 threads form two
@@ -436,20 +416,25 @@ __global__ void __launch_bounds__(kThreads) naive_scores_kernel(const float* __r
                                                                 float* __restrict__ Sc, int64_t N, int S,
                                                                 int causal, float scale) {
   extern __shared__ float4 smem4[];
-  float* Qs = reinterpret_cast<float*>(smem4);  // [D][kLD]
-  float* Ks = Qs + D * kLD;                      // [D][kLD]
-  const int ntiles = (S + kBR - 1) / kBR;
+  constexpr int LDK = flash_ldk<D>();
+  float* Qs = reinterpret_cast<float*>(smem4);  // [D][kLD] (transposed)
+  float* Ks = Qs + D * kLD;                      // [kBC][D + 4] (row-major)
   const int kt = blockIdx.x, qt = blockIdx.y;
   const int64_t n = blockIdx.z;
   if (causal && kt > qt) return;
   const int q0 = qt * kBR, k0 = kt * kBC;
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
-  (void)ntiles;
   load_transposed<D>(Qs, Q + n * S * D, q0, S, scale);
-  load_transposed<D>(Ks, K + n * S * D, k0, S, 1.0f);
+  const float* Kh = K + n * S * D;
+  for (int f = tid; f < kBC * (D / 4); f += kThreads) {  // coalesced 16-byte loads; rows >= S read as 0
+    const int r = f / (D / 4), c4 = f % (D / 4);
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (k0 + r < S) x = ld4(Kh + (int64_t)(k0 + r) * D + 4 * c4);
+    *reinterpret_cast<float4*>(Ks + r * LDK + 4 * c4) = x;
+  }
   __syncthreads();
   float s[4][4];
-  qk_tile<D>(s, Qs, Ks, ty, tx);
+  qk_tile_rowk<D>(s, Qs, Ks, ty, tx);  // the thread's keys: tx, tx + 16, tx + 32, tx + 48
   float* Sh = Sc + n * (int64_t)S * S;
 #pragma unroll
   for (int a = 0; a < 4; ++a) {
@@ -457,7 +442,7 @@ __global__ void __launch_bounds__(kThreads) naive_scores_kernel(const float* __r
     if (row >= S) continue;
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
-      const int key = k0 + tx * 4 + b;
+      const int key = k0 + tx + 16 * b;
       if (key >= S) continue;
       Sh[(int64_t)row * S + key] = (causal && key > row) ? -INFINITY : s[a][b];
     }
@@ -785,7 +770,7 @@ size_t flash_smem(int d) {
   const int group = d == 32 ? flash_group_floats<32>() : d == 64 ? flash_group_floats<64>() : flash_group_floats<128>();
   return sizeof(float) * (size_t)(d * kLD + 2 * group);
 }
-size_t naive_scores_smem(int d) { return sizeof(float) * (size_t)(2 * d * kLD); }
+size_t naive_scores_smem(int d) { return sizeof(float) * (size_t)(d * kLD + kBC * (d + 4)); }
 size_t naive_pv_smem(int d) { return sizeof(float) * (size_t)(2 * 2 * (kBR * kLDP + kBC * d)); }
 size_t fused_smem(int S, int d, int rows = 1) {
   return sizeof(float) * (size_t)(kFusedKeys * (d + 16) + rows * d + kFusedWarps * rows + rows * kFusedThreads +
