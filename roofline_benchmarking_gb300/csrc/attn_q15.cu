@@ -134,8 +134,11 @@ __global__ void __launch_bounds__(8 * ROWS) q15_attn_kernel(const short* __restr
 
   const int tid = threadIdx.x;
   const int r = tid >> 3, g = tid & 7;
-  const long long n = blockIdx.x / tiles_per_head;
-  const int i0 = (int)(blockIdx.x % tiles_per_head) * ROWS;
+  // heads interleaved, the last (causal: heaviest) row tiles first, so that the
+  // lightest blocks fill the last wave
+  const long long nheads = gridDim.x / tiles_per_head;
+  const long long n = blockIdx.x % nheads;
+  const int i0 = (tiles_per_head - 1 - (int)(blockIdx.x / nheads)) * ROWS;
   const int i = i0 + r;
   const short* Qh = Q + n * S * D;
   const short* Kg = K + n * S * D;
