@@ -672,8 +672,10 @@ __global__ void __launch_bounds__(kFusedThreads) fused_row_f32_kernel(const floa
   float* part = red + kFusedWarps * R;           // [R][kFusedThreads]
   float* sc = part + R * kFusedThreads;          // [R][S]
   const int tiles = (S + R - 1) / R;
-  const int64_t n = blockIdx.x / tiles;
-  const int i0 = (int)(blockIdx.x % tiles) * R;
+  // heads interleaved, the last (causal: heaviest) row tiles first
+  const int64_t nheads = gridDim.x / tiles;
+  const int64_t n = blockIdx.x % nheads;
+  const int i0 = (tiles - 1 - (int)(blockIdx.x / nheads)) * R;
   const int tid = threadIdx.x;
   const int last_block = causal ? min(i0 + R - 1, S - 1) : S - 1;  // keys any row of the block sees
   const float* Kh = K + n * S * D;
