@@ -151,6 +151,23 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   }
 }
 
+// Sixteen fp32 values of one O row, times inv, rounded to 16 bits and stored at
+// dst: one 32-byte store (a whole L2 sector) when the output base is 32-byte
+// aligned (st32; every row and chunk offset is a multiple of 32 bytes), else two
+// 16-byte stores.
+template <bool F16>
+__device__ __forceinline__ void store_o16(uint8_t* dst, const uint32_t* u, float inv, bool st32) {
+  uint32_t w[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) w[e] = pack2<F16>(__uint_as_float(u[2 * e]) * inv, __uint_as_float(u[2 * e + 1]) * inv);
+  if (st32) {
+    ptx::st_global_v8(dst, w);
+  } else {
+    *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4*>(dst + 16) = make_uint4(w[4], w[5], w[6], w[7]);
+  }
+}
+
 // Per-CTA work lists built on the host (passed by value as a kernel parameter):
 // CTA c runs units item[start[c]], item[start[c] + 1], ... < start[c + 1], an
 // entry holding head << 16 | unit. The lists come from list scheduling over
@@ -508,6 +525,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         // natural log of sum_j exp(score): the scores sum to 2^m_run * l_run in base 2
         if (lse != nullptr && row < S) lse[(size_t)it.n * S + row] = (m_run + log2f(l_run)) * 0.6931471805599453f;
         uint8_t* orow = out + ((size_t)it.n * S + row) * (size_t)dout * 2;
+        const bool st32 = (reinterpret_cast<uintptr_t>(out) & 31) == 0;
         // the whole O row in one round trip to TMEM (the score registers are free by now);
         // then the accumulator may take the next item while this one is scaled and stored
         uint32_t u[D / 32][32];
@@ -519,15 +537,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
 #pragma unroll
         for (int cb = 0; cb < D / 32; ++cb) {
           if (row < S && cb * 32 < dout) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              uint4 w;
-              w.x = pack2<F16>(__uint_as_float(u[cb][q * 8 + 0]) * inv, __uint_as_float(u[cb][q * 8 + 1]) * inv);
-              w.y = pack2<F16>(__uint_as_float(u[cb][q * 8 + 2]) * inv, __uint_as_float(u[cb][q * 8 + 3]) * inv);
-              w.z = pack2<F16>(__uint_as_float(u[cb][q * 8 + 4]) * inv, __uint_as_float(u[cb][q * 8 + 5]) * inv);
-              w.w = pack2<F16>(__uint_as_float(u[cb][q * 8 + 6]) * inv, __uint_as_float(u[cb][q * 8 + 7]) * inv);
-              *reinterpret_cast<uint4*>(orow + cb * 64 + q * 16) = w;
-            }
+            store_o16<F16>(orow + cb * 64, &u[cb][0], inv, st32);
+            store_o16<F16>(orow + cb * 64 + 32, &u[cb][16], inv, st32);
           }
         }
       }
@@ -907,6 +918,7 @@ __global__ void __launch_bounds__(kThreads256, 1)
         const float inv = 1.0f / l_run;
         if (lse != nullptr && row < S) lse[(size_t)it.n * S + row] = (m_run + log2f(l_run)) * 0.6931471805599453f;
         uint8_t* orow = out + ((size_t)it.n * S + row) * (size_t)C::D * 2;
+        const bool st32 = (reinterpret_cast<uintptr_t>(out) & 31) == 0;
         uint32_t u[32];
 #pragma unroll 1
         for (int cb = 0; cb < C::D / 32; ++cb) {
@@ -917,15 +929,8 @@ __global__ void __launch_bounds__(kThreads256, 1)
             ptx::mbar_arrive(bar(C::B_OFREE));
           }
           if (row < S) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              uint4 w;
-              w.x = pack2<F16>(__uint_as_float(u[q * 8 + 0]) * inv, __uint_as_float(u[q * 8 + 1]) * inv);
-              w.y = pack2<F16>(__uint_as_float(u[q * 8 + 2]) * inv, __uint_as_float(u[q * 8 + 3]) * inv);
-              w.z = pack2<F16>(__uint_as_float(u[q * 8 + 4]) * inv, __uint_as_float(u[q * 8 + 5]) * inv);
-              w.w = pack2<F16>(__uint_as_float(u[q * 8 + 6]) * inv, __uint_as_float(u[q * 8 + 7]) * inv);
-              *reinterpret_cast<uint4*>(orow + cb * 64 + q * 16) = w;
-            }
+            store_o16<F16>(orow + cb * 64, &u[0], inv, st32);
+            store_o16<F16>(orow + cb * 64 + 32, &u[16], inv, st32);
           }
         }
       }

@@ -242,5 +242,13 @@ __host__ __device__ constexpr uint32_t f16_idesc(uint32_t M, uint32_t N, uint32_
   return (1u << 4) | (ab_type << 7) | (ab_type << 10) | (b_mn_major << 16) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
+// One 32-byte global store (eight 32-bit words): a whole L2 sector per thread.
+// The address must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t (&w)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
+               "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
 }  // namespace ptx
 }  // namespace kb

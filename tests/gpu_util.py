@@ -12,19 +12,22 @@ class Guarded:
     value is legal, completeness is checked by writing twice into buffers with
     different poisons (see ``run_twice``)."""
 
-    def __init__(self, shape, dtype, device="cuda", poison=0x5A5A):
+    def __init__(self, shape, dtype, device="cuda", poison=0x5A5A, lead=0):
+        """``lead`` extra poisoned elements before the output move its base
+        address off the buffer's (256-byte aligned) allocation."""
         n = int(np.prod(shape))
         self.is_float = dtype.is_floating_point
         fill = float("nan") if self.is_float else poison
         self.poison = fill
-        self.buf = torch.full((CANARY + n + CANARY,), fill, dtype=dtype, device=device)
+        self.buf = torch.full((CANARY + lead + n + CANARY,), fill, dtype=dtype, device=device)
         self.n = n
-        self.out = self.buf[CANARY:CANARY + n].view(*shape)
+        self.start = CANARY + lead
+        self.out = self.buf[self.start:self.start + n].view(*shape)
 
     def check(self):
         torch.cuda.synchronize()
-        head = self.buf[:CANARY]
-        tail = self.buf[CANARY + self.n:]
+        head = self.buf[:self.start]
+        tail = self.buf[self.start + self.n:]
         if self.is_float:
             assert torch.isnan(head).all() and torch.isnan(tail).all(), "write outside the output tensor"
             assert not torch.isnan(self.out).any(), "part of the output was not written"

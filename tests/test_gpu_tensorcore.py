@@ -119,6 +119,25 @@ def test_repeat_calls_are_deterministic(d):
     assert torch.equal(a, b)
 
 
+@pytest.mark.parametrize("d,dtype", [(32, "bf16"), (64, "f16"), (128, "bf16"), (256, "bf16")])
+def test_output_base_aligned_to_16_bytes_only(oracle, d, dtype):
+    """The epilogue writes 32 bytes per store when the output base is 32-byte
+    aligned and two 16-byte stores when it is only 16-byte aligned (what the
+    boundary accepts): the second path gives the same bits, in place."""
+    w = inputs.Workload("t", 1, 2, 300, d, True, dtype, 41 + d, "normal")
+    q, k, v = inputs.make_qkv(w)
+    wide = run_tc(q, k, v, w.causal, w.scale)
+    assert wide.data_ptr() % 32 == 0
+    g = Guarded(q.shape, q.dtype, lead=8)  # 8 elements of 2 bytes
+    assert g.out.data_ptr() % 32 == 16
+    kbattn.kb_attn_fwd(q.cuda(), k.cuda(), v.cuda(), g.out, causal=w.causal, scale=w.scale, variant=Variant.TC)
+    assert kbattn.kb_check_device_error() == kbattn.Status.OK
+    narrow = g.check()
+    assert torch.equal(narrow, wide)
+    mx, mean, _ = errors(narrow.float().cpu().numpy(), oracle.attn(q, k, v, w.causal, w.scale))
+    assert mx <= MAX_TOL and mean <= MEAN_TOL, (mx, mean)
+
+
 def test_tc_rejects_unsupported_head_dim():
     st = kbattn.kb_attn_fwd_ptr(1 << 20, 1 << 20, 1 << 20, 1 << 20, 1, 1, 128, 96, False, 0.17,
                                 kbattn.DType.BF16, Variant.TC, 0)
