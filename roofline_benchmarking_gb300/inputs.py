@@ -114,6 +114,28 @@ def make_qkv(w: Workload):
     return tuple(out)
 
 
+def make_qkv_device(w: Workload, device: str = "cuda"):
+    """Q, K, V for workload ``w`` drawn directly on ``device`` with that device's
+    generator seeded by ``w.seed``: the same distributions and storage rounding
+    as ``make_qkv`` (other values: another generator), for problems whose fp32
+    draws would not fit comfortably in host memory."""
+    g = torch.Generator(device=device)
+    g.manual_seed(w.seed)
+    shape = (w.B, w.H, w.S, w.d)
+    out = []
+    for which in ("q", "k", "v"):
+        if w.dist == "uniform":
+            x = torch.rand(shape, generator=g, device=device, dtype=torch.float32).mul_(2.0).sub_(1.0)
+        elif w.dist == "normal":
+            sigma = w.sigma_v if which == "v" else w.sigma_qk
+            x = torch.randn(shape, generator=g, device=device, dtype=torch.float32).mul_(sigma)
+        else:
+            raise ValueError(f"unknown distribution {w.dist!r}")
+        out.append(to_q15(x) if w.dtype == "q15" else x.to(torch_dtype(w.dtype)).contiguous())
+        del x
+    return tuple(out)
+
+
 def to_q15(x: torch.Tensor) -> torch.Tensor:
     """Storage rounding to Q15: round(x * 2^15) (ties to even), saturated to int16."""
     return torch.round(x.float() * 32768.0).clamp(-32768, 32767).to(torch.int16).contiguous()
