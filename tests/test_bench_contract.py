@@ -1,0 +1,62 @@
+"""The benchmark's one-line JSON contract: every key the driver reads, with
+the types and units it expects, for the reference arm (the oracle on the host
+cores; runs on CPU) and for the library's own arm (GPU)."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+BASE_KEYS = {"metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+             "scaling", "vs_baseline", "dtype", "data", "config"}
+
+
+def run_bench(*args, timeout=600):
+    r = subprocess.run([sys.executable, "bench.py", *args], cwd=ROOT, capture_output=True, text=True,
+                       timeout=timeout)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1, r.stdout[-2000:]  # exactly one line on stdout
+    return json.loads(lines[0])
+
+
+def check_common(line, steps, warmup, dtype):
+    assert BASE_KEYS <= set(line), BASE_KEYS - set(line)
+    assert line["steps"] == steps and line["warmup"] == warmup and line["n_gpus"] == 1
+    assert line["unit"] == "TFLOP/s" and line["higher_is_better"] is True and line["scaling"] == "weak"
+    assert line["value"] > 0 and line["ms_per_step"] > 0
+    assert line["config"]["workload"] == "bf16_causal_b4h16s4096d128"
+    assert line["dtype"] == dtype and line["data"] == "synthetic"  # the arithmetic type of the arm
+
+
+def test_reference_arm_line():
+    line = run_bench("--impl", "reference", "--steps", "2", "--warmup", "1", "--reference-seconds", "1.5")
+    check_common(line, 2, 1, "f64")
+    assert line["impl"] == "reference"
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"] and cb["sample"]
+    e2e = line["e2e"]
+    assert e2e["value"] == line["value"] and e2e["unit"] == line["unit"]
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+@pytest.mark.gpu
+def test_library_arm_line():
+    line = run_bench("--steps", "5", "--warmup", "3", "--e2e-steps", "3", "--cpu-seconds", "1", "--no-triad")
+    check_common(line, 5, 3, "bf16")
+    assert line.get("impl", "ours") != "reference"
+    r = line["roofline"]
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s" and r["peak"] > 0
+    assert r["achieved"] > 0 and abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-9
+    assert r["traffic"] is None or r["traffic"] > 0
+    c = line["clocks"]
+    assert c["sm_max_mhz"] > 0 and isinstance(c["reasons"], list)
+    assert line["gpu_launches"] >= 5
+    e2e = line["e2e"]
+    assert e2e["value"] > 0 and e2e["unit"] == "TFLOP/s"
+    assert e2e["h2d_bytes_per_step"] == 3 * 4 * 16 * 4096 * 128 * 2  # Q, K, V in bf16
+    assert e2e["d2h_bytes_per_step"] == 4 * 16 * 4096 * 128 * 2      # O
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] > 0
