@@ -84,7 +84,14 @@ struct TcCfg {
   static constexpr int OFF_Q = 0;              // Q_A then Q_B
   static constexpr int OFF_K = OFF_Q + 2 * TILE;
   static constexpr int OFF_V = OFF_K + KS * TILE;
-  static constexpr int OFF_BAR = OFF_V + VS * TILE;
+  // d = 128: output staging of the eight softmax warps, 32 rows x 64 columns each,
+  // in the 128-byte swizzled layout of the output tensor map's boxes (TMA stores).
+  // d = 64 stores O from registers (measured faster there: its smaller K/V loads
+  // come more often and would share the TMA unit with the stores).
+  static constexpr bool TMA_STORE = D == 128;
+  static constexpr int STG = 32 * 64 * 2;
+  static constexpr int OFF_O = OFF_V + VS * TILE;
+  static constexpr int OFF_BAR = OFF_O + (TMA_STORE ? 8 * STG : 0);
   enum {
     B_Q = 0,
     B_KFULL = 1,
@@ -102,6 +109,7 @@ struct TcCfg {
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // [0] TMEM base, [1] abort flag
   static constexpr int BYTES = OFF_MISC + 16;
   static constexpr int SMEM = BYTES + 1024;  // slack to align the base to 1024 bytes
+  static_assert(SMEM <= 232448, "at most 227 KB of shared memory per CTA");
   // TMEM columns of tile g: S (and P in its first 64 columns) at 128 g, O at 256 + 128 g.
   __host__ __device__ static constexpr uint32_t tm_s(int g) { return 128u * (uint32_t)g; }
   __host__ __device__ static constexpr uint32_t tm_o(int g) { return 256u + 128u * (uint32_t)g; }
@@ -229,7 +237,8 @@ struct Schedule {
 template <int D, bool F16>
 __global__ void __launch_bounds__(kThreadsTC, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                   const __grid_constant__ CUtensorMap tmv, const __grid_constant__ SchedTable tab,
+                   const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo,
+                   const __grid_constant__ SchedTable tab,
                    uint8_t* __restrict__ out, float* __restrict__ lse, int dout, int N, int S, int causal,
                    float scale_log2, unsigned long long limit) {
   // dout: output columns per row (D, or 32 when a d = 32 problem runs on the 64-wide kernel
@@ -287,6 +296,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         ptx::tma_prefetch_desc(&tmq);
         ptx::tma_prefetch_desc(&tmk);
         ptx::tma_prefetch_desc(&tmv);
+        ptx::tma_prefetch_desc(&tmo);
         int kdone = 0, vdone = 0, items = 0;  // K tiles, V tiles and items whose loads were issued
         bool ok = true;
         Item it;
@@ -524,8 +534,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         const float inv = 1.0f / l_run;
         // natural log of sum_j exp(score): the scores sum to 2^m_run * l_run in base 2
         if (lse != nullptr && row < S) lse[(size_t)it.n * S + row] = (m_run + log2f(l_run)) * 0.6931471805599453f;
-        uint8_t* orow = out + ((size_t)it.n * S + row) * (size_t)dout * 2;
-        const bool st32 = (reinterpret_cast<uintptr_t>(out) & 31) == 0;
         // the whole O row in one round trip to TMEM (the score registers are free by now);
         // then the accumulator may take the next item while this one is scaled and stored
         uint32_t u[D / 32][32];
@@ -534,15 +542,46 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         ptx::tmem_wait_ld();
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar(C::B_OFREE + g));
+        if constexpr (!C::TMA_STORE) {
+          uint8_t* orow = out + ((size_t)it.n * S + row) * (size_t)dout * 2;
+          const bool st32 = (reinterpret_cast<uintptr_t>(out) & 31) == 0;
 #pragma unroll
-        for (int cb = 0; cb < D / 32; ++cb) {
-          if (row < S && cb * 32 < dout) {
-            store_o16<F16>(orow + cb * 64, &u[cb][0], inv, st32);
-            store_o16<F16>(orow + cb * 64 + 32, &u[cb][16], inv, st32);
+          for (int cb = 0; cb < D / 32; ++cb) {
+            if (row < S && cb * 32 < dout) {
+              store_o16<F16>(orow + cb * 64, &u[cb][0], inv, st32);
+              store_o16<F16>(orow + cb * 64 + 32, &u[cb][16], inv, st32);
+            }
+          }
+        } else {
+          // O / l, rounded to 16 bits, through this warp's staging buffer: one TMA store
+          // per 64 columns of its 32 rows. Rows past S and columns past dout lie outside
+          // the output tensor and are not written.
+          const uint32_t stg = base + C::OFF_O + (uint32_t)warp * C::STG;
+          const int y0 = it.q0 + g * kBM + wq * 32;  // first row of this warp (warp-uniform)
+#pragma unroll
+          for (int h = 0; h < (y0 < S ? D / 64 : 0); ++h) {
+            if (lane == 0) ptx::bulk_wait_read_all();  // the buffer's previous store has read it
+            __syncwarp();
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {  // 16-byte chunk c of the row, at chunk c ^ (row % 8)
+              const uint32_t* v = &u[2 * h + c / 4][(c % 4) * 8];
+              ptx::st_shared_v4(stg + (uint32_t)lane * 128u + ((uint32_t)(c ^ (lane & 7)) << 4),
+                                pack2<F16>(__uint_as_float(v[0]) * inv, __uint_as_float(v[1]) * inv),
+                                pack2<F16>(__uint_as_float(v[2]) * inv, __uint_as_float(v[3]) * inv),
+                                pack2<F16>(__uint_as_float(v[4]) * inv, __uint_as_float(v[5]) * inv),
+                                pack2<F16>(__uint_as_float(v[6]) * inv, __uint_as_float(v[7]) * inv));
+            }
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              ptx::tma_store_3d(&tmo, stg, h * 64, y0, it.n);
+              ptx::bulk_commit();
+            }
           }
         }
       }
     }
+    if (C::TMA_STORE && lane == 0) ptx::bulk_wait_all();  // this warp's output stores are complete
   }
 
   ptx::tc_fence_before();
@@ -1063,8 +1102,9 @@ cudaError_t tc_launch(const AttnProblem& p, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   const int dreal = p.d;  // D, or 32 with D = 64
   CUtensorMap mq, mk, mv;
+  CUtensorMap mo;  // output boxes: 64 columns x the 32 rows of one softmax warp
   if (!make_map(&mq, p.q, p.N, p.S, dreal, F16) || !make_map(&mk, p.k, p.N, p.S, dreal, F16) ||
-      !make_map(&mv, p.v, p.N, p.S, dreal, F16))
+      !make_map(&mv, p.v, p.N, p.S, dreal, F16) || !make_map(&mo, p.o, p.N, p.S, dreal, F16, 32))
     return cudaErrorInvalidValue;
   int dev = 0, sms = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
@@ -1075,7 +1115,7 @@ cudaError_t tc_launch(const AttnProblem& p, cudaStream_t st) {
   const SchedTable tab = sched_table(p.N, units, (p.S + kBN - 1) / kBN, p.causal != 0, (int)grid,
                                      2.0 * p.S * dreal * 2.0);
   attn_tc_kernel<D, F16><<<(unsigned)grid, kThreadsTC, C::SMEM, st>>>(
-      mq, mk, mv, tab, static_cast<uint8_t*>(p.o), p.lse, dreal, (int)p.N, p.S, p.causal,
+      mq, mk, mv, mo, tab, static_cast<uint8_t*>(p.o), p.lse, dreal, (int)p.N, p.S, p.causal,
       p.scale * 1.4426950408889634f, kDefaultWaitLimitNs);
   return cudaGetLastError();
 }
