@@ -621,7 +621,11 @@ struct Tc256 {
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + QTILE;
   static constexpr int OFF_V = OFF_K + KS * KTILE;
-  static constexpr int OFF_BAR = OFF_V + VS * KTILE;
+  // output staging: two 32-row x 64-column buffers per softmax warp, in the
+  // 128-byte swizzled layout of the output tensor map's boxes (TMA stores)
+  static constexpr int STG = 32 * 64 * 2;
+  static constexpr int OFF_O = OFF_V + VS * KTILE;
+  static constexpr int OFF_BAR = OFF_O + 4 * 2 * STG;
   enum {
     B_Q = 0,
     B_KFULL = 1,
@@ -640,6 +644,7 @@ struct Tc256 {
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_MISC + 16;
   static constexpr int SMEM = BYTES + 1024;
+  static_assert(SMEM <= 232448, "at most 227 KB of shared memory per CTA");
   static constexpr uint32_t TM_O = 256;  // O in columns 256-511; score buffer b in 64 b .. 64 b + 63
 };
 
@@ -683,7 +688,8 @@ struct Schedule256 {
 template <bool F16>
 __global__ void __launch_bounds__(kThreads256, 1)
     attn_tc256_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                      const __grid_constant__ CUtensorMap tmv, const __grid_constant__ SchedTable tab,
+                      const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo,
+                      const __grid_constant__ SchedTable tab,
                       uint8_t* __restrict__ out, float* __restrict__ lse, int N, int S, int causal,
                       float scale_log2, unsigned long long limit) {
   using C = Tc256;
@@ -767,6 +773,7 @@ __global__ void __launch_bounds__(kThreads256, 1)
     // ------------------------------------------------------------ TMA producer: V
     if (lane == 0) {
       ptx::tma_prefetch_desc(&tmv);
+      ptx::tma_prefetch_desc(&tmo);
       int vdone = 0;
       bool ok = true;
       Item256 it;
@@ -956,24 +963,43 @@ __global__ void __launch_bounds__(kThreads256, 1)
         ptx::tc_fence_after();
         const float inv = 1.0f / l_run;
         if (lse != nullptr && row < S) lse[(size_t)it.n * S + row] = (m_run + log2f(l_run)) * 0.6931471805599453f;
-        uint8_t* orow = out + ((size_t)it.n * S + row) * (size_t)C::D * 2;
-        const bool st32 = (reinterpret_cast<uintptr_t>(out) & 31) == 0;
-        uint32_t u[32];
+        // O / l, rounded to 16 bits, 64 columns at a time through this warp's two
+        // staging buffers (alternating), one TMA store each; rows past S lie outside
+        // the output tensor and are not written.
+        const int y0 = it.q0 + warp * 32;  // first row of this warp (warp-uniform)
+        uint32_t u[2][32];
 #pragma unroll 1
-        for (int cb = 0; cb < C::D / 32; ++cb) {
-          ptx::tmem_ld32(to + cb * 32, u);
+        for (int h = 0; h < C::D / 64; ++h) {
+          ptx::tmem_ld32(to + h * 64, u[0]);
+          ptx::tmem_ld32(to + h * 64 + 32, u[1]);
           ptx::tmem_wait_ld();
-          if (cb == C::D / 32 - 1) {
+          if (h == C::D / 64 - 1) {
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar(C::B_OFREE));
           }
-          if (row < S) {
-            store_o16<F16>(orow + cb * 64, &u[0], inv, st32);
-            store_o16<F16>(orow + cb * 64 + 32, &u[16], inv, st32);
+          if (y0 >= S) continue;
+          const uint32_t stg = base + C::OFF_O + (uint32_t)(warp * 2 + (h & 1)) * C::STG;
+          if (lane == 0) ptx::bulk_wait_read_1();  // the store that last used this buffer has read it
+          __syncwarp();
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {  // 16-byte chunk c of the row, at chunk c ^ (row % 8)
+            const uint32_t* v = &u[c / 4][(c % 4) * 8];
+            ptx::st_shared_v4(stg + (uint32_t)lane * 128u + ((uint32_t)(c ^ (lane & 7)) << 4),
+                              pack2<F16>(__uint_as_float(v[0]) * inv, __uint_as_float(v[1]) * inv),
+                              pack2<F16>(__uint_as_float(v[2]) * inv, __uint_as_float(v[3]) * inv),
+                              pack2<F16>(__uint_as_float(v[4]) * inv, __uint_as_float(v[5]) * inv),
+                              pack2<F16>(__uint_as_float(v[6]) * inv, __uint_as_float(v[7]) * inv));
+          }
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            ptx::tma_store_3d(&tmo, stg, h * 64, y0, it.n);
+            ptx::bulk_commit();
           }
         }
       }
     }
+    if (lane == 0) ptx::bulk_wait_all();  // this warp's output stores are complete
   }
 
   ptx::tc_fence_before();
@@ -1126,8 +1152,9 @@ cudaError_t tc256_launch(const AttnProblem& p, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(attn_tc256_kernel<F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   CUtensorMap mq, mk, mv;
+  CUtensorMap mo;  // output boxes: 64 columns x the 32 rows of one softmax warp
   if (!make_map(&mq, p.q, p.N, p.S, C::D, F16, kBM) || !make_map(&mk, p.k, p.N, p.S, C::D, F16, kBN256) ||
-      !make_map(&mv, p.v, p.N, p.S, C::D, F16, kBN256))
+      !make_map(&mv, p.v, p.N, p.S, C::D, F16, kBN256) || !make_map(&mo, p.o, p.N, p.S, C::D, F16, 32))
     return cudaErrorInvalidValue;
   int dev = 0, sms = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
@@ -1138,7 +1165,7 @@ cudaError_t tc256_launch(const AttnProblem& p, cudaStream_t st) {
   const SchedTable tab = sched_table(p.N, units, (p.S + kBN256 - 1) / kBN256, p.causal != 0, (int)grid,
                                      2.0 * p.S * C::D * 2.0);
   attn_tc256_kernel<F16><<<(unsigned)grid, kThreads256, C::SMEM, st>>>(
-      mq, mk, mv, tab, static_cast<uint8_t*>(p.o), p.lse, (int)p.N, p.S, p.causal, p.scale * 1.4426950408889634f,
+      mq, mk, mv, mo, tab, static_cast<uint8_t*>(p.o), p.lse, (int)p.N, p.S, p.causal, p.scale * 1.4426950408889634f,
       kDefaultWaitLimitNs);
   return cudaGetLastError();
 }
