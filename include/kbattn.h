@@ -122,7 +122,8 @@ typedef struct {
  *   q, k, v : const device pointers, [B, H, S, d] of `dtype`
  *   o       : device pointer, [B, H, S, d] of `dtype`, written in full
  *             (bf16/f16 outputs are rounded to nearest even from fp32)
- *   B, H, S : >= 1; B*H*S*d must fit in int64 and B*H in int32
+ *   B, H, S : >= 1; B*H*S*d must fit in int64 and B*H in int32;
+ *             S <= 2^31 - 257 (longer -> KB_ERR_UNSUPPORTED)
  *   d       : head dimension: 32, 64 or 128, and 256 for KB_TC (others -> UNSUPPORTED)
  *   causal  : 0 or 1
  *   scale   : finite and > 0 (callers normally pass 1/sqrt(d))
@@ -157,6 +158,30 @@ KB_API int kb_attn_fwd(const void* q, const void* k, const void* v, void* o,
 KB_API int kb_attn_fwd_lse(const void* q, const void* k, const void* v, void* o, float* lse,
                            int B, int H, int S, int d, int causal, float scale,
                            int dtype, int variant, void* stream);
+
+/*
+ * kb_attn_fwd_host -- kb_attn_fwd from host memory to host memory: on
+ * `stream`, copies Q, K and V from the host buffers into the caller's device
+ * buffers, runs the forward pass there, and copies O back into o_host (the
+ * kbench page's launch layer keeps these copies outside its timed window; this
+ * call is the whole round trip a host caller makes).
+ *   q_host, k_host, v_host : host pointers, [B, H, S, d] of `dtype`, read
+ *   o_host  : host pointer, [B, H, S, d] of `dtype`, written
+ *   q_dev, k_dev, v_dev, o_dev : device pointers as in kb_attn_fwd (the
+ *             caller's staging buffers; overwritten)
+ *   others  : as kb_attn_fwd
+ * Asynchronous: o_host holds the result once `stream` reaches the end of the
+ * call. Page-locked host buffers let the copies run asynchronously and overlap
+ * other streams' work; with pageable buffers the CUDA runtime may stage them and
+ * block the calling thread. The host buffers must stay valid until then.
+ * Validation, workspace and errors are those of kb_attn_fwd (plus
+ * KB_ERR_INVALID_ARG for a null host pointer); copies are issued only after
+ * the arguments have been validated.
+ */
+KB_API int kb_attn_fwd_host(const void* q_host, const void* k_host, const void* v_host, void* o_host,
+                            void* q_dev, void* k_dev, void* v_dev, void* o_dev,
+                            int B, int H, int S, int d, int causal, float scale,
+                            int dtype, int variant, void* stream);
 
 /* Workspace bytes kb_attn_fwd_ws uses: KB_NAIVE's N*S*S*4 score matrix; for
  * KB_FLASH, the partial states of its split causal query tiles (the heavier
@@ -272,8 +297,11 @@ KB_API int kb_selftest_timeout(unsigned long long limit_ns, void* stream);
 
 /*
  * Size in bytes of the library-owned score array of kb_attn_fwd_naive_noalloc:
- * 32 MiB, i.e. N*S*S <= 8388608 (for example 8 heads at S = 1024). Every GPU
- * that loads the library holds this array until the process exits.
+ * 32 MiB, i.e. N*S*S <= 8388608 (for example 8 heads at S = 1024). A GPU holds
+ * this array from the moment the library's module is loaded there until the
+ * process exits: under CUDA's default lazy module loading that is the first
+ * kb_attn_fwd_naive_noalloc call on that GPU (with CUDA_MODULE_LOADING=EAGER,
+ * the library's load).
  */
 #define KB_NAIVE_NOALLOC_MAX_BYTES (32u * 1024u * 1024u)
 
@@ -290,11 +318,16 @@ KB_API int kb_selftest_timeout(unsigned long long limit_ns, void* stream);
  * Returns KB_ERR_NO_MEMORY, before any device work, when N*S*S*4 bytes exceed
  * KB_NAIVE_NOALLOC_MAX_BYTES. Calls no cudaMalloc, cudaFree or other
  * allocating routine. The first call on a device looks up the array's device
- * address (cudaGetSymbolAddress) with that device current; make that first
- * call before any stream capture. All calls share the one array and it keeps
- * the last call's contents (nothing needs clearing: every score a call reads
- * it has written first), so calls whose work overlaps on the GPU -- on
- * different streams or from different host threads -- race on it.
+ * address (cudaGetSymbolAddress) with that device current; that lookup may
+ * load the library's module and commit the 32 MiB array on the device, so
+ * make the first call before the caller's own pool reserves the device's
+ * memory (else it can fail with KB_ERR_CUDA), and before any stream capture.
+ * The address is cached with the identity of the CUDA context; after a device
+ * reset the next call looks it up again (and commits the array again). All
+ * calls share the one array and it keeps the last call's contents (nothing
+ * needs clearing: every score a call reads it has written first), so calls
+ * whose work overlaps on the GPU -- on different streams or from different
+ * host threads -- race on it.
  */
 KB_API int kb_attn_fwd_naive_noalloc(const void* q, const void* k, const void* v, void* o,
                                      int B, int H, int S, int d, int causal, float scale,
@@ -308,7 +341,7 @@ KB_API int kb_attn_fwd_naive_noalloc(const void* q, const void* k, const void* v
  * 32 MB of L2; within a group the units go heaviest first (causal: most key
  * tiles), each to the CTA with the least modelled work so far (key tiles + 1).
  * The kernel runs CTA c's units in list order. The lists are deterministic.
- *   N      : heads (B * H), > 0;  S > 0;  d : 32, 64, 128 or 256
+ *   N      : heads (B * H), > 0;  0 < S <= 2^31 - 257;  d : 32, 64, 128 or 256
  *   grid   : persistent CTAs (the launch uses min(units, SMs))
  *   start  : host array of grid + 1 ints; CTA c runs items[start[c] .. start[c + 1])
  *   items  : host array of `cap` entries, head << 16 | unit
@@ -330,6 +363,15 @@ KB_API int kb_last_cuda_error(void);
 
 /* Library ABI version: 100 * major + minor. */
 KB_API int kb_version(void);
+
+/*
+ * kb_binary_version -- the architecture the library's kernels were compiled
+ * for, as the CUDA runtime reports it for the tensor-core attention kernel on
+ * the current device (cudaFuncAttributes::binaryVersion, 10 * major + minor:
+ * 103 for sm_103a code). *out receives it. KB_ERR_INVALID_ARG for a null
+ * pointer, KB_ERR_NO_DEVICE without a usable sm_103 device.
+ */
+KB_API int kb_binary_version(int* out);
 
 /*
  * kb_q15_exp_table -- the 64-entry table of the KB_FIXEDPOINT path,

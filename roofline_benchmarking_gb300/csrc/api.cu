@@ -23,6 +23,11 @@ thread_local int t_last_cuda_error = 0;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Longest sequence any kernel accepts: S + 256 (a tile's rows past S) stays in int.
+constexpr int kMaxSeq = std::numeric_limits<int32_t>::max() - 256;
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
 // Validation shared by every attention entry point; no CUDA call is made, so a
 // rejected request has no effect on any device.
 int validate(const void* q, const void* k, const void* v, const void* o, int B, int H, int S, int d,
@@ -40,6 +45,8 @@ int validate(const void* q, const void* k, const void* v, const void* o, int B, 
   const int64_t lim = std::numeric_limits<int64_t>::max() / 4;
   if (N > lim / S || N * S > lim / d) return KB_ERR_INVALID_ARG;
   if (d != 32 && d != 64 && d != 128 && d != 256) return KB_ERR_UNSUPPORTED;
+  // every kernel counts rows and tiles in 32 bits: S plus a tile's rows must fit
+  if (S > kMaxSeq) return KB_ERR_UNSUPPORTED;
   int var = variant;
   if (var == KB_AUTO) var = dtype == KB_F32 ? KB_FLASH : (dtype == KB_Q15 ? KB_FIXEDPOINT : KB_TC);
   if ((dtype == KB_Q15) != (var == KB_FIXEDPOINT)) return KB_ERR_UNSUPPORTED;
@@ -47,19 +54,19 @@ int validate(const void* q, const void* k, const void* v, const void* o, int B, 
   if ((dtype == KB_BF16 || dtype == KB_F16) && var != KB_TC) return KB_ERR_UNSUPPORTED;
   if (d == 256 && var != KB_TC) return KB_ERR_UNSUPPORTED;  // d = 256: tensor-core path only
   // the tensor-core kernels index their work items (256-row pairs, 128-row tiles at d = 256) in 32 bits
-  if (var == KB_TC && N * ((S + (d == 256 ? 127 : 255)) / (d == 256 ? 128 : 256)) > std::numeric_limits<int32_t>::max())
+  if (var == KB_TC && N * ceil_div(S, d == 256 ? 128 : 256) > std::numeric_limits<int32_t>::max())
     return KB_ERR_UNSUPPORTED;
   if (var == KB_FIXEDPOINT) {
     // keeps every fixed-point intermediate inside 64 bits
     if (S > 65536 || !q15_scale_ok(scale)) return KB_ERR_INVALID_ARG;
-    if (N * ((S + 15) / 16) > std::numeric_limits<int32_t>::max()) return KB_ERR_UNSUPPORTED;  // 16-row blocks
+    if (N * ceil_div(S, 16) > std::numeric_limits<int32_t>::max()) return KB_ERR_UNSUPPORTED;  // 16-row blocks
   }
   // one block per query row (fused) or per 64-row tile (flash, naive)
   const int64_t grid_limit = std::numeric_limits<int32_t>::max();
   if (var == KB_FUSED && N * S > grid_limit) return KB_ERR_UNSUPPORTED;
-  if ((var == KB_FLASH || var == KB_NAIVE) && N * ((S + 63) / 64) > grid_limit) return KB_ERR_UNSUPPORTED;
+  if ((var == KB_FLASH || var == KB_NAIVE) && N * ceil_div(S, 64) > grid_limit) return KB_ERR_UNSUPPORTED;
   if (var == KB_NAIVE && N > 65535) return KB_ERR_UNSUPPORTED;  // grid.z of the score pass
-  if (var == KB_NAIVE && (S + 63) / 64 > 65535) return KB_ERR_UNSUPPORTED;  // grid.y of the score pass
+  if (var == KB_NAIVE && ceil_div(S, 64) > 65535) return KB_ERR_UNSUPPORTED;  // grid.y of the score pass
   // the naive score matrix, N*S*S fp32, must be addressable
   if (var == KB_NAIVE && N > lim / S / S) return KB_ERR_INVALID_ARG;
   *resolved = var;
@@ -235,7 +242,15 @@ using namespace kb;
 
 extern "C" {
 
-int kb_version(void) { return 100; }
+int kb_version(void) { return 101; }
+
+int kb_binary_version(int* out) {
+  if (!out) return KB_ERR_INVALID_ARG;
+  int st = check_device();
+  if (st != KB_OK) return st;
+  cudaError_t e = tc_binary_version(out);
+  return e == cudaSuccess ? KB_OK : cuda_fail(e);
+}
 
 int kb_q15_exp_table(unsigned short* out64) {
   if (!out64) return KB_ERR_INVALID_ARG;
@@ -244,7 +259,8 @@ int kb_q15_exp_table(unsigned short* out64) {
 
 int kb_attn_work_lists(long long N, int S, int d, int causal, int grid, int* start, unsigned int* items, int cap,
                        int* count) {
-  if (N <= 0 || S <= 0 || grid <= 0 || cap < 0 || !start || !items || !count) return KB_ERR_INVALID_ARG;
+  if (N <= 0 || S <= 0 || S > kMaxSeq || grid <= 0 || cap < 0 || !start || !items || !count)
+    return KB_ERR_INVALID_ARG;
   if (d != 32 && d != 64 && d != 128 && d != 256) return KB_ERR_INVALID_ARG;
   return kb::tc_work_lists(N, S, d, causal != 0, grid, start, items, cap, count);
 }
@@ -262,6 +278,28 @@ int kb_attn_fwd_lse(const void* q, const void* k, const void* v, void* o, float*
   if (st != KB_OK) return st;
   if (var != KB_TC && var != KB_FLASH) return KB_ERR_UNSUPPORTED;
   return run_attention(q, k, v, o, B, H, S, d, causal, scale, dtype, variant, stream, nullptr, 0, false, lse);
+}
+
+int kb_attn_fwd_host(const void* q_host, const void* k_host, const void* v_host, void* o_host, void* q_dev,
+                     void* k_dev, void* v_dev, void* o_dev, int B, int H, int S, int d, int causal, float scale,
+                     int dtype, int variant, void* stream) {
+  if (!q_host || !k_host || !v_host || !o_host) return KB_ERR_INVALID_ARG;
+  int var = 0;
+  int st = validate(q_dev, k_dev, v_dev, o_dev, B, H, S, d, causal, scale, dtype, variant, &var);
+  if (st != KB_OK) return st;
+  if ((st = check_device()) != KB_OK) return st;
+  const size_t bytes = (size_t)B * H * S * d * (dtype == KB_F32 ? 4u : 2u);
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const void* src[3] = {q_host, k_host, v_host};
+  void* dst[3] = {q_dev, k_dev, v_dev};
+  for (int t = 0; t < 3; ++t) {
+    cudaError_t e = cudaMemcpyAsync(dst[t], src[t], bytes, cudaMemcpyHostToDevice, cs);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  st = run_attention(q_dev, k_dev, v_dev, o_dev, B, H, S, d, causal, scale, dtype, variant, stream, nullptr, 0, false);
+  if (st != KB_OK) return st;
+  cudaError_t e = cudaMemcpyAsync(o_host, o_dev, bytes, cudaMemcpyDeviceToHost, cs);
+  return e == cudaSuccess ? KB_OK : cuda_fail(e);
 }
 
 size_t kb_attn_workspace_bytes(int B, int H, int S, int d, int dtype, int variant) {

@@ -1223,4 +1223,11 @@ cudaError_t launch_selftest_timeout(unsigned long long limit_ns, cudaStream_t st
   return cudaGetLastError();
 }
 
+cudaError_t tc_binary_version(int* out) {
+  cudaFuncAttributes a;
+  cudaError_t e = cudaFuncGetAttributes(&a, attn_tc_kernel<128, false>);
+  if (e == cudaSuccess) *out = a.binaryVersion;
+  return e;
+}
+
 }  // namespace kb

@@ -41,6 +41,9 @@ int fused_f32_check(int S, int d);
 
 cudaError_t launch_tc(const AttnProblem& p, cudaStream_t st);
 int tc_check(int S, int d, int dtype);
+// cudaFuncAttributes::binaryVersion (10 * major + minor) of the tensor-core
+// kernel's code on the current device.
+cudaError_t tc_binary_version(int* out);
 // The per-CTA work lists of the tensor-core path (host only); *count = 0 when
 // the kernel falls back to its snake order.
 int tc_work_lists(int64_t N, int S, int d, bool causal, int grid, int* start, unsigned int* items, int cap,

@@ -10,10 +10,17 @@
 // `g_naive_noalloc_scores` below.
 //
 // The array is a file-scope __device__ variable: every GPU that loads this
-// library holds KB_NAIVE_NOALLOC_MAX_BYTES of it until the process exits. In
-// host code its name is only a host-side stand-in for the symbol, so the
-// device address is obtained with cudaGetSymbolAddress, once per device, with
-// that device current, on the first call made on that device.
+// library holds KB_NAIVE_NOALLOC_MAX_BYTES of it until the process exits. With
+// CUDA's lazy module loading (the default) the module that holds it, and so the
+// 32 MiB, is loaded on a device by the first call made there, inside
+// cudaGetSymbolAddress: that first call is where the memory is committed. In
+// host code the array's name is only a host-side stand-in for the symbol, so
+// the device address is obtained with cudaGetSymbolAddress with the device
+// current, and cached together with the identity of the CUDA context it
+// belongs to. A device reset (or a primary context torn down and created
+// again) reloads the module at a possibly different address; the cached
+// address is then looked up again instead of being reused.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -27,13 +34,47 @@ static __device__ __align__(256) float g_naive_noalloc_scores[KB_NAIVE_NOALLOC_M
 
 namespace {
 
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// The driver's id of the calling thread's current context (unique over the
+// process's lifetime, unlike the context handle, which can be reused); false
+// when there is none or the driver does not provide the query.
+bool current_context_id(unsigned long long* id) {
+  static std::once_flag once;
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+    (void)cudaGetLastError();
+  });
+  if (!get_current || !get_id) return false;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+  return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+struct ScratchEntry {
+  float* ptr = nullptr;        // device address of the array, nullptr until looked up
+  unsigned long long ctx = 0;  // id of the context the address belongs to
+  bool ctx_known = false;      // false: no context id was available, look up on every call
+};
+
 struct ScratchAddress {
   std::mutex mu;
-  std::vector<float*> ptr;  // per device ordinal, nullptr until set up
+  std::vector<ScratchEntry> dev;  // per device ordinal
 };
 ScratchAddress g_scratch;
 
-// Device address of the array on the current device (set up on first use).
+// Device address of the array in the current device's current context.
 int scratch_address(float** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -41,18 +82,27 @@ int scratch_address(float** out) {
     (void)cudaGetLastError();
     return KB_ERR_NO_DEVICE;
   }
+  unsigned long long ctx = 0;
+  bool known = current_context_id(&ctx);
   std::lock_guard<std::mutex> lk(g_scratch.mu);
-  if ((int)g_scratch.ptr.size() <= dev) g_scratch.ptr.resize(dev + 1, nullptr);
-  if (!g_scratch.ptr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_naive_noalloc_scores);
-    if (e != cudaSuccess) {
-      set_last_cuda_error(e);
-      return KB_ERR_CUDA;
-    }
-    g_scratch.ptr[dev] = static_cast<float*>(p);
+  if ((int)g_scratch.dev.size() <= dev) g_scratch.dev.resize(dev + 1);
+  ScratchEntry& s = g_scratch.dev[dev];
+  if (s.ptr && known && s.ctx_known && s.ctx == ctx) {
+    *out = s.ptr;
+    return KB_OK;
   }
-  *out = g_scratch.ptr[dev];
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_naive_noalloc_scores);
+  if (e != cudaSuccess) {
+    set_last_cuda_error(e);
+    return KB_ERR_CUDA;
+  }
+  // the lookup made the device's primary context current if none was
+  if (!known) known = current_context_id(&ctx);
+  s.ptr = static_cast<float*>(p);
+  s.ctx = ctx;
+  s.ctx_known = known;
+  *out = s.ptr;
   return KB_OK;
 }
 

@@ -84,6 +84,7 @@ SIGNATURES = {
     "kb_attn_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "kb_attn_fwd_lse": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P]),
     "kb_attn_fwd_ws": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P, _P, _SZ]),
+    "kb_attn_fwd_host": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P]),
     "kb_attn_bench": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P, _P, _SZ, _I, _I, _FP]),
     "kb_attn_bench_graph": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P, _P, _SZ, _I, _I, _I, _FP]),
     "kb_triad": (_I, [_P, _P, _P, _F, _SZ, _I, _P]),
@@ -94,6 +95,7 @@ SIGNATURES = {
     "kb_status_string": (ctypes.c_char_p, [_I]),
     "kb_last_cuda_error": (_I, []),
     "kb_version": (_I, []),
+    "kb_binary_version": (_I, [ctypes.POINTER(ctypes.c_int)]),
     "kb_q15_exp_table": (_I, [ctypes.POINTER(ctypes.c_uint16)]),
     "kb_attn_work_lists": (_I, [ctypes.c_longlong, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_int),
                                 ctypes.POINTER(ctypes.c_uint32), _I, ctypes.POINTER(ctypes.c_int)]),
@@ -150,6 +152,14 @@ def last_cuda_error() -> int:
 
 def version() -> int:
     return load().kb_version()
+
+
+def binary_version() -> int:
+    """10 * major + minor of the architecture the kernels were compiled for
+    (cudaFuncAttributes::binaryVersion on the current device)."""
+    out = ctypes.c_int(0)
+    _check(load().kb_binary_version(ctypes.byref(out)), "kb_binary_version")
+    return out.value
 
 
 def _check(status: int, what: str) -> None:
@@ -216,6 +226,26 @@ def kb_attn_fwd(q, k, v, o=None, causal: bool = False, scale: float | None = Non
                             int(bool(causal)), float(scale), dt, int(variant), _stream_ptr(stream))
     _check(st, "kb_attn_fwd")
     return o
+
+
+def kb_attn_fwd_host(qh, kh, vh, oh, q, k, v, o, causal: bool = False, scale: float | None = None,
+                     variant: int = Variant.AUTO, stream=None):
+    """kb_attn_fwd from host tensors to a host tensor: ``qh``, ``kh``, ``vh`` are
+    copied into the device staging tensors ``q``, ``k``, ``v`` on ``stream``,
+    the forward pass runs into ``o`` and ``o`` is copied back into ``oh``
+    (asynchronously: ``oh`` is valid once the stream gets there). Host tensors
+    should be pinned (``Tensor.pin_memory()``) for the copies to be asynchronous."""
+    B, H, S, d, dt = _attn_args(q, k, v, o)
+    for name, t in (("qh", qh), ("kh", kh), ("vh", vh), ("oh", oh)):
+        if t.is_cuda or not t.is_contiguous() or t.shape != q.shape or t.dtype != q.dtype:
+            raise ValueError(f"{name} must be a contiguous host tensor shaped and typed like q")
+    if scale is None:
+        scale = d ** -0.5
+    st = load().kb_attn_fwd_host(qh.data_ptr(), kh.data_ptr(), vh.data_ptr(), oh.data_ptr(), q.data_ptr(),
+                                 k.data_ptr(), v.data_ptr(), o.data_ptr(), B, H, S, d, int(bool(causal)),
+                                 float(scale), dt, int(variant), _stream_ptr(stream))
+    _check(st, "kb_attn_fwd_host")
+    return oh
 
 
 def kb_attn_fwd_lse(q, k, v, o=None, lse=None, causal: bool = False, scale: float | None = None,

@@ -48,12 +48,21 @@ def test_library_exports_every_declared_symbol(lib):
     assert not extra, extra
 
 
-def test_library_targets_sm103a_only(lib):
-    r = subprocess.run(["cuobjdump", "--list-elf", kbattn.LIBRARY], capture_output=True, text=True)
-    if r.returncode != 0:
-        pytest.skip("cuobjdump unavailable")
-    archs = set(re.findall(r"sm_\w+", r.stdout))
-    assert archs == {"sm_103a"}, archs
+def test_build_targets_sm103a_only():
+    """Every translation unit and the link get exactly one target: sm_103a
+    machine code, no PTX and no other architecture."""
+    assert kb_build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+    assert not any("arch" in f or "code=" in f for f in kb_build.NVCC_FLAGS)
+
+
+@pytest.mark.gpu
+def test_runtime_reports_sm103_code(lib):
+    """The CUDA runtime's view of the loaded kernels: binaryVersion 103."""
+    assert kbattn.binary_version() == 103
+
+
+def test_binary_version_rejects_a_null_pointer(lib):
+    assert lib.kb_binary_version(None) == Status.INVALID_ARG
 
 
 FAKE = 1 << 20  # an aligned, never-dereferenced address
@@ -212,7 +221,7 @@ def test_status_strings(lib):
     for s in Status:
         assert kbattn.status_string(s) == "KB_" + ("OK" if s == Status.OK else "ERR_" + s.name)
     assert kbattn.status_string(99) == "KB_UNKNOWN_STATUS"
-    assert kbattn.version() == 100
+    assert kbattn.version() == 101
 
 
 def test_binding_refuses_to_run_without_the_library(tmp_path):
@@ -222,3 +231,20 @@ def test_binding_refuses_to_run_without_the_library(tmp_path):
             "try:\n    k.load(k.LIBRARY)\nexcept RuntimeError as e:\n    print('raised', e)\n")
     r = subprocess.run(["python", "-c", code], capture_output=True, text=True, cwd=ROOT)
     assert "raised" in r.stdout and "not built" in r.stdout
+
+
+def test_host_call_validates_before_copying(lib):
+    """kb_attn_fwd_host rejects null host pointers and every kb_attn_fwd argument
+    error before it issues any copy (so no device is needed here)."""
+    f = ctypes.c_void_p(FAKE)
+    args = [f] * 8 + [1, 1, 64, 64, 0, ctypes.c_float(0.125), DType.F32, Variant.FLASH, None]
+    for i in range(8):
+        a = list(args)
+        a[i] = None
+        assert lib.kb_attn_fwd_host(*a) == Status.INVALID_ARG, i
+    a = list(args)
+    a[11] = 48  # d
+    assert lib.kb_attn_fwd_host(*a) == Status.UNSUPPORTED
+    a = list(args)
+    a[13] = ctypes.c_float(0.0)  # scale
+    assert lib.kb_attn_fwd_host(*a) == Status.INVALID_ARG
