@@ -121,6 +121,42 @@ class Oracle:
             raise ValueError(f"kb_oracle_attn_rows returned {rc}")
         return o
 
+    def attn_threads(self, q, k, v, causal: bool, scale: float, threads: int | None = None) -> np.ndarray:
+        """The same result as ``attn``, with the heads dealt out to host threads.
+
+        Heads are independent problems (each one's rows read only its own Q, K
+        and V), so every thread runs the unchanged single-threaded oracle on a
+        contiguous range of heads; the ctypes calls release the GIL. Returns
+        float64 [B, H, S, d], element for element what ``attn`` returns.
+        """
+        import concurrent.futures as cf
+
+        q, k, v = self._f64(q), self._f64(k), self._f64(v)
+        if q.ndim != 4 or q.shape != k.shape or q.shape != v.shape:
+            raise ValueError(f"q, k, v must share one [B,H,S,d] shape, got {q.shape} {k.shape} {v.shape}")
+        B, H, S, d = q.shape
+        N = B * H
+        qf, kf, vf = (x.reshape(N, S, d) for x in (q, k, v))
+        o = np.empty((N, S, d), dtype=np.float64)
+        if threads is None:
+            threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+        threads = max(1, min(int(threads), N))
+        bounds = [N * t // threads for t in range(threads + 1)]
+
+        def run(t):
+            n0, n1 = bounds[t], bounds[t + 1]
+            if n1 == n0:
+                return 0
+            return self.lib.kb_oracle_attn(qf[n0:n1].ctypes.data_as(_DP), kf[n0:n1].ctypes.data_as(_DP),
+                                           vf[n0:n1].ctypes.data_as(_DP), o[n0:n1].ctypes.data_as(_DP),
+                                           1, n1 - n0, S, d, int(bool(causal)), float(scale))
+
+        with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+            rcs = list(ex.map(run, range(threads)))
+        if any(rcs):
+            raise ValueError(f"kb_oracle_attn returned {rcs}")
+        return o.reshape(B, H, S, d)
+
     def triad(self, b, c, s: float) -> np.ndarray:
         """a = b + s*c in fp32, rounded once."""
         b = np.ascontiguousarray(np.asarray(b, dtype=np.float32))

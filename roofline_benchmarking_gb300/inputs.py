@@ -73,6 +73,11 @@ BF16_CAUSAL_S16384 = Workload("bf16_causal_b1h32s16384d128_sharp", 1, 32, 16384,
 # one-query-tile-per-CTA layout, at the bench workload's sequence length.
 BF16_CAUSAL_D256 = Workload("bf16_causal_b2h16s4096d256", 2, 16, 4096, 256, True, "bf16", 6, "normal")
 
+# fp16 operands on the tensor-core path: the bench workload's and the d = 64
+# workload's shapes and draws, rounded to fp16 instead of bf16.
+F16_CAUSAL_S4096 = BF16_CAUSAL_S4096.with_(name="f16_causal_b4h16s4096d128", dtype="f16")
+F16_S2048_D64 = BF16_S2048_D64.with_(name="f16_b16h12s2048d64", dtype="f16")
+
 # The Q15 fixed-point model runs on the fp32 workloads' shapes and draws.
 Q15_SINGLE_HEAD = SINGLE_HEAD_F32.with_(name="q15_b1h1s64d32", dtype="q15")
 Q15_S1024 = F32_S1024.with_(name="q15_b1h8s1024d64", dtype="q15")
@@ -80,6 +85,7 @@ Q15_S1024_CAUSAL = F32_S1024_CAUSAL.with_(name="q15_b1h8s1024d64_causal", dtype=
 
 WORKLOADS = {w.name: w for w in (SINGLE_HEAD_F32, F32_S1024, F32_S1024_CAUSAL,
                                  BF16_CAUSAL_S4096, BF16_S2048_D64, BF16_CAUSAL_S16384, BF16_CAUSAL_D256,
+                                 F16_CAUSAL_S4096, F16_S2048_D64,
                                  Q15_SINGLE_HEAD, Q15_S1024, Q15_S1024_CAUSAL)}
 
 # STREAM Triad working set: three fp32 arrays of 2 GiB each.

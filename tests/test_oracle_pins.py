@@ -230,6 +230,16 @@ def pin_rows_api_matches_full(orc):
     assert np.array_equal(got, flat[heads, rows])
 
 
+def pin_threaded_heads_match_full(orc):
+    """attn_threads deals heads to host threads: the same bits as one call."""
+    rng = _rng(24)
+    q, k, v = (_rand(rng, (2, 5, 9, 3)) for _ in range(3))
+    for causal in (False, True):
+        full = orc.attn(q, k, v, causal, 0.6)
+        for threads in (1, 3, 4, 16):
+            assert np.array_equal(orc.attn_threads(q, k, v, causal, 0.6, threads=threads), full)
+
+
 def pin_triad_exact(orc):
     """a = b + s*c rounded once to fp32: compare with exact rational arithmetic."""
     rng = _rng(23)
@@ -314,7 +324,7 @@ def pin_hbm_reference_kernels(orc):
 PINS = [pin_brute_force, pin_rows_are_probabilities, pin_constant_v, pin_zero_query_is_mean,
         pin_causal_first_row_and_single_key, pin_causal_is_prefix_attention, pin_key_permutation,
         pin_key_shift, pin_affine_in_v, pin_hard_attention_limit, pin_two_key_closed_form,
-        pin_heads_are_independent, pin_rows_api_matches_full, pin_triad_exact,
+        pin_heads_are_independent, pin_rows_api_matches_full, pin_threaded_heads_match_full, pin_triad_exact,
         pin_triad_stream_constants, pin_hbm_reference_kernels, pin_lse]
 
 
