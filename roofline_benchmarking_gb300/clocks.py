@@ -76,6 +76,7 @@ class ClockSampler:
             out["sm_mhz"] = statistics.median(sm)
             out["sm_max_mhz"] = max(smax)
             out["power_w_max"] = max(power)
+            out["power_w_median"] = statistics.median(power)
         out["reasons"] = sorted(reasons)
         return out
 

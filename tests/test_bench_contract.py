@@ -32,31 +32,65 @@ def check_common(line, steps, warmup, dtype):
 
 
 def test_reference_arm_line():
+    import bench
+    from roofline_benchmarking_gb300 import inputs
     line = run_bench("--impl", "reference", "--steps", "2", "--warmup", "1", "--reference-seconds", "1.5")
     check_common(line, 2, 1, "f64")
     assert line["impl"] == "reference"
+    # the same config dict the library's arm prints for this workload
+    assert line["config"] == json.loads(json.dumps(bench.bench_config(inputs.BF16_CAUSAL_S4096, 1)))
     cb = line["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"] and cb["sample"]
+    assert cb["cores_available"] >= cb["cores"] and cb["rows_per_step"] > 0
     e2e = line["e2e"]
     assert e2e["value"] == line["value"] and e2e["unit"] == line["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
 
 
+def test_roofline_kernel_follows_the_workload():
+    import bench
+    from roofline_benchmarking_gb300 import inputs
+    want = {"bf16_causal_b4h16s4096d128": ("attn_tc_kernel<128,bf16>", "tensor"),
+            "bf16_b16h12s2048d64": ("attn_tc_kernel<64,bf16>", "tensor"),
+            "f16_b16h12s2048d64": ("attn_tc_kernel<64,f16>", "tensor"),
+            "bf16_causal_b2h16s4096d256": ("attn_tc256_kernel<bf16>", "tensor"),
+            "f32_b1h8s1024d64": ("flash_f32_kernel", "alu"),
+            "f32_b1h8s1024d64_causal": ("flash_f32_kernel + flash_merge_kernel", "alu")}
+    for name, (kernel, bound) in want.items():
+        k = bench.kernel_for(inputs.WORKLOADS[name], 152)
+        assert (k["kernel"], k["bound"]) == (kernel, bound), name
+    assert bench.kernel_for(inputs.F32_S1024_CAUSAL, 152)["launches_per_step"] == 2
+    assert bench.metric_for(inputs.BF16_CAUSAL_S4096) == bench.METRIC
+
+
 @pytest.mark.gpu
 def test_library_arm_line():
-    line = run_bench("--steps", "5", "--warmup", "3", "--e2e-steps", "3", "--cpu-seconds", "1", "--no-triad")
+    line = run_bench("--steps", "5", "--warmup", "3", "--e2e-steps", "3", "--cpu-seconds", "1", "--no-triad",
+                     "--soak-seconds", "0.5")
     check_common(line, 5, 3, "bf16")
     assert line.get("impl", "ours") != "reference"
     r = line["roofline"]
+    assert r["kernel"] == "attn_tc_kernel<128,bf16>"
     assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s" and r["peak"] > 0
     assert r["achieved"] > 0 and abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-9
     assert r["traffic"] is None or r["traffic"] > 0
+    assert r["bandwidth_source"].endswith("(no Triad in this run)") and r["attainable"] > 0
+    sus = r["sustained"]
+    assert sus["launches"] >= 1 and sus["achieved"] > 0 and sus["clock_samples"] >= 1
     c = line["clocks"]
-    assert c["sm_max_mhz"] > 0 and isinstance(c["reasons"], list)
+    assert c["sm_max_mhz"] > 0 and isinstance(c["reasons"], list) and "timed_region_only" in c
     assert line["gpu_launches"] >= 5
     e2e = line["e2e"]
-    assert e2e["value"] > 0 and e2e["unit"] == "TFLOP/s"
+    assert e2e["value"] > 0 and e2e["unit"] == "TFLOP/s" and e2e["output_equals_device_run"] is True
     assert e2e["h2d_bytes_per_step"] == 3 * 4 * 16 * 4096 * 128 * 2  # Q, K, V in bf16
     assert e2e["d2h_bytes_per_step"] == 4 * 16 * 4096 * 128 * 2      # O
     cb = line["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] > 0
+
+
+@pytest.mark.gpu
+def test_library_arm_line_names_the_d64_kernel():
+    line = run_bench("--workload", "bf16_b16h12s2048d64", "--steps", "3", "--warmup", "3", "--no-e2e",
+                     "--no-cpu-baseline", "--no-triad", "--soak-seconds", "0")
+    assert line["config"]["workload"] == "bf16_b16h12s2048d64"
+    assert line["roofline"]["kernel"] == "attn_tc_kernel<64,bf16>"
