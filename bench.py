@@ -477,7 +477,7 @@ def run_ours(args, d: Dist):
         clocks = sampler.summary(h0 - 0.3, sus["window"][1])
         clocks["window"] = f"timed region and the {sus['seconds']:.1f} s soak of the same kernel right after it"
     else:
-        clocks = narrow
+        clocks = dict(narrow)
     clocks["timed_region_only"] = narrow
 
     total_ms = d.max(total_ms)

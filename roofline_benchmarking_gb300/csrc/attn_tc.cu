@@ -593,6 +593,374 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
 }
 
 // ---------------------------------------------------------------------------
+// d <= 64: P in tensor-memory columns of its own. At d = 64 the two O
+// accumulators take 128 columns, which leaves room for the packed P tiles
+// beside the score tiles: S_A 0-127, S_B 128-255, P_A 256-319, P_B 320-383,
+// O_A 384-447, O_B 448-511. The next score tile S_g(j+1) is then issued as
+// soon as the softmax of tile g has copied S_g(j) into registers (SFREE), and
+// O_g += P_g(j) V_j as soon as P_g(j) is written (PFULL): the score MMA no longer
+// waits for the P V that used to read P out of the score tile's columns, so
+// the tensor core computes the next scores while the softmax exponentiates the
+// current ones, and each softmax warpgroup finds its next tile ready. The
+// softmax writes P_g(j) only after P V(j-1) has read P_g(j-1) (PVDONE, which
+// also makes O hold exactly tiles < j when it must be rescaled).
+// MMA issue order per key tile j: S_A(j+1), S_B(j+1), then P V_A(j), P V_B(j).
+// ---------------------------------------------------------------------------
+struct Tc64 {
+  static constexpr int D = 64;
+  static constexpr int TILE = kBM * D * 2;  // bytes of a Q, K or V tile (128 rows x 128 bytes)
+  static constexpr int KS = 4, VS = 4;      // K and V ring stages
+  static constexpr int OFF_Q = 0;           // Q_A then Q_B
+  static constexpr int OFF_K = OFF_Q + 2 * TILE;
+  static constexpr int OFF_V = OFF_K + KS * TILE;
+  static constexpr int OFF_BAR = OFF_V + VS * TILE;
+  enum {
+    B_Q = 0,
+    B_KFULL = 1,
+    B_KEMPTY = B_KFULL + KS,
+    B_VFULL = B_KEMPTY + KS,
+    B_VEMPTY = B_VFULL + VS,
+    B_SFULL = B_VEMPTY + VS,  // [2]: S of tile A / B computed
+    B_SFREE = B_SFULL + 2,    // [2]: S of tile A / B copied into registers by the softmax
+    B_PFULL = B_SFREE + 2,    // [2]: P of tile A / B written (and O rescaled)
+    B_PVDONE = B_PFULL + 2,   // [2]: a P V of tile A / B completed (each one commits)
+    B_OFREE = B_PVDONE + 2,   // [2]: O of tile A / B read out by the epilogue
+    B_QFREE = B_OFREE + 2,    // last score MMA of an item done: Q may be replaced
+    B_DRAIN = B_QFREE + 1,
+    NBAR = B_DRAIN + 1
+  };
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // [0] TMEM base, [1] abort flag
+  static constexpr int BYTES = OFF_MISC + 16;
+  static constexpr int SMEM = BYTES + 1024;
+  static_assert(SMEM <= 232448, "at most 227 KB of shared memory per CTA");
+  __host__ __device__ static constexpr uint32_t tm_s(int g) { return 128u * (uint32_t)g; }
+  __host__ __device__ static constexpr uint32_t tm_p(int g) { return 256u + 64u * (uint32_t)g; }
+  __host__ __device__ static constexpr uint32_t tm_o(int g) { return 384u + 64u * (uint32_t)g; }
+};
+
+template <bool F16>
+__global__ void __launch_bounds__(kThreadsTC, 1)
+    attn_tc64_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                     const __grid_constant__ CUtensorMap tmv, const __grid_constant__ SchedTable tab,
+                     uint8_t* __restrict__ out, float* __restrict__ lse, int dout, int N, int S, int causal,
+                     float scale_log2, unsigned long long limit) {
+  // dout: output columns per row (64, or 32 when a d = 32 problem runs here with its
+  // tiles zero-filled by TMA past column 32)
+  using C = Tc64;
+  constexpr int D = C::D;
+  constexpr uint32_t kAB = F16 ? 0u : 1u;
+  constexpr uint32_t IDESC_QK = ptx::f16_idesc(kBM, kBN, kAB, 0);
+  constexpr uint32_t IDESC_PV = ptx::f16_idesc(kBM, D, kAB, 1);
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* sm = smem_raw + (base - raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::OFF_MISC + 4);
+  auto bar = [&](int i) -> uint32_t { return base + C::OFF_BAR + 8u * (uint32_t)i; };
+
+  const Schedule sched(N, S, causal, &tab);
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    ptx::mbar_init(bar(C::B_Q), 1);
+    for (int s = 0; s < C::KS; ++s) {
+      ptx::mbar_init(bar(C::B_KFULL + s), 1);
+      ptx::mbar_init(bar(C::B_KEMPTY + s), 1);
+    }
+    for (int s = 0; s < C::VS; ++s) {
+      ptx::mbar_init(bar(C::B_VFULL + s), 1);
+      ptx::mbar_init(bar(C::B_VEMPTY + s), 1);
+    }
+    for (int g = 0; g < 2; ++g) {
+      ptx::mbar_init(bar(C::B_SFULL + g), 1);
+      ptx::mbar_init(bar(C::B_SFREE + g), 4 * 32);
+      ptx::mbar_init(bar(C::B_PFULL + g), 4 * 32);
+      ptx::mbar_init(bar(C::B_PVDONE + g), 1);
+      ptx::mbar_init(bar(C::B_OFREE + g), 4 * 32);
+    }
+    ptx::mbar_init(bar(C::B_QFREE), 1);
+    ptx::mbar_init(bar(C::B_DRAIN), 1);
+    ptx::fence_mbar_init();
+  }
+  if (warp == kWarpMMA) {
+    ptx::tmem_alloc(base + C::OFF_MISC, kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + C::OFF_MISC);
+
+  if (warp >= kWarpTMA) {
+    ptx::regs_decrease<kRegsControl>();
+    if (warp == kWarpTMA) {
+      // ------------------------------------------------------------ TMA producer
+      if (lane == 0) {
+        ptx::tma_prefetch_desc(&tmq);
+        ptx::tma_prefetch_desc(&tmk);
+        ptx::tma_prefetch_desc(&tmv);
+        int kdone = 0, vdone = 0, items = 0;
+        bool ok = true;
+        Item it;
+        for (int round = 0; ok && sched.get(round, it); ++round) {
+          if (items > 0) ok = wait_bar(bar(C::B_QFREE), (items - 1) & 1, abort_flag, limit, true);
+          if (!ok) break;
+          ptx::mbar_arrive_expect_tx(bar(C::B_Q), 2 * C::TILE);
+          for (int g = 0; g < 2; ++g)
+            ptx::tma_load_3d(base + C::OFF_Q + g * C::TILE, &tmq, bar(C::B_Q), 0, it.q0 + g * kBM, it.n);
+          for (int j = 0; j < it.nB && ok; ++j) {
+            const int ks = kdone % C::KS, vs = vdone % C::VS;
+            if (kdone >= C::KS) ok = wait_bar(bar(C::B_KEMPTY + ks), ((kdone / C::KS) & 1) ^ 1, abort_flag, limit, true);
+            if (!ok) break;
+            ptx::mbar_arrive_expect_tx(bar(C::B_KFULL + ks), C::TILE);
+            ptx::tma_load_3d(base + C::OFF_K + ks * C::TILE, &tmk, bar(C::B_KFULL + ks), 0, j * kBN, it.n);
+            ++kdone;
+            if (vdone >= C::VS) ok = wait_bar(bar(C::B_VEMPTY + vs), ((vdone / C::VS) & 1) ^ 1, abort_flag, limit, true);
+            if (!ok) break;
+            ptx::mbar_arrive_expect_tx(bar(C::B_VFULL + vs), C::TILE);
+            ptx::tma_load_3d(base + C::OFF_V + vs * C::TILE, &tmv, bar(C::B_VFULL + vs), 0, j * kBN, it.n);
+            ++vdone;
+          }
+          ++items;
+        }
+        if (items > 0) wait_bar(bar(C::B_Q), (items - 1) & 1, abort_flag, limit, false);
+        for (int x = kdone - C::KS < 0 ? 0 : kdone - C::KS; x < kdone; ++x)
+          wait_bar(bar(C::B_KFULL + x % C::KS), (x / C::KS) & 1, abort_flag, limit, false);
+        for (int x = vdone - C::VS < 0 ? 0 : vdone - C::VS; x < vdone; ++x)
+          wait_bar(bar(C::B_VFULL + x % C::VS), (x / C::VS) & 1, abort_flag, limit, false);
+      }
+      __syncwarp();
+    } else if (warp == kWarpMMA) {
+      // ------------------------------------------------------------ MMA issuer
+      auto issue_s = [&](int g, int ks) {
+        const uint64_t a0 = ptx::sw128_desc(base + C::OFF_Q + g * C::TILE, 16, 1024);
+        const uint64_t b0 = ptx::sw128_desc(base + C::OFF_K + ks * C::TILE, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (uint32_t)(kk * 32) >> 4;
+          ptx::mma_f16_ss_elect(tmem + C::tm_s(g), a0 + off, b0 + off, IDESC_QK, kk > 0 ? 1u : 0u);
+        }
+        ptx::mma_commit_elect(bar(C::B_SFULL + g));
+      };
+      auto issue_pv = [&](int g, int vs, bool first) {
+        const uint64_t b0 = ptx::sw128_desc(base + C::OFF_V + vs * C::TILE, kColBlock, 1024);
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          ptx::mma_f16_ts_elect(tmem + C::tm_o(g), tmem + C::tm_p(g) + kk * 8, b0 + ((kk * 16 * 128) >> 4), IDESC_PV,
+                                (!first || kk > 0) ? 1u : 0u);
+        ptx::mma_commit_elect(bar(C::B_PVDONE + g));
+      };
+      bool ok = true;
+      int kbase = 0, vbase = 0;  // ring positions of the current item's first K and V tiles
+      int sa = 0, sb = 0;        // score tiles of tile A / B issued
+      int pa = 0, pb = 0;        // P tiles of tile A / B consumed
+      Item it;
+      for (int item = 0; ok && sched.get(item, it); ++item) {
+        const int nA = it.nA, nB = it.nB;
+        ok = warp_wait(bar(C::B_Q), item & 1, abort_flag, limit);
+        const int ks0 = kbase % C::KS;
+        if (ok) ok = warp_wait(bar(C::B_KFULL + ks0), (kbase / C::KS) & 1, abort_flag, limit);
+        // a score tile is overwritten only after the softmax has copied the previous one out
+        if (ok && sa > 0) ok = warp_wait(bar(C::B_SFREE + 0), (sa - 1) & 1, abort_flag, limit);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        issue_s(0, ks0);
+        ++sa;
+        if (sb > 0) ok = warp_wait(bar(C::B_SFREE + 1), (sb - 1) & 1, abort_flag, limit);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        issue_s(1, ks0);
+        ++sb;
+        ptx::mma_commit_elect(bar(C::B_KEMPTY + ks0));
+        if (nB == 1) ptx::mma_commit_elect(bar(C::B_QFREE));
+        for (int j = 0; j < nB && ok; ++j) {
+          const int jn = j + 1, kpn = kbase + jn, ksn = kpn % C::KS;
+          if (jn < nB) {  // the next scores first: the softmax waits for them, P V is off its path
+            ok = warp_wait(bar(C::B_KFULL + ksn), (kpn / C::KS) & 1, abort_flag, limit);
+            if (ok && jn < nA) {
+              ok = warp_wait(bar(C::B_SFREE + 0), (sa - 1) & 1, abort_flag, limit);
+              if (ok) {
+                ptx::tc_fence_after();
+                issue_s(0, ksn);
+                ++sa;
+              }
+            }
+            if (ok) ok = warp_wait(bar(C::B_SFREE + 1), (sb - 1) & 1, abort_flag, limit);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            issue_s(1, ksn);
+            ++sb;
+            ptx::mma_commit_elect(bar(C::B_KEMPTY + ksn));
+            if (jn == nB - 1) ptx::mma_commit_elect(bar(C::B_QFREE));  // the item's last score MMA
+          }
+          const int vp = vbase + j, vs = vp % C::VS;
+          ok = warp_wait(bar(C::B_VFULL + vs), (vp / C::VS) & 1, abort_flag, limit);
+          if (ok && j < nA) {
+            ok = warp_wait(bar(C::B_PFULL + 0), pa & 1, abort_flag, limit);
+            if (ok && j == 0 && item > 0) ok = warp_wait(bar(C::B_OFREE + 0), (item - 1) & 1, abort_flag, limit);
+            if (ok) {
+              ++pa;
+              ptx::tc_fence_after();
+              issue_pv(0, vs, j == 0);
+            }
+          }
+          if (ok) ok = warp_wait(bar(C::B_PFULL + 1), pb & 1, abort_flag, limit);
+          if (ok && j == 0 && item > 0) ok = warp_wait(bar(C::B_OFREE + 1), (item - 1) & 1, abort_flag, limit);
+          if (!ok) break;
+          ++pb;
+          ptx::tc_fence_after();
+          issue_pv(1, vs, j == 0);
+          ptx::mma_commit_elect(bar(C::B_VEMPTY + vs));
+        }
+        kbase += nB;
+        vbase += nB;
+      }
+      ptx::mma_commit_elect(bar(C::B_DRAIN));
+      warp_wait_all(bar(C::B_DRAIN), 0, abort_flag, limit, false);
+    }
+  } else {
+    ptx::regs_increase<kRegsSoftmax>();
+    // ------------------------------------------------------------ softmax, warps 0-7
+    const int g = warp >> 2;
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;
+    const uint32_t tl = tmem + ((uint32_t)(wq * 32) << 16);
+    const uint32_t ts = tl + C::tm_s(g), tp = tl + C::tm_p(g), to = tl + C::tm_o(g);
+    int scnt = 0;  // score tiles consumed
+    int pcnt = 0;  // P tiles written (= P V of this tile issued or to be issued)
+    bool ok = true;
+    Item it;
+    for (int item = 0; ok && sched.get(item, it); ++item) {
+      const int row = it.q0 + g * kBM + r;
+      const int nj = g ? it.nB : it.nA;
+      const int diag = 2 * it.t + g;
+      float m_run = -INFINITY, l_run = 0.f;
+      for (int j = 0; j < nj; ++j) {
+        if (!(ok = warp_wait(bar(C::B_SFULL + g), scnt & 1, abort_flag, limit))) break;
+        ++scnt;
+        ptx::tc_fence_after();
+        float s[kBN];
+        {
+          uint32_t u0[32], u1[32], u2[32], u3[32];
+          ptx::tmem_ld32(ts + 0, u0);
+          ptx::tmem_ld32(ts + 32, u1);
+          ptx::tmem_ld32(ts + 64, u2);
+          ptx::tmem_ld32(ts + 96, u3);
+          ptx::tmem_wait_ld();
+          // the score columns may take the next tile's scores now
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(bar(C::B_SFREE + g));
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            s[e] = __uint_as_float(u0[e]);
+            s[32 + e] = __uint_as_float(u1[e]);
+            s[64 + e] = __uint_as_float(u2[e]);
+            s[96 + e] = __uint_as_float(u3[e]);
+          }
+        }
+        const int k0 = j * kBN;
+        if ((causal && j == diag) || k0 + kBN > S) {
+          const int lim = min(causal ? row - k0 : kBN - 1, S - 1 - k0);
+#pragma unroll
+          for (int c = 0; c < kBN; ++c)
+            if (c > lim) s[c] = -INFINITY;
+        }
+        float mx[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mx[e] = fmaxf(s[e], s[8 + e]);
+#pragma unroll
+        for (int c = 16; c < kBN; c += 16)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) mx[e] = ptx::max3(mx[e], s[c + e], s[c + 8 + e]);
+        const float m_tile =
+            fmaxf(ptx::max3(mx[0], mx[1], mx[2]), ptx::max3(mx[3], mx[4], ptx::max3(mx[5], mx[6], mx[7]))) *
+            scale_log2;
+        float alpha = 1.f;
+        bool corr = false;
+        if (j == 0) {
+          m_run = m_tile == -INFINITY ? 0.f : m_tile;
+        } else if (m_tile > m_run + 8.0f) {
+          alpha = ptx::ex2(m_run - m_tile);
+          m_run = m_tile;
+          l_run *= alpha;
+          corr = true;
+        }
+        const float2 sl2 = make_float2(scale_log2, scale_log2);
+        const float2 nm2 = make_float2(-m_run, -m_run);
+        float2 sum2[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sum2[e] = make_float2(0.f, 0.f);
+        uint32_t pk[2][32];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const float2 x = ptx::fma2(make_float2(s[h * 64 + 2 * c], s[h * 64 + 2 * c + 1]), sl2, nm2);
+            const float2 pv = make_float2(ptx::ex2(x.x), ptx::ex2(x.y));
+            sum2[c & 3] = ptx::add2(sum2[c & 3], pv);
+            pk[h][c] = pack2<F16>(pv.x, pv.y);
+          }
+        }
+        const float2 t2 = ptx::add2(ptx::add2(sum2[0], sum2[1]), ptx::add2(sum2[2], sum2[3]));
+        l_run += t2.x + t2.y;
+        // P V of the previous tile has read P and added into O: P may be overwritten,
+        // and O holds exactly the tiles before j for the rescale
+        if (pcnt > 0 && !(ok = warp_wait(bar(C::B_PVDONE + g), (pcnt - 1) & 1, abort_flag, limit))) break;
+        ptx::tc_fence_after();
+        ptx::tmem_st32(tp + 0, pk[0]);
+        ptx::tmem_st32(tp + 32, pk[1]);
+        if (__any_sync(0xffffffffu, corr)) {
+          uint32_t u[32];
+#pragma unroll 1
+          for (int cb = 0; cb < D / 32; ++cb) {
+            ptx::tmem_ld32(to + cb * 32, u);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * alpha);
+            ptx::tmem_st32(to + cb * 32, u);
+          }
+        }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(C::B_PFULL + g));
+        ++pcnt;
+      }
+      // the item's last P V of this tile complete: O is final
+      if (ok) ok = warp_wait(bar(C::B_PVDONE + g), (pcnt - 1) & 1, abort_flag, limit);
+      if (ok) {
+        ptx::tc_fence_after();
+        const float inv = 1.0f / l_run;
+        if (lse != nullptr && row < S) lse[(size_t)it.n * S + row] = (m_run + log2f(l_run)) * 0.6931471805599453f;
+        uint32_t u[D / 32][32];
+#pragma unroll
+        for (int cb = 0; cb < D / 32; ++cb) ptx::tmem_ld32(to + cb * 32, u[cb]);
+        ptx::tmem_wait_ld();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(C::B_OFREE + g));
+        uint8_t* orow = out + ((size_t)it.n * S + row) * (size_t)dout * 2;
+        const bool st32 = (reinterpret_cast<uintptr_t>(out) & 31) == 0;
+#pragma unroll
+        for (int cb = 0; cb < D / 32; ++cb) {
+          if (row < S && cb * 32 < dout) {
+            store_o16<F16>(orow + cb * 64, &u[cb][0], inv, st32);
+            store_o16<F16>(orow + cb * 64 + 32, &u[cb][16], inv, st32);
+          }
+        }
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMMA) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // d = 256. Two 128 x 256 fp32 O accumulators would take all 512 TMEM columns,
 // so here a work item is ONE 128-row query tile, and TMEM holds two 128 x 64
 // score buffers (the scores of key tile j+1 are computed while the softmax
@@ -1123,8 +1491,13 @@ bool make_map(CUtensorMap* m, const void* ptr, int64_t N, int S, int d, bool f16
 template <int D, bool F16>
 cudaError_t tc_launch(const AttnProblem& p, cudaStream_t st) {
   using C = TcCfg<D>;
+  constexpr int smem = D == 64 ? Tc64::SMEM : C::SMEM;
   // per-device attribute, so it is set on every launch
-  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  cudaError_t e;
+  if constexpr (D == 64)
+    e = cudaFuncSetAttribute(attn_tc64_kernel<F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  else
+    e = cudaFuncSetAttribute(attn_tc_kernel<D, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int dreal = p.d;  // D, or 32 with D = 64
   CUtensorMap mq, mk, mv;
@@ -1140,9 +1513,14 @@ cudaError_t tc_launch(const AttnProblem& p, cudaStream_t st) {
   const int64_t grid = items < sms ? items : sms;  // persistent: at most one CTA per SM
   const SchedTable tab = sched_table(p.N, units, (p.S + kBN - 1) / kBN, p.causal != 0, (int)grid,
                                      2.0 * p.S * dreal * 2.0);
-  attn_tc_kernel<D, F16><<<(unsigned)grid, kThreadsTC, C::SMEM, st>>>(
-      mq, mk, mv, mo, tab, static_cast<uint8_t*>(p.o), p.lse, dreal, (int)p.N, p.S, p.causal,
-      p.scale * 1.4426950408889634f, kDefaultWaitLimitNs);
+  if constexpr (D == 64)
+    attn_tc64_kernel<F16><<<(unsigned)grid, kThreadsTC, smem, st>>>(
+        mq, mk, mv, tab, static_cast<uint8_t*>(p.o), p.lse, dreal, (int)p.N, p.S, p.causal,
+        p.scale * 1.4426950408889634f, kDefaultWaitLimitNs);
+  else
+    attn_tc_kernel<D, F16><<<(unsigned)grid, kThreadsTC, smem, st>>>(
+        mq, mk, mv, mo, tab, static_cast<uint8_t*>(p.o), p.lse, dreal, (int)p.N, p.S, p.causal,
+        p.scale * 1.4426950408889634f, kDefaultWaitLimitNs);
   return cudaGetLastError();
 }
 
@@ -1180,7 +1558,7 @@ int tc_check(int S, int d, int dtype) {
   if (cudaGetDevice(&dev) != cudaSuccess) return KB_ERR_NO_DEVICE;
   if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
     return KB_ERR_CUDA;
-  const int need = d == 256 ? Tc256::SMEM : (d == 128 ? TcCfg<128>::SMEM : TcCfg<64>::SMEM);  // d = 32: the 64 kernel
+  const int need = d == 256 ? Tc256::SMEM : (d == 128 ? TcCfg<128>::SMEM : Tc64::SMEM);  // d = 32: the 64 kernel
   return need <= optin ? KB_OK : KB_ERR_UNSUPPORTED;
 }
 
