@@ -159,6 +159,18 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   }
 }
 
+// A weight as the P V MMA sees it: p rounded to 16 bits (the packing's
+// round-to-nearest-even), widened back to fp32.
+template <bool F16>
+__device__ __forceinline__ float rounded16(float p) {
+  const uint32_t w = pack2<F16>(p, 0.f);
+  if constexpr (F16) {
+    return __low2float(*reinterpret_cast<const __half2*>(&w));
+  } else {
+    return __uint_as_float(w << 16);
+  }
+}
+
 // Sixteen fp32 values of one O row, times inv, rounded to 16 bits and stored at
 // dst: one 32-byte store (a whole L2 sector) when the output base is 32-byte
 // aligned (st32; every row and chunk offset is a multiple of 32 bytes), else two
@@ -439,7 +451,13 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       const int row = it.q0 + g * kBM + r;
       const int nj = g ? it.nB : it.nA;
       const int diag = 2 * it.t + g;  // the key tile on the diagonal (causal)
-      float m_run = -INFINITY, l_run = 0.f;
+      // l_run sums the unrounded weights (the log-sum-exp uses it). The P V MMA sees
+      // each weight rounded to 16 bits; l_corr adds, for the largest weight of every
+      // tile, the difference its rounding made, so that O / (l_run + l_corr) is the
+      // mean of V under the weights the MMA used where it matters: a dominant
+      // weight's rounding error then cancels instead of scaling O (the smaller
+      // weights' errors are relatively small and of both signs).
+      float m_run = -INFINITY, l_run = 0.f, l_corr = 0.f;
       for (int j = 0; j < nj; ++j) {
         if (!(ok = warp_wait(bar(C::B_SFULL + g), scnt & 1, abort_flag, limit))) break;
         ++scnt;
@@ -475,9 +493,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         for (int c = 16; c < kBN; c += 16)
 #pragma unroll
           for (int e = 0; e < 8; ++e) mx[e] = ptx::max3(mx[e], s[c + e], s[c + 8 + e]);
-        const float m_tile =
-            fmaxf(ptx::max3(mx[0], mx[1], mx[2]), ptx::max3(mx[3], mx[4], ptx::max3(mx[5], mx[6], mx[7]))) *
-            scale_log2;
+        const float s_max =
+            fmaxf(ptx::max3(mx[0], mx[1], mx[2]), ptx::max3(mx[3], mx[4], ptx::max3(mx[5], mx[6], mx[7])));
+        const float m_tile = s_max * scale_log2;
         float alpha = 1.f;
         bool corr = false;
         if (j == 0) {
@@ -486,6 +504,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
           alpha = ptx::ex2(m_run - m_tile);
           m_run = m_tile;
           l_run *= alpha;
+          l_corr *= alpha;
           corr = true;
         }
         // P = exp2(s * scale_log2 - m) as 16-bit pairs into columns [0, 64) of S;
@@ -509,6 +528,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         }
         const float2 t2 = ptx::add2(ptx::add2(sum2[0], sum2[1]), ptx::add2(sum2[2], sum2[3]));
         l_run += t2.x + t2.y;
+        {
+          // the tile's largest weight, computed exactly as the loop above computes it
+          const float p_max = ptx::ex2(fmaf(s_max, scale_log2, -m_run));
+          l_corr += rounded16<F16>(p_max) - p_max;
+        }
         if (__any_sync(0xffffffffu, corr)) {
           // Rescale O after P is out (the scores are dead by now). S_g(j)
           // completing implies P V of tile j-1 has completed (one issuing
@@ -531,7 +555,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       if (ok) ok = warp_wait(bar(C::B_OFINAL + g), item & 1, abort_flag, limit);
       if (ok) {
         ptx::tc_fence_after();
-        const float inv = 1.0f / l_run;
+        const float inv = 1.0f / (l_run + l_corr);
         // natural log of sum_j exp(score): the scores sum to 2^m_run * l_run in base 2
         if (lse != nullptr && row < S) lse[(size_t)it.n * S + row] = (m_run + log2f(l_run)) * 0.6931471805599453f;
         // the whole O row in one round trip to TMEM (the score registers are free by now);
@@ -836,7 +860,13 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       const int row = it.q0 + g * kBM + r;
       const int nj = g ? it.nB : it.nA;
       const int diag = 2 * it.t + g;
-      float m_run = -INFINITY, l_run = 0.f;
+      // l_run sums the unrounded weights (the log-sum-exp uses it). The P V MMA sees
+      // each weight rounded to 16 bits; l_corr adds, for the largest weight of every
+      // tile, the difference its rounding made, so that O / (l_run + l_corr) is the
+      // mean of V under the weights the MMA used where it matters: a dominant
+      // weight's rounding error then cancels instead of scaling O (the smaller
+      // weights' errors are relatively small and of both signs).
+      float m_run = -INFINITY, l_run = 0.f, l_corr = 0.f;
       for (int j = 0; j < nj; ++j) {
         if (!(ok = warp_wait(bar(C::B_SFULL + g), scnt & 1, abort_flag, limit))) break;
         ++scnt;
@@ -874,9 +904,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         for (int c = 16; c < kBN; c += 16)
 #pragma unroll
           for (int e = 0; e < 8; ++e) mx[e] = ptx::max3(mx[e], s[c + e], s[c + 8 + e]);
-        const float m_tile =
-            fmaxf(ptx::max3(mx[0], mx[1], mx[2]), ptx::max3(mx[3], mx[4], ptx::max3(mx[5], mx[6], mx[7]))) *
-            scale_log2;
+        const float s_max =
+            fmaxf(ptx::max3(mx[0], mx[1], mx[2]), ptx::max3(mx[3], mx[4], ptx::max3(mx[5], mx[6], mx[7])));
+        const float m_tile = s_max * scale_log2;
         float alpha = 1.f;
         bool corr = false;
         if (j == 0) {
@@ -885,6 +915,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
           alpha = ptx::ex2(m_run - m_tile);
           m_run = m_tile;
           l_run *= alpha;
+          l_corr *= alpha;
           corr = true;
         }
         const float2 sl2 = make_float2(scale_log2, scale_log2);
@@ -905,6 +936,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         }
         const float2 t2 = ptx::add2(ptx::add2(sum2[0], sum2[1]), ptx::add2(sum2[2], sum2[3]));
         l_run += t2.x + t2.y;
+        {
+          // the tile's largest weight, computed exactly as the loop above computes it
+          const float p_max = ptx::ex2(fmaf(s_max, scale_log2, -m_run));
+          l_corr += rounded16<F16>(p_max) - p_max;
+        }
         // P V of the previous tile has read P and added into O: P may be overwritten,
         // and O holds exactly the tiles before j for the rescale
         if (pcnt > 0 && !(ok = warp_wait(bar(C::B_PVDONE + g), (pcnt - 1) & 1, abort_flag, limit))) break;
@@ -931,7 +967,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       if (ok) ok = warp_wait(bar(C::B_PVDONE + g), (pcnt - 1) & 1, abort_flag, limit);
       if (ok) {
         ptx::tc_fence_after();
-        const float inv = 1.0f / l_run;
+        const float inv = 1.0f / (l_run + l_corr);
         if (lse != nullptr && row < S) lse[(size_t)it.n * S + row] = (m_run + log2f(l_run)) * 0.6931471805599453f;
         uint32_t u[D / 32][32];
 #pragma unroll
@@ -1242,7 +1278,13 @@ __global__ void __launch_bounds__(kThreads256, 1)
     Item256 it;
     for (int item = 0; ok && sched.get(item, it); ++item) {
       const int row = it.q0 + r;
-      float m_run = -INFINITY, l_run = 0.f;
+      // l_run sums the unrounded weights (the log-sum-exp uses it). The P V MMA sees
+      // each weight rounded to 16 bits; l_corr adds, for the largest weight of every
+      // tile, the difference its rounding made, so that O / (l_run + l_corr) is the
+      // mean of V under the weights the MMA used where it matters: a dominant
+      // weight's rounding error then cancels instead of scaling O (the smaller
+      // weights' errors are relatively small and of both signs).
+      float m_run = -INFINITY, l_run = 0.f, l_corr = 0.f;
       for (int j = 0; j < it.nk; ++j) {
         const int b = scnt & 1;
         if (!(ok = warp_wait(bar(C::B_SFULL + b), (scnt >> 1) & 1, abort_flag, limit))) break;
@@ -1274,9 +1316,9 @@ __global__ void __launch_bounds__(kThreads256, 1)
         for (int c = 16; c < kBN256; c += 16)
 #pragma unroll
           for (int e = 0; e < 8; ++e) mx[e] = ptx::max3(mx[e], s[c + e], s[c + 8 + e]);
-        const float m_tile =
-            fmaxf(ptx::max3(mx[0], mx[1], mx[2]), ptx::max3(mx[3], mx[4], ptx::max3(mx[5], mx[6], mx[7]))) *
-            scale_log2;
+        const float s_max =
+            fmaxf(ptx::max3(mx[0], mx[1], mx[2]), ptx::max3(mx[3], mx[4], ptx::max3(mx[5], mx[6], mx[7])));
+        const float m_tile = s_max * scale_log2;
         float alpha = 1.f;
         bool corr = false;
         if (j == 0) {
@@ -1285,6 +1327,7 @@ __global__ void __launch_bounds__(kThreads256, 1)
           alpha = ptx::ex2(m_run - m_tile);
           m_run = m_tile;
           l_run *= alpha;
+          l_corr *= alpha;
           corr = true;
         }
         const float2 sl2 = make_float2(scale_log2, scale_log2);
@@ -1305,6 +1348,11 @@ __global__ void __launch_bounds__(kThreads256, 1)
         }
         const float2 t2 = ptx::add2(ptx::add2(sum2[0], sum2[1]), ptx::add2(sum2[2], sum2[3]));
         l_run += t2.x + t2.y;
+        {
+          // the tile's largest weight, computed exactly as the loop above computes it
+          const float p_max = ptx::ex2(fmaf(s_max, scale_log2, -m_run));
+          l_corr += rounded16<F16>(p_max) - p_max;
+        }
         if (__any_sync(0xffffffffu, corr)) {
           // O must hold exactly the tiles before j: wait for P V of tile j-1
           // (global index scnt - 1). Its phase is unambiguous: S of this tile
@@ -1329,7 +1377,7 @@ __global__ void __launch_bounds__(kThreads256, 1)
       if (ok) ok = warp_wait(bar(C::B_OFINAL), item & 1, abort_flag, limit);
       if (ok) {
         ptx::tc_fence_after();
-        const float inv = 1.0f / l_run;
+        const float inv = 1.0f / (l_run + l_corr);
         if (lse != nullptr && row < S) lse[(size_t)it.n * S + row] = (m_run + log2f(l_run)) * 0.6931471805599453f;
         // O / l, rounded to 16 bits, 64 columns at a time through this warp's two
         // staging buffers (alternating), one TMA store each; rows past S lie outside
