@@ -35,9 +35,12 @@ def fp32_peak_gflops(sms: int, clock_mhz: float, cores_per_sm: int = CUDA_CORES_
     return sms * cores_per_sm * 2.0 * clock_mhz * 1e6 / 1e9
 
 
-# 32-bit integer multiply-add lanes per SM: half the FP32 lanes, the ratio of
-# the integer multiply-add rate to the FP32 FMA rate in NVIDIA's published
-# per-SM throughput tables for recent architectures (an assumption for sm_103).
+# Integer multiply-add lanes per SM per clock, the roof of the Q15 kernel. That
+# kernel forms each 16-bit x 16-bit product of its scores and weighted sums with
+# one dp2a lane-operation (two 16 x 8-bit products on the split operands), so its
+# bound is the dp2a issue rate. Measured on GB300 with independent dp2a, IMAD and
+# FFMA chains in one run: dp2a and IMAD each issue 65.6 lanes per SM per clock
+# where FFMA issues 128, i.e. half the FP32 lanes (64).
 INT32_MAD_PER_SM = 64
 
 

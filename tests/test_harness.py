@@ -21,9 +21,10 @@ def test_outputs_share_one_schema(tmp_path):
                mean_ms=0.2, p99_ms=0.21, tflops=1200.0, gbs=1000.0, bound="tensor", attainable=1961.8,
                roofline_unit="TFLOP/s", roofline_frac=0.61, sm_mhz=1900.0, clock_reasons="none", iters=10)
     meta = {"device": "GPU", "sms": 152, "peaks": {"bf16_tflops": 1961.8, "hbm_gbs": 6655.3}, "peaks_source": "measured",
-            "theoretical_hbm_gbs": 7928.0, "fp32_peak_tflops": 80.5}
+            "theoretical_hbm_gbs": 7928.0, "fp32_peak_tflops": 80.5, "attention_bandwidth_gbs": 7262.3,
+            "attention_bandwidth_source": "best STREAM Triad of this run"}
     md = harness.write_outputs([row, dict(row, kernel="triad", block=256)], str(tmp_path), meta)
-    assert md.count("\n| ") == 3 and "0.610" in md
+    assert md.count("\n| ") == 3 and "0.610" in md and "7262 GB/s (best STREAM Triad of this run)" in md
     lines = (tmp_path / "results.jsonl").read_text().splitlines()
     assert json.loads(lines[0])["meta"]["sms"] == 152 and len(lines) == 3
     rows = list(csv.DictReader(open(tmp_path / "results.csv")))
