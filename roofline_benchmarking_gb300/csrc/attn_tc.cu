@@ -1000,7 +1000,14 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
 // d = 256. Two 128 x 256 fp32 O accumulators would take all 512 TMEM columns,
 // so here a work item is ONE 128-row query tile, and TMEM holds two 128 x 64
 // score buffers (the scores of key tile j+1 are computed while the softmax
-// works on tile j) and the 128 x 256 O. Key tiles are 64 keys; K and V rings
+// works on tile j), the item's Q tile as 16-bit pairs (the A operand of the
+// score MMAs, so that they read only K from shared memory: with Q read from
+// shared memory as well, the MMAs' operand reads and the TMA writes of K and V
+// took more of the shared-memory port than the tensor pipe had work) and the
+// 128 x 256 O. The softmax warps copy each Q tile from its TMA landing zone in
+// shared memory into TMEM: the first item's before its first tile, every later
+// one during the previous item's last tile, as soon as that tile's scores are
+// in registers (all of that item's score MMAs have then completed). Key tiles are 64 keys; K and V rings
 // of two 32 KB stages each plus the 64 KB Q tile use 192 KB of shared memory.
 // Warps 0-3 run the softmax (thread = row = TMEM lane), warp 4 loads Q and K
 // with TMA, warp 6 loads V (so K tiles are not held behind V's ring), warp 5
@@ -1041,8 +1048,8 @@ struct Tc256 {
     B_PVDONE = B_PFULL + 2,   // every P V completed, in order
     B_OFINAL = B_PVDONE + 1,  // last P V of an item completed
     B_OFREE = B_OFINAL + 1,   // O read out by the epilogue
-    B_QFREE = B_OFREE + 1,    // last score MMA of an item completed
-    B_DRAIN = B_QFREE + 1,
+    B_QTM = B_OFREE + 1,      // the item's Q copied from shared memory into TMEM
+    B_DRAIN = B_QTM + 1,
     NBAR = B_DRAIN + 1
   };
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
@@ -1050,6 +1057,7 @@ struct Tc256 {
   static constexpr int SMEM = BYTES + 1024;
   static_assert(SMEM <= 232448, "at most 227 KB of shared memory per CTA");
   static constexpr uint32_t TM_O = 256;  // O in columns 256-511; score buffer b in 64 b .. 64 b + 63
+  static constexpr uint32_t TM_Q = 128;  // Q in columns 128-255: column c holds features 2c, 2c + 1
 };
 
 // One query tile per item: from the host's work lists (same construction as for
@@ -1129,7 +1137,7 @@ __global__ void __launch_bounds__(kThreads256, 1)
     ptx::mbar_init(bar(C::B_PVDONE), 1);
     ptx::mbar_init(bar(C::B_OFINAL), 1);
     ptx::mbar_init(bar(C::B_OFREE), 4 * 32);
-    ptx::mbar_init(bar(C::B_QFREE), 1);
+    ptx::mbar_init(bar(C::B_QTM), 4 * 32);
     ptx::mbar_init(bar(C::B_DRAIN), 1);
     ptx::fence_mbar_init();
   }
@@ -1151,7 +1159,8 @@ __global__ void __launch_bounds__(kThreads256, 1)
       bool ok = true;
       Item256 it;
       for (int round = 0; ok && sched.get(round, it); ++round) {
-        if (items > 0) ok = wait_bar(bar(C::B_QFREE), (items - 1) & 1, abort_flag, limit, true);
+        // the previous Q tile has been copied into TMEM: its landing zone may be reused
+        if (items > 0) ok = wait_bar(bar(C::B_QTM), (items - 1) & 1, abort_flag, limit, true);
         if (!ok) break;
         ptx::mbar_arrive_expect_tx(bar(C::B_Q), C::QTILE);
         for (int b = 0; b < 4; ++b)
@@ -1201,15 +1210,15 @@ __global__ void __launch_bounds__(kThreads256, 1)
     // ------------------------------------------------------------ MMA issuer
     // The whole warp runs the issue loop; one elected lane issues each MMA and commit.
     {
-      // S(buffer b) = Q K^T: 16 k-steps of 16 features; both operands K-major
+      // S(buffer b) = Q K^T: 16 k-steps of 16 features; Q from TMEM (8 columns a
+      // k-step), K K-major from shared memory
       auto issue_s = [&](int b, int ks) {
-        const uint64_t a0 = ptx::sw128_desc(base + C::OFF_Q, 16, 1024);
         const uint64_t b0 = ptx::sw128_desc(base + C::OFF_K + ks * C::KTILE, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < C::D / 16; ++kk) {
-          const uint32_t offa = ((kk >> 2) * C::QBLK + (kk & 3) * 32) >> 4;
           const uint32_t offb = ((kk >> 2) * C::KBLK + (kk & 3) * 32) >> 4;
-          ptx::mma_f16_ss_elect(tmem + 64u * (uint32_t)b, a0 + offa, b0 + offb, IDESC_QK, kk > 0 ? 1u : 0u);
+          ptx::mma_f16_ts_elect(tmem + 64u * (uint32_t)b, tmem + C::TM_Q + kk * 8, b0 + offb, IDESC_QK,
+                                kk > 0 ? 1u : 0u);
         }
         ptx::mma_commit_elect(bar(C::B_SFULL + b));
       };
@@ -1226,7 +1235,7 @@ __global__ void __launch_bounds__(kThreads256, 1)
       Item256 it;
       for (int item = 0; ok && sched.get(item, it); ++item) {
         const int nk = it.nk;
-        ok = warp_wait(bar(C::B_Q), item & 1, abort_flag, limit);
+        ok = warp_wait(bar(C::B_QTM), item & 1, abort_flag, limit);
         // S(0) and S(1)
         for (int j = 0; j < 2 && j < nk && ok; ++j) {
           const int ks = kcons % C::KS;
@@ -1235,7 +1244,6 @@ __global__ void __launch_bounds__(kThreads256, 1)
           ptx::tc_fence_after();
           issue_s(scnt & 1, ks);
           ptx::mma_commit_elect(bar(C::B_KEMPTY + ks));
-          if (j == nk - 1) ptx::mma_commit_elect(bar(C::B_QFREE));
           ++kcons;
           ++scnt;
         }
@@ -1258,7 +1266,6 @@ __global__ void __launch_bounds__(kThreads256, 1)
             ptx::tc_fence_after();
             issue_s(scnt & 1, ks);
             ptx::mma_commit_elect(bar(C::B_KEMPTY + ks));
-            if (j + 2 == nk - 1) ptx::mma_commit_elect(bar(C::B_QFREE));
             ++kcons;
             ++scnt;
           }
@@ -1273,10 +1280,36 @@ __global__ void __launch_bounds__(kThreads256, 1)
     const int r = warp * 32 + lane;
     const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
     const uint32_t to = tl + C::TM_O;
+    // Q tile of item k: this thread's row of the 128-byte-swizzled landing zone
+    // (16-byte chunk c of a 64-feature block at chunk c ^ (row % 8)) into TMEM
+    // columns TM_Q + 32 b + 4 c .. + 3 (four feature pairs per chunk)
+    auto copy_q = [&](int k) -> bool {
+      if (!warp_wait(bar(C::B_Q), k & 1, abort_flag, limit)) return false;
+#pragma unroll 1
+      for (int blk = 0; blk < C::D / 64; ++blk) {
+        uint32_t u[32];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 x = *reinterpret_cast<const uint4*>(sm + C::OFF_Q + blk * C::QBLK + r * 128 +
+                                                          ((c ^ (r & 7)) << 4));
+          u[4 * c] = x.x;
+          u[4 * c + 1] = x.y;
+          u[4 * c + 2] = x.z;
+          u[4 * c + 3] = x.w;
+        }
+        ptx::tmem_st32(tl + C::TM_Q + blk * 32, u);
+      }
+      ptx::tmem_wait_st();
+      ptx::fence_proxy_async_smem();  // the reads of the landing zone before TMA rewrites it
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar(C::B_QTM));
+      return true;
+    };
     int scnt = 0;  // score tiles consumed (global)
     bool ok = true;
     Item256 it;
     for (int item = 0; ok && sched.get(item, it); ++item) {
+      if (item == 0 && !(ok = copy_q(0))) break;
       const int row = it.q0 + r;
       // l_run sums the unrounded weights (the log-sum-exp uses it). The P V MMA sees
       // each weight rounded to 16 bits; l_corr adds, for the largest weight of every
@@ -1301,6 +1334,11 @@ __global__ void __launch_bounds__(kThreads256, 1)
             s[e] = __uint_as_float(u0[e]);
             s[32 + e] = __uint_as_float(u1[e]);
           }
+        }
+        if (j == it.nk - 1) {
+          // every score MMA of this item has completed: the next item's Q may replace it
+          Item256 nx;
+          if (sched.get(item + 1, nx) && !(ok = copy_q(item + 1))) break;
         }
         const int k0 = j * kBN256;
         if ((causal && k0 + kBN256 - 1 > it.q0) || k0 + kBN256 > S) {

@@ -272,7 +272,8 @@ def _plan():
     H = kbattn.HbmOp
     return [
         ("tc " + inputs.BF16_CAUSAL_S4096.name, r"attn_tc_kernel<128", attn(inputs.BF16_CAUSAL_S4096, V.TC)),
-        ("tc " + inputs.BF16_S2048_D64.name, r"attn_tc_kernel<64", attn(inputs.BF16_S2048_D64, V.TC)),
+        ("tc " + inputs.BF16_S2048_D64.name, r"attn_tc64_kernel", attn(inputs.BF16_S2048_D64, V.TC)),
+        ("tc " + inputs.BF16_CAUSAL_D256.name, r"attn_tc256_kernel", attn(inputs.BF16_CAUSAL_D256, V.TC)),
         ("naive " + inputs.F32_S1024.name, r"naive_", attn(inputs.F32_S1024, V.NAIVE)),
         ("fused " + inputs.F32_S1024.name, r"fused_row", attn(inputs.F32_S1024, V.FUSED)),
         ("flash " + inputs.F32_S1024.name, r"flash_f32", attn(inputs.F32_S1024, V.FLASH)),
