@@ -4,7 +4,11 @@ roofline, with SM clocks sampled during each row. One schema for all rows,
 written as CSV, Markdown and JSON lines.
 
   python -m roofline_benchmarking_gb300.harness [--only SUBSTR] [--out DIR]
-                                                [--seconds S] [--quick]
+                                                [--seconds S] [--quick] [--sweep]
+
+``--sweep`` runs only the kbench page's sequence sweep (section "Running") and
+writes its table (speed-up of each variant over the naive one per S) to
+``sweep.md`` beside the other outputs.
 
 Sources (web pages): the kbench page, "Implementation details" (events around
 the kernel only, configurable warm-up, mean / p50 / p99 / min, achieved GFLOP/s
@@ -186,6 +190,30 @@ def write_outputs(rows, out_dir, meta):
     return "\n".join(md)
 
 
+def sweep_table(rows) -> str | None:
+    """The kbench page's sequence sweep (16 heads, d = 64, fp32) as the page
+    reports it: per S and variant the median time, GFLOP/s, effective GB/s
+    (naive: with its modelled score traffic) and the speed-up over the naive
+    variant; the page's "Expected results" give naive 1.0x, fused ~2.2x and
+    flash ~4.7x at S = 2048 on its own (unnamed) GPU."""
+    names = {w.name: w for w in inputs.KBENCH_SWEEP}
+    by = {(r["workload"], r["variant"]): r for r in rows if r["workload"] in names and r["kernel"] == "attention"}
+    if not by:
+        return None
+    md = ["| S | variant | p50 ms | GFLOP/s | effective GB/s | speed-up over naive | frac of FMA roof |",
+          "|---|---|---|---|---|---|---|"]
+    for w in inputs.KBENCH_SWEEP:
+        base = by.get((w.name, "NAIVE"))
+        for v in ("NAIVE", "FUSED", "FLASH"):
+            r = by.get((w.name, v))
+            if r is None:
+                continue
+            up = f"{base['p50_ms'] / r['p50_ms']:.2f}x" if base else ""
+            md.append(f"| {w.S} | {v} | {r['p50_ms']:.4f} | {r['tflops'] * 1e3:.0f} | {r['gbs']:.0f} | {up} | "
+                      f"{r['roofline_frac']:.3f} |")
+    return "\n".join(md)
+
+
 def main(argv=None) -> int:
     p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     p.add_argument("--only", default="", help="run only rows whose workload, variant or kernel contains this")
@@ -194,7 +222,13 @@ def main(argv=None) -> int:
     p.add_argument("--quick", action="store_true", help="small HBM arrays and few repetitions")
     p.add_argument("--no-hbm", action="store_true")
     p.add_argument("--no-attention", action="store_true")
+    p.add_argument("--sweep", action="store_true",
+                   help="only the kbench page's sequence sweep (fp32, 16 heads, d = 64, S = 128 ... 2048; "
+                        "no HBM rows unless --with-hbm)")
+    p.add_argument("--with-hbm", action="store_true", help="with --sweep: run the HBM kernels too")
     args = p.parse_args(argv)
+    if args.sweep and not args.with_hbm:
+        args.no_hbm = True
     if not torch.cuda.is_available():
         print("the harness needs a CUDA GPU", file=sys.stderr)
         return 2
@@ -219,7 +253,8 @@ def main(argv=None) -> int:
         triad = [r["gbs"] for r in hbm if r["kernel"] == "triad"]
         bandwidth = max(triad) if triad else peaks["hbm_gbs"]
         bw_source = "best STREAM Triad of this run" if triad else "measured copy bandwidth (no Triad run)"
-        for w in ([] if args.no_attention else inputs.WORKLOADS.values()):
+        todo = inputs.KBENCH_SWEEP if args.sweep else inputs.WORKLOADS.values()
+        for w in ([] if args.no_attention else todo):
             for variant in ATTN_VARIANTS[w.dtype]:
                 if only and only not in w.name.lower() and only not in variant.name.lower():
                     continue
@@ -236,6 +271,11 @@ def main(argv=None) -> int:
             "theoretical_hbm_gbs": rf.theoretical_dram_gbs(info["mem_clock_khz"] / 1e3, info["mem_bus_width_bits"]),
             "fp32_peak_tflops": rf.fp32_peak_gflops(info["sm_count"], info["sm_clock_khz"] / 1e3) / 1e3}
     print(write_outputs(rows, args.out, meta))
+    sweep = sweep_table(rows)
+    if sweep:
+        with open(os.path.join(args.out, "sweep.md"), "w") as f:
+            f.write(sweep + "\n")
+        print(sweep)
     return 0
 
 

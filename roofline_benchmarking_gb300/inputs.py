@@ -83,10 +83,19 @@ Q15_SINGLE_HEAD = SINGLE_HEAD_F32.with_(name="q15_b1h1s64d32", dtype="q15")
 Q15_S1024 = F32_S1024.with_(name="q15_b1h8s1024d64", dtype="q15")
 Q15_S1024_CAUSAL = F32_S1024_CAUSAL.with_(name="q15_b1h8s1024d64_causal", dtype="q15")
 
+# The kbench page's own sequence sweep (section "Running": --seq 128,256,512,1024,2048
+# --heads 16 --dim 64, fp32, every kernel), whose "Expected results" give the
+# three variants' relative latency at S = 2048. The page names no batch, seed or
+# distribution: one batch, non-causal, U[-1, 1] as in the other fp32 workloads,
+# seed 5.
+KBENCH_SWEEP_S = (128, 256, 512, 1024, 2048)
+KBENCH_SWEEP = tuple(Workload(f"f32_b1h16s{S}d64", 1, 16, S, 64, False, "f32", 5, "uniform")
+                     for S in KBENCH_SWEEP_S)
+
 WORKLOADS = {w.name: w for w in (SINGLE_HEAD_F32, F32_S1024, F32_S1024_CAUSAL,
                                  BF16_CAUSAL_S4096, BF16_S2048_D64, BF16_CAUSAL_S16384, BF16_CAUSAL_D256,
                                  F16_CAUSAL_S4096, F16_S2048_D64,
-                                 Q15_SINGLE_HEAD, Q15_S1024, Q15_S1024_CAUSAL)}
+                                 Q15_SINGLE_HEAD, Q15_S1024, Q15_S1024_CAUSAL, *KBENCH_SWEEP)}
 
 # STREAM Triad working set: three fp32 arrays of 2 GiB each.
 TRIAD_ARRAY_BYTES = 2 << 30

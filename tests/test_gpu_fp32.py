@@ -63,6 +63,27 @@ def test_f32_workloads_match_oracle(oracle, variant, w):
     assert mx <= F32_TOL, (mx, mean, rel)
 
 
+@pytest.fixture(scope="module")
+def sweep_oracle(oracle):
+    cache = {}
+
+    def get(w):
+        if w.name not in cache:
+            cache[w.name] = oracle.attn_threads(*inputs.make_qkv(w), w.causal, w.scale)
+        return cache[w.name]
+    return get
+
+
+@pytest.mark.parametrize("variant", VARIANTS, ids=lambda v: v.name)
+@pytest.mark.parametrize("w", inputs.KBENCH_SWEEP, ids=lambda w: w.name)
+def test_kbench_sequence_sweep_matches_oracle(sweep_oracle, variant, w):
+    """The kbench page's own sweep (16 heads, d = 64, S = 128 ... 2048), every
+    element of every variant against the oracle."""
+    got = run(w, variant)
+    mx, mean, rel = errors(got, sweep_oracle(w))
+    assert mx <= F32_TOL, (mx, mean, rel)
+
+
 def test_naive_with_caller_workspace_matches_cached(oracle):
     w = inputs.F32_S1024_CAUSAL.with_(H=2, S=320)
     a = run(w, Variant.NAIVE, use_ws=False)

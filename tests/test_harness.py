@@ -31,6 +31,23 @@ def test_outputs_share_one_schema(tmp_path):
     assert [r["kernel"] for r in rows] == ["attention", "triad"] and list(rows[0]) == harness.FIELDS
 
 
+def test_kbench_sequence_sweep_table():
+    # the page's sweep: 16 heads, d = 64, fp32, S = 128 ... 2048
+    assert [w.S for w in inputs.KBENCH_SWEEP] == [128, 256, 512, 1024, 2048]
+    assert all((w.B, w.H, w.d, w.dtype, w.causal) == (1, 16, 64, "f32", False) for w in inputs.KBENCH_SWEEP)
+    assert all(inputs.WORKLOADS[w.name] is w for w in inputs.KBENCH_SWEEP)
+    w = inputs.KBENCH_SWEEP[-1]
+    rows = [{"kernel": "attention", "workload": w.name, "variant": v, "p50_ms": ms, "tflops": w.flops / ms / 1e9,
+             "gbs": 1.0, "roofline_frac": 0.5} for v, ms in (("NAIVE", 2.0), ("FUSED", 1.0), ("FLASH", 0.5))]
+    rows.append(dict(rows[0], workload=inputs.F32_S1024.name))  # not a sweep row: ignored
+    md = harness.sweep_table(rows)
+    lines = md.splitlines()[2:]
+    assert len(lines) == 3
+    assert lines[0].startswith("| 2048 | NAIVE | 2.0000 |") and "| 1.00x |" in lines[0]
+    assert "| 2.00x |" in lines[1] and "| 4.00x |" in lines[2]
+    assert harness.sweep_table([rows[-1]]) is None
+
+
 @pytest.mark.gpu
 def test_harness_runs_a_quick_sweep(tmp_path):
     assert harness.main(["--only", "f32_b1h1s64d32", "--no-hbm", "--seconds", "0.02",
