@@ -197,7 +197,8 @@ def kernel_for(w, sms: int) -> dict:
     # (N * ceil(S / 64) <= 2 x SMs, S >= 256) and merges them in a second launch
     tiles = (w.S + 63) // 64
     split = w.causal and tiles >= 4 and w.N * tiles <= 2 * sms
-    return {"kernel": "flash_f32_kernel" + (" + flash_merge_kernel" if split else ""), "bound": "alu",
+    name = "flash_f32x2_kernel" if w.d <= 64 else "flash_f32_kernel"
+    return {"kernel": name + (" + flash_merge_kernel" if split else ""), "bound": "alu",
             "launches_per_step": 2 if split else 1, "peak_key": None,
             "peak_note": "fp32 FMA: SMs x 128 lanes x 2 x max SM clock"}
 

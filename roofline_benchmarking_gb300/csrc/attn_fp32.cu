@@ -376,6 +376,278 @@ __global__ void __launch_bounds__(kFlashThreads, 1) flash_f32_kernel(const float
   }
 }
 
+// ---------------------------------------------------------------------------
+// flash at d <= 64 with paired fp32 FMAs (fma.rn.f32x2: two products per lane
+// and instruction; the FMA pipe's rate per product is that of the scalar FMA,
+// measured on GB300, but each instruction issues two). Blocks, the two thread
+// groups over even and odd key tiles, the causal split and the merge are those
+// of flash_f32_kernel; what changes is the shared-memory layout of the two tile
+// products, so that each paired FMA finds both of its operand pairs in
+// adjacent registers of one 16-byte load:
+//  * Q K^T: Q and K row-major; one paired FMA takes features (k, k+1) of a
+//    query row and of a key, so each score is carried as two partial sums
+//    (even and odd features) that are added once per tile;
+//  * P V: P row-major as the softmax writes it; V re-laid from its row-major
+//    copy into key pairs, Vp[j/2][c] = (V[j][c], V[j+1][c]), so one paired FMA
+//    takes keys (j, j+1) of a P row and of a V column; each output gathers
+//    even-key and odd-key partial sums over a tile, added into O after it.
+// A thread owns query rows ty*4 + a, keys tx + 16 b and output columns
+// 32 g + 2 tx + e (e < 2, g < D / 32); the lanes of a warp hold two row groups.
+// ---------------------------------------------------------------------------
+template <int D>
+struct Fx2 {
+  static constexpr int LDQ = D + 4;       // row stride of the Q and K tiles
+  static constexpr int LDP = kBC + 4;     // row stride of the P tile
+  static constexpr int G = D / 32;        // column groups of a thread
+  static constexpr int NO = 2 * G;        // output columns of a thread per row
+  static constexpr int KBUF = kBC * LDQ;  // one K buffer
+  static constexpr int VBUF = kBC * D;    // one row-major V buffer (the cp.async target)
+  static constexpr int GROUP = 2 * KBUF + 2 * VBUF + kBC * D + kBR * LDP;  // K x 2, V x 2, Vp, P
+  static constexpr int SMEM_FLOATS = kBR * LDQ + 2 * GROUP;
+};
+
+__device__ __forceinline__ void st4(float* p, float4 x) { *reinterpret_cast<float4*>(p) = x; }
+
+// Max and sum over the 16 lanes of a row (lane bits 0, 1, 2 and 4).
+__device__ __forceinline__ float tx_max(float x) {
+#pragma unroll
+  for (int o : {1, 2, 4, 16}) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+__device__ __forceinline__ float tx_sum(float x) {
+#pragma unroll
+  for (int o : {1, 2, 4, 16}) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kFlashThreads, 1) flash_f32x2_kernel(const float* __restrict__ Q,
+                                                                    const float* __restrict__ K,
+                                                                    const float* __restrict__ V,
+                                                                    float* __restrict__ O, float* __restrict__ lse,
+                                                                    int64_t N, int S, int causal, float scale_log2,
+                                                                    float* __restrict__ part, int split_from) {
+  static_assert(D == 32 || D == 64, "the paired-FMA flash kernel runs d = 32 and 64");
+  using F = Fx2<D>;
+  extern __shared__ float4 smem4[];
+  float* Qs = reinterpret_cast<float*>(smem4);  // [kBR][LDQ], scaled, both groups
+  const int grp = threadIdx.x / kThreads, ltid = threadIdx.x % kThreads;
+  float* Kb = Qs + kBR * F::LDQ + grp * F::GROUP;  // buffer b: [kBC][LDQ] at Kb + b KBUF
+  float* Vb = Kb + 2 * F::KBUF;                    // buffer b: [kBC][D] at Vb + b VBUF
+  float* Vp = Vb + 2 * F::VBUF;                    // [kBC / 2][2 D]: key pairs
+  float* Pr = Vp + kBC * D;                        // [kBR][LDP]
+
+  const int ntiles = (S + kBR - 1) / kBR;
+  const int nsplit = ntiles - split_from;
+  const int64_t n = blockIdx.x % N;
+  const int u = (int)(blockIdx.x / N);
+  int qt, kb, ke, pt = -1;
+  if (u < 2 * nsplit) {
+    qt = ntiles - 1 - u / 2;
+    pt = u & 1;
+    const int h = (qt + 2) / 2;
+    kb = pt ? h : 0;
+    ke = pt ? qt : h - 1;
+  } else {
+    qt = split_from - 1 - (u - 2 * nsplit);
+    kb = 0;
+    ke = causal ? qt : ntiles - 1;
+  }
+  const int q0 = qt * kBR;
+  // A half-warp is 8 key columns (tx) x 2 row groups (ty), so each of its 16-byte
+  // shared loads touches at most 128 distinct bytes (one wavefront per half-warp);
+  // a row's 16 tx stay in one warp (lanes differing in bits 0, 1, 2 and 4).
+  const int wl = ltid & 31;
+  const int tx = (wl & 7) | ((wl >> 4) << 3), ty = 2 * (ltid >> 5) + ((wl >> 3) & 1);
+  const float* Qh = Q + n * S * D;
+  const float* Kh = K + n * S * D;
+  const float* Vh = V + n * S * D;
+
+  for (int f = threadIdx.x; f < kBR * (D / 4); f += kFlashThreads) {  // Q rows, scaled; rows >= S read as 0
+    const int r = f / (D / 4), c4 = f % (D / 4);
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (q0 + r < S) x = ld4(Qh + (int64_t)(q0 + r) * D + 4 * c4);
+    st4(Qs + r * F::LDQ + 4 * c4, make_float4(x.x * scale_log2, x.y * scale_log2, x.z * scale_log2,
+                                               x.w * scale_log2));
+  }
+  __syncthreads();
+
+  float m[4], l[4], o[4][F::NO];
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    m[a] = -INFINITY;
+    l[a] = 0.f;
+#pragma unroll
+    for (int j = 0; j < F::NO; ++j) o[a][j] = 0.f;
+  }
+
+  if (kb + grp <= ke) flash_issue_kv<D>(Kb, Vb, Kh, Vh, (kb + grp) * kBC, S, ltid);
+  cp_async_commit();
+  for (int kt = kb + grp, it = 0; kt <= ke; kt += 2, ++it) {
+    const int k0 = kt * kBC;
+    const float* Ks = Kb + (it & 1) * F::KBUF;
+    const float* Vs = Vb + (it & 1) * F::VBUF;
+    // the buffers of the group's previous tile: every thread of the group passed
+    // the previous iteration's second barrier, after its last read of them
+    if (kt + 2 <= ke)
+      flash_issue_kv<D>(Kb + ((it + 1) & 1) * F::KBUF, Vb + ((it + 1) & 1) * F::VBUF, Kh, Vh, k0 + 2 * kBC, S,
+                        ltid);
+    cp_async_commit();
+    cp_async_wait<1>();  // this thread's copies of tile kt have landed
+    group_bar(grp);      // everyone's have; the group's previous P and Vp are no longer read
+
+    // V as key pairs. Per store instruction the 16 lanes of one key pair write
+    // 16-byte chunks 2 c4 + h with h = (c4 / 4) % 2: all eight bank groups.
+    for (int w = ltid; w < (kBC / 2) * (D / 4); w += kThreads) {
+      const int kp = w / (D / 4), c4 = w % (D / 4);
+      const float4 a = ld4(Vs + (2 * kp) * D + 4 * c4), b = ld4(Vs + (2 * kp + 1) * D + 4 * c4);
+      const float4 lo = make_float4(a.x, b.x, a.y, b.y), hi = make_float4(a.z, b.z, a.w, b.w);
+      float* dst = Vp + kp * 2 * D + 8 * c4;
+      const int sw = ((c4 >> 2) & 1) * 4;
+      st4(dst + sw, sw ? hi : lo);
+      st4(dst + 4 - sw, sw ? lo : hi);
+    }
+
+    // scores of rows ty*4 + a and keys tx + 16 b, as even- and odd-feature sums
+    float s[4][4];
+    {
+      float2 s2[4][4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) s2[a][b] = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < D; k += 4) {
+        float4 qv[4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) qv[a] = ld4(Qs + (ty * 4 + a) * F::LDQ + k);
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const float4 kv = ld4(Ks + (tx + 16 * b) * F::LDQ + k);
+#pragma unroll
+          for (int a = 0; a < 4; ++a) {
+            s2[a][b] = __ffma2_rn(make_float2(qv[a].x, qv[a].y), make_float2(kv.x, kv.y), s2[a][b]);
+            s2[a][b] = __ffma2_rn(make_float2(qv[a].z, qv[a].w), make_float2(kv.z, kv.w), s2[a][b]);
+          }
+        }
+      }
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) s[a][b] = s2[a][b].x + s2[a][b].y;
+    }
+
+    // mask, online-softmax update, P row-major
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      const int row = q0 + ty * 4 + a;
+      float tmax = -INFINITY;
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const int key = k0 + tx + 16 * b;
+        if (key >= S || (causal && key > row)) s[a][b] = -INFINITY;
+        tmax = fmaxf(tmax, s[a][b]);
+      }
+      tmax = tx_max(tmax);
+      const float m_new = fmaxf(m[a], tmax);
+      const float m_use = m_new == -INFINITY ? 0.f : m_new;
+      const float alpha = exp2f(m[a] - m_use);
+      float rs = 0.f;
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        s[a][b] = exp2f(s[a][b] - m_use);
+        rs += s[a][b];
+      }
+      rs = tx_sum(rs);
+      l[a] = l[a] * alpha + rs;
+      m[a] = m_new;
+#pragma unroll
+      for (int j = 0; j < F::NO; ++j) o[a][j] *= alpha;
+#pragma unroll
+      for (int b = 0; b < 4; ++b) Pr[(ty * 4 + a) * F::LDP + tx + 16 * b] = s[a][b];
+    }
+    group_bar(grp);  // P and Vp of this tile are visible to the group
+
+    // O += P V over the tile's 64 keys, two keys per paired FMA, as even-key and
+    // odd-key partial sums added into O at the end of the tile
+    float2 acc[4][F::NO];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int j = 0; j < F::NO; ++j) acc[a][j] = make_float2(0.f, 0.f);
+#pragma unroll 4
+    for (int c4 = 0; c4 < kBC / 4; ++c4) {
+      float4 p[4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) p[a] = ld4(Pr + (ty * 4 + a) * F::LDP + 4 * c4);
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+        for (int g = 0; g < F::G; ++g) {
+          const float4 v = ld4(Vp + (2 * c4 + kk) * 2 * D + 64 * g + 4 * tx);
+#pragma unroll
+          for (int a = 0; a < 4; ++a) {
+            const float2 pp = kk == 0 ? make_float2(p[a].x, p[a].y) : make_float2(p[a].z, p[a].w);
+            acc[a][2 * g] = __ffma2_rn(pp, make_float2(v.x, v.y), acc[a][2 * g]);
+            acc[a][2 * g + 1] = __ffma2_rn(pp, make_float2(v.z, v.w), acc[a][2 * g + 1]);
+          }
+        }
+    }
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int j = 0; j < F::NO; ++j) o[a][j] += acc[a][j].x + acc[a][j].y;
+  }
+
+  // merge of the two groups' online softmaxes, as in flash_f32_kernel; output
+  // column of the thread's value j: 32 (j / 2) + 2 tx + j % 2
+  float* X = Qs + kBR * F::LDQ + F::GROUP;  // group 1's buffers
+  static_assert((8 + 4 * F::NO) * kThreads <= F::GROUP, "merge state fits in one group's buffers");
+  __syncthreads();
+  if (grp == 1) {
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      X[a * kThreads + ltid] = m[a];
+      X[(4 + a) * kThreads + ltid] = l[a];
+#pragma unroll
+      for (int j = 0; j < F::NO; ++j) X[(8 + a * F::NO + j) * kThreads + ltid] = o[a][j];
+    }
+  }
+  __syncthreads();
+  if (grp == 1) return;
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    const int row = q0 + ty * 4 + a;
+    const float m1 = X[a * kThreads + ltid], l1 = X[(4 + a) * kThreads + ltid];
+    const float mm = fmaxf(m[a], m1);
+    const float s0 = exp2f(m[a] - mm);
+    const float s1 = m1 == -INFINITY ? 0.f : exp2f(m1 - mm);
+    const float lt = l[a] * s0 + l1 * s1;
+    if (row >= S) continue;
+    float val[F::NO];
+#pragma unroll
+    for (int j = 0; j < F::NO; ++j) val[j] = o[a][j] * s0 + X[(8 + a * F::NO + j) * kThreads + ltid] * s1;
+    if (pt >= 0) {  // a part of a split tile: its state, for flash_merge_kernel
+      const int lr = ty * 4 + a;
+      float* st = part + ((n * nsplit + (ntiles - 1 - qt)) * 2 + pt) * (int64_t)(kBR * (D + 2));
+      if (tx == 0) {
+        st[lr] = mm;
+        st[kBR + lr] = lt;
+      }
+#pragma unroll
+      for (int g = 0; g < F::G; ++g)
+        *reinterpret_cast<float2*>(st + 2 * kBR + lr * D + 32 * g + 2 * tx) = make_float2(val[2 * g], val[2 * g + 1]);
+      continue;
+    }
+    const float inv = 1.0f / lt;
+    if (lse != nullptr && tx == 0) lse[n * S + row] = (mm + log2f(lt)) * 0.6931471805599453f;
+    float* orow = O + (n * S + row) * D;
+#pragma unroll
+    for (int g = 0; g < F::G; ++g)
+      *reinterpret_cast<float2*>(orow + 32 * g + 2 * tx) = make_float2(val[2 * g] * inv, val[2 * g + 1] * inv);
+  }
+}
+
 // Combines the two parts of every split query tile: O = (acc0 s0 + acc1 s1) / l
 // with s_p = 2^(m_p - max(m0, m1)), l = l0 s0 + l1 s1 (two online-softmax states
 // over disjoint key ranges, combined like the flash kernel's own group merge).
@@ -769,8 +1041,9 @@ __global__ void __launch_bounds__(kFusedThreads) fused_row_f32_kernel(const floa
 }
 
 size_t flash_smem(int d) {
-  const int group = d == 32 ? flash_group_floats<32>() : d == 64 ? flash_group_floats<64>() : flash_group_floats<128>();
-  return sizeof(float) * (size_t)(d * kLD + 2 * group);
+  if (d == 32) return sizeof(float) * (size_t)Fx2<32>::SMEM_FLOATS;
+  if (d == 64) return sizeof(float) * (size_t)Fx2<64>::SMEM_FLOATS;
+  return sizeof(float) * (size_t)(d * kLD + 2 * flash_group_floats<128>());
 }
 size_t naive_scores_smem(int d) { return sizeof(float) * (size_t)(d * kLD + kBC * (d + 4)); }
 size_t naive_pv_smem(int d) { return sizeof(float) * (size_t)(2 * 2 * (kBR * kLDP + kBC * d)); }
@@ -784,20 +1057,30 @@ cudaError_t set_smem(F* kernel, size_t bytes) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
-template <int D>
-cudaError_t flash_launch(const AttnProblem& p, cudaStream_t st) {
+// d <= 64: the paired-FMA kernel; d = 128: flash_f32_kernel (its two groups'
+// single-buffered K/V tiles and the re-laid V would not fit beside each other).
+template <int D, typename Kernel>
+cudaError_t flash_launch(Kernel kernel, const AttnProblem& p, cudaStream_t st) {
   const size_t smem = flash_smem(D);
-  cudaError_t e = set_smem(flash_f32_kernel<D>, smem);
+  cudaError_t e = set_smem(kernel, smem);
   if (e != cudaSuccess) return e;
   const int tiles = (p.S + kBR - 1) / kBR;
   const int split_from = p.work ? (tiles + 1) / 2 : tiles;
   const int nsplit = tiles - split_from;
-  flash_f32_kernel<D><<<(unsigned)((tiles + nsplit) * p.N), kFlashThreads, smem, st>>>(
+  kernel<<<(unsigned)((tiles + nsplit) * p.N), kFlashThreads, smem, st>>>(
       (const float*)p.q, (const float*)p.k, (const float*)p.v, (float*)p.o, p.lse, p.N, p.S, p.causal,
       p.scale * kLog2e, p.work, split_from);
   if (nsplit > 0 && (e = cudaGetLastError()) == cudaSuccess)
     flash_merge_kernel<D><<<(unsigned)(nsplit * p.N), 256, 0, st>>>(p.work, (float*)p.o, p.lse, p.S, nsplit);
   return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t flash_launch(const AttnProblem& p, cudaStream_t st) {
+  if constexpr (D <= 64)
+    return flash_launch<D>(flash_f32x2_kernel<D>, p, st);
+  else
+    return flash_launch<D>(flash_f32_kernel<D>, p, st);
 }
 
 template <int D>

@@ -54,8 +54,8 @@ def test_roofline_kernel_follows_the_workload():
             "bf16_b16h12s2048d64": ("attn_tc_kernel<64,bf16>", "tensor"),
             "f16_b16h12s2048d64": ("attn_tc_kernel<64,f16>", "tensor"),
             "bf16_causal_b2h16s4096d256": ("attn_tc256_kernel<bf16>", "tensor"),
-            "f32_b1h8s1024d64": ("flash_f32_kernel", "alu"),
-            "f32_b1h8s1024d64_causal": ("flash_f32_kernel + flash_merge_kernel", "alu")}
+            "f32_b1h8s1024d64": ("flash_f32x2_kernel", "alu"),
+            "f32_b1h8s1024d64_causal": ("flash_f32x2_kernel + flash_merge_kernel", "alu")}
     for name, (kernel, bound) in want.items():
         k = bench.kernel_for(inputs.WORKLOADS[name], 152)
         assert (k["kernel"], k["bound"]) == (kernel, bound), name
