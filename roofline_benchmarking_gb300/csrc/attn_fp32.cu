@@ -139,16 +139,17 @@ template <int D>
 constexpr int flash_ldk() { return D + 4; }
 
 // One group's copies of key tile [k0, k0 + 64): K row-major into Kr[r * (D + 4) + k]
-// and V row-major into Vr[r * D + c], 16-byte copies; rows >= S are zero-filled.
+// and V row-major into Vr[r * D + c], 16-byte copies by the group's `nthreads`
+// threads; rows >= S are zero-filled.
 template <int D>
 __device__ __forceinline__ void flash_issue_kv(float* Kr, float* Vr, const float* Kh, const float* Vh, int k0, int S,
-                                               int tid) {
-  for (int f = tid; f < kBC * (D / 4); f += kThreads) {
+                                               int tid, int nthreads = kThreads) {
+  for (int f = tid; f < kBC * (D / 4); f += nthreads) {
     const int r = f / (D / 4), c4 = f % (D / 4);
     const bool ok = k0 + r < S;
     cp_async<16>(Kr + r * flash_ldk<D>() + 4 * c4, Kh + (int64_t)(ok ? k0 + r : 0) * D + 4 * c4, ok);
   }
-  for (int f = tid; f < kBC * (D / 4); f += kThreads) {
+  for (int f = tid; f < kBC * (D / 4); f += nthreads) {
     const int r = f / (D / 4), c4 = f % (D / 4);
     const bool ok = k0 + r < S;
     cp_async<16>(Vr + r * D + 4 * c4, Vh + (int64_t)(ok ? k0 + r : 0) * D + 4 * c4, ok);
@@ -379,25 +380,32 @@ __global__ void __launch_bounds__(kFlashThreads, 1) flash_f32_kernel(const float
 // ---------------------------------------------------------------------------
 // flash at d <= 64 with paired fp32 FMAs (fma.rn.f32x2: two products per lane
 // and instruction; the FMA pipe's rate per product is that of the scalar FMA,
-// measured on GB300, but each instruction issues two). Blocks, the two thread
-// groups over even and odd key tiles, the causal split and the merge are those
-// of flash_f32_kernel; what changes is the shared-memory layout of the two tile
-// products, so that each paired FMA finds both of its operand pairs in
-// adjacent registers of one 16-byte load:
+// measured on GB300, but each instruction issues two). The query tile, the two
+// thread groups over even and odd key tiles, the causal split and the merge are
+// those of flash_f32_kernel. What changes:
 //  * Q K^T: Q and K row-major; one paired FMA takes features (k, k+1) of a
 //    query row and of a key, so each score is carried as two partial sums
 //    (even and odd features) that are added once per tile;
 //  * P V: P row-major as the softmax writes it; V re-laid from its row-major
 //    copy into key pairs, Vp[j/2][c] = (V[j][c], V[j+1][c]), so one paired FMA
 //    takes keys (j, j+1) of a P row and of a V column; each output gathers
-//    even-key and odd-key partial sums over a tile, added into O after it.
-// A thread owns query rows ty*4 + a, keys tx + 16 b and output columns
-// 32 g + 2 tx + e (e < 2, g < D / 32); the lanes of a warp hold two row groups.
+//    even-key and odd-key partial sums over a tile, added into O after it;
+//  * register tiles of 8 rows x 4 keys (and 8 rows x 4 output columns), with
+//    groups of 128 threads at up to 255 registers. A 16-byte shared load
+//    costs about 4 wavefronts when the lanes read distinct rows (K, V) and 2
+//    when each half-warp reads one row (Q, P) (measured); with 4 x 4 tiles a
+//    warp's 32 paired FMAs per 4 features took 24 wavefronts for 16 cycles of
+//    FMA-pipe work, with 8 x 4 tiles its 64 take 32 wavefronts for 32 cycles.
+// Thread (tx, ty) of a group owns query rows ty + 8 a (a < 8), keys tx + 16 b
+// (b < 4) and output columns 32 g + 2 tx + e (e < 2, g < D / 32).
 // ---------------------------------------------------------------------------
+constexpr int kFx2Group = 128;              // threads per key-tile group
+constexpr int kFx2Threads = 2 * kFx2Group;  // two groups: even and odd key tiles
+
 template <int D>
 struct Fx2 {
   static constexpr int LDQ = D + 4;       // row stride of the Q and K tiles
-  static constexpr int LDP = kBC + 4;     // row stride of the P tile
+  static constexpr int LDP = kBC + 16;    // row stride of the P tile: rows ty and ty + 1 16 banks apart
   static constexpr int G = D / 32;        // column groups of a thread
   static constexpr int NO = 2 * G;        // output columns of a thread per row
   static constexpr int KBUF = kBC * LDQ;  // one K buffer
@@ -408,30 +416,23 @@ struct Fx2 {
 
 __device__ __forceinline__ void st4(float* p, float4 x) { *reinterpret_cast<float4*>(p) = x; }
 
-// Max and sum over the 16 lanes of a row (lane bits 0, 1, 2 and 4).
-__device__ __forceinline__ float tx_max(float x) {
-#pragma unroll
-  for (int o : {1, 2, 4, 16}) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-  return x;
-}
-__device__ __forceinline__ float tx_sum(float x) {
-#pragma unroll
-  for (int o : {1, 2, 4, 16}) x += __shfl_xor_sync(0xffffffffu, x, o);
-  return x;
+__device__ __forceinline__ void fx2_group_bar(int grp) {
+  asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "r"(kFx2Group) : "memory");
 }
 
 template <int D>
-__global__ void __launch_bounds__(kFlashThreads, 1) flash_f32x2_kernel(const float* __restrict__ Q,
-                                                                    const float* __restrict__ K,
-                                                                    const float* __restrict__ V,
-                                                                    float* __restrict__ O, float* __restrict__ lse,
-                                                                    int64_t N, int S, int causal, float scale_log2,
-                                                                    float* __restrict__ part, int split_from) {
+__global__ void __launch_bounds__(kFx2Threads, 1) flash_f32x2_kernel(const float* __restrict__ Q,
+                                                                  const float* __restrict__ K,
+                                                                  const float* __restrict__ V,
+                                                                  float* __restrict__ O, float* __restrict__ lse,
+                                                                  int64_t N, int S, int causal, float scale_log2,
+                                                                  float* __restrict__ part, int split_from) {
   static_assert(D == 32 || D == 64, "the paired-FMA flash kernel runs d = 32 and 64");
   using F = Fx2<D>;
+  constexpr int RT = 8;  // query rows per thread
   extern __shared__ float4 smem4[];
   float* Qs = reinterpret_cast<float*>(smem4);  // [kBR][LDQ], scaled, both groups
-  const int grp = threadIdx.x / kThreads, ltid = threadIdx.x % kThreads;
+  const int grp = threadIdx.x / kFx2Group, ltid = threadIdx.x % kFx2Group;
   float* Kb = Qs + kBR * F::LDQ + grp * F::GROUP;  // buffer b: [kBC][LDQ] at Kb + b KBUF
   float* Vb = Kb + 2 * F::KBUF;                    // buffer b: [kBC][D] at Vb + b VBUF
   float* Vp = Vb + 2 * F::VBUF;                    // [kBC / 2][2 D]: key pairs
@@ -454,16 +455,12 @@ __global__ void __launch_bounds__(kFlashThreads, 1) flash_f32x2_kernel(const flo
     ke = causal ? qt : ntiles - 1;
   }
   const int q0 = qt * kBR;
-  // A half-warp is 8 key columns (tx) x 2 row groups (ty), so each of its 16-byte
-  // shared loads touches at most 128 distinct bytes (one wavefront per half-warp);
-  // a row's 16 tx stay in one warp (lanes differing in bits 0, 1, 2 and 4).
-  const int wl = ltid & 31;
-  const int tx = (wl & 7) | ((wl >> 4) << 3), ty = 2 * (ltid >> 5) + ((wl >> 3) & 1);
+  const int tx = ltid & 15, ty = ltid >> 4;  // a half-warp shares ty: its row's 16 key lanes
   const float* Qh = Q + n * S * D;
   const float* Kh = K + n * S * D;
   const float* Vh = V + n * S * D;
 
-  for (int f = threadIdx.x; f < kBR * (D / 4); f += kFlashThreads) {  // Q rows, scaled; rows >= S read as 0
+  for (int f = threadIdx.x; f < kBR * (D / 4); f += kFx2Threads) {  // Q rows, scaled; rows >= S read as 0
     const int r = f / (D / 4), c4 = f % (D / 4);
     float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
     if (q0 + r < S) x = ld4(Qh + (int64_t)(q0 + r) * D + 4 * c4);
@@ -472,16 +469,16 @@ __global__ void __launch_bounds__(kFlashThreads, 1) flash_f32x2_kernel(const flo
   }
   __syncthreads();
 
-  float m[4], l[4], o[4][F::NO];
+  float m[RT], l[RT], o[RT][F::NO];
 #pragma unroll
-  for (int a = 0; a < 4; ++a) {
+  for (int a = 0; a < RT; ++a) {
     m[a] = -INFINITY;
     l[a] = 0.f;
 #pragma unroll
     for (int j = 0; j < F::NO; ++j) o[a][j] = 0.f;
   }
 
-  if (kb + grp <= ke) flash_issue_kv<D>(Kb, Vb, Kh, Vh, (kb + grp) * kBC, S, ltid);
+  if (kb + grp <= ke) flash_issue_kv<D>(Kb, Vb, Kh, Vh, (kb + grp) * kBC, S, ltid, kFx2Group);
   cp_async_commit();
   for (int kt = kb + grp, it = 0; kt <= ke; kt += 2, ++it) {
     const int k0 = kt * kBC;
@@ -491,14 +488,14 @@ __global__ void __launch_bounds__(kFlashThreads, 1) flash_f32x2_kernel(const flo
     // the previous iteration's second barrier, after its last read of them
     if (kt + 2 <= ke)
       flash_issue_kv<D>(Kb + ((it + 1) & 1) * F::KBUF, Vb + ((it + 1) & 1) * F::VBUF, Kh, Vh, k0 + 2 * kBC, S,
-                        ltid);
+                        ltid, kFx2Group);
     cp_async_commit();
     cp_async_wait<1>();  // this thread's copies of tile kt have landed
-    group_bar(grp);      // everyone's have; the group's previous P and Vp are no longer read
+    fx2_group_bar(grp);  // everyone's have; the group's previous P and Vp are no longer read
 
-    // V as key pairs. Per store instruction the 16 lanes of one key pair write
+    // V as key pairs. Per store instruction the lanes of one key pair write
     // 16-byte chunks 2 c4 + h with h = (c4 / 4) % 2: all eight bank groups.
-    for (int w = ltid; w < (kBC / 2) * (D / 4); w += kThreads) {
+    for (int w = ltid; w < (kBC / 2) * (D / 4); w += kFx2Group) {
       const int kp = w / (D / 4), c4 = w % (D / 4);
       const float4 a = ld4(Vs + (2 * kp) * D + 4 * c4), b = ld4(Vs + (2 * kp + 1) * D + 4 * c4);
       const float4 lo = make_float4(a.x, b.x, a.y, b.y), hi = make_float4(a.z, b.z, a.w, b.w);
@@ -508,39 +505,39 @@ __global__ void __launch_bounds__(kFlashThreads, 1) flash_f32x2_kernel(const flo
       st4(dst + 4 - sw, sw ? lo : hi);
     }
 
-    // scores of rows ty*4 + a and keys tx + 16 b, as even- and odd-feature sums
-    float s[4][4];
+    // scores of rows ty + 8 a and keys tx + 16 b, as even- and odd-feature sums
+    float s[RT][4];
     {
-      float2 s2[4][4];
+      float2 s2[RT][4];
 #pragma unroll
-      for (int a = 0; a < 4; ++a)
+      for (int a = 0; a < RT; ++a)
 #pragma unroll
         for (int b = 0; b < 4; ++b) s2[a][b] = make_float2(0.f, 0.f);
 #pragma unroll
       for (int k = 0; k < D; k += 4) {
-        float4 qv[4];
+        float4 kv[4];
 #pragma unroll
-        for (int a = 0; a < 4; ++a) qv[a] = ld4(Qs + (ty * 4 + a) * F::LDQ + k);
+        for (int b = 0; b < 4; ++b) kv[b] = ld4(Ks + (tx + 16 * b) * F::LDQ + k);
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          const float4 kv = ld4(Ks + (tx + 16 * b) * F::LDQ + k);
+        for (int a = 0; a < RT; ++a) {
+          const float4 qv = ld4(Qs + (ty + 8 * a) * F::LDQ + k);
 #pragma unroll
-          for (int a = 0; a < 4; ++a) {
-            s2[a][b] = __ffma2_rn(make_float2(qv[a].x, qv[a].y), make_float2(kv.x, kv.y), s2[a][b]);
-            s2[a][b] = __ffma2_rn(make_float2(qv[a].z, qv[a].w), make_float2(kv.z, kv.w), s2[a][b]);
+          for (int b = 0; b < 4; ++b) {
+            s2[a][b] = __ffma2_rn(make_float2(qv.x, qv.y), make_float2(kv[b].x, kv[b].y), s2[a][b]);
+            s2[a][b] = __ffma2_rn(make_float2(qv.z, qv.w), make_float2(kv[b].z, kv[b].w), s2[a][b]);
           }
         }
       }
 #pragma unroll
-      for (int a = 0; a < 4; ++a)
+      for (int a = 0; a < RT; ++a)
 #pragma unroll
         for (int b = 0; b < 4; ++b) s[a][b] = s2[a][b].x + s2[a][b].y;
     }
 
     // mask, online-softmax update, P row-major
 #pragma unroll
-    for (int a = 0; a < 4; ++a) {
-      const int row = q0 + ty * 4 + a;
+    for (int a = 0; a < RT; ++a) {
+      const int row = q0 + ty + 8 * a;
       float tmax = -INFINITY;
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
@@ -548,7 +545,7 @@ __global__ void __launch_bounds__(kFlashThreads, 1) flash_f32x2_kernel(const flo
         if (key >= S || (causal && key > row)) s[a][b] = -INFINITY;
         tmax = fmaxf(tmax, s[a][b]);
       }
-      tmax = tx_max(tmax);
+      tmax = group_max<16>(tmax);
       const float m_new = fmaxf(m[a], tmax);
       const float m_use = m_new == -INFINITY ? 0.f : m_new;
       const float alpha = exp2f(m[a] - m_use);
@@ -558,43 +555,46 @@ __global__ void __launch_bounds__(kFlashThreads, 1) flash_f32x2_kernel(const flo
         s[a][b] = exp2f(s[a][b] - m_use);
         rs += s[a][b];
       }
-      rs = tx_sum(rs);
+      rs = group_sum<16>(rs);
       l[a] = l[a] * alpha + rs;
       m[a] = m_new;
 #pragma unroll
       for (int j = 0; j < F::NO; ++j) o[a][j] *= alpha;
 #pragma unroll
-      for (int b = 0; b < 4; ++b) Pr[(ty * 4 + a) * F::LDP + tx + 16 * b] = s[a][b];
+      for (int b = 0; b < 4; ++b) Pr[(ty + 8 * a) * F::LDP + tx + 16 * b] = s[a][b];
     }
-    group_bar(grp);  // P and Vp of this tile are visible to the group
+    fx2_group_bar(grp);  // P and Vp of this tile are visible to the group
 
     // O += P V over the tile's 64 keys, two keys per paired FMA, as even-key and
     // odd-key partial sums added into O at the end of the tile
-    float2 acc[4][F::NO];
+    float2 acc[RT][F::NO];
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
+    for (int a = 0; a < RT; ++a)
 #pragma unroll
       for (int j = 0; j < F::NO; ++j) acc[a][j] = make_float2(0.f, 0.f);
-#pragma unroll 4
+#pragma unroll 2
     for (int c4 = 0; c4 < kBC / 4; ++c4) {
-      float4 p[4];
-#pragma unroll
-      for (int a = 0; a < 4; ++a) p[a] = ld4(Pr + (ty * 4 + a) * F::LDP + 4 * c4);
+      float4 v[2][F::G];
 #pragma unroll
       for (int kk = 0; kk < 2; ++kk)
 #pragma unroll
-        for (int g = 0; g < F::G; ++g) {
-          const float4 v = ld4(Vp + (2 * c4 + kk) * 2 * D + 64 * g + 4 * tx);
+        for (int g = 0; g < F::G; ++g) v[kk][g] = ld4(Vp + (2 * c4 + kk) * 2 * D + 64 * g + 4 * tx);
 #pragma unroll
-          for (int a = 0; a < 4; ++a) {
-            const float2 pp = kk == 0 ? make_float2(p[a].x, p[a].y) : make_float2(p[a].z, p[a].w);
-            acc[a][2 * g] = __ffma2_rn(pp, make_float2(v.x, v.y), acc[a][2 * g]);
-            acc[a][2 * g + 1] = __ffma2_rn(pp, make_float2(v.z, v.w), acc[a][2 * g + 1]);
+      for (int a = 0; a < RT; ++a) {
+        const float4 p = ld4(Pr + (ty + 8 * a) * F::LDP + 4 * c4);
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+          const float2 pp = kk == 0 ? make_float2(p.x, p.y) : make_float2(p.z, p.w);
+#pragma unroll
+          for (int g = 0; g < F::G; ++g) {
+            acc[a][2 * g] = __ffma2_rn(pp, make_float2(v[kk][g].x, v[kk][g].y), acc[a][2 * g]);
+            acc[a][2 * g + 1] = __ffma2_rn(pp, make_float2(v[kk][g].z, v[kk][g].w), acc[a][2 * g + 1]);
           }
         }
+      }
     }
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
+    for (int a = 0; a < RT; ++a)
 #pragma unroll
       for (int j = 0; j < F::NO; ++j) o[a][j] += acc[a][j].x + acc[a][j].y;
   }
@@ -602,23 +602,24 @@ __global__ void __launch_bounds__(kFlashThreads, 1) flash_f32x2_kernel(const flo
   // merge of the two groups' online softmaxes, as in flash_f32_kernel; output
   // column of the thread's value j: 32 (j / 2) + 2 tx + j % 2
   float* X = Qs + kBR * F::LDQ + F::GROUP;  // group 1's buffers
-  static_assert((8 + 4 * F::NO) * kThreads <= F::GROUP, "merge state fits in one group's buffers");
+  constexpr int FIELDS = 2 * RT + RT * F::NO;
+  static_assert(FIELDS * kFx2Group <= F::GROUP, "merge state fits in one group's buffers");
   __syncthreads();
   if (grp == 1) {
 #pragma unroll
-    for (int a = 0; a < 4; ++a) {
-      X[a * kThreads + ltid] = m[a];
-      X[(4 + a) * kThreads + ltid] = l[a];
+    for (int a = 0; a < RT; ++a) {
+      X[a * kFx2Group + ltid] = m[a];
+      X[(RT + a) * kFx2Group + ltid] = l[a];
 #pragma unroll
-      for (int j = 0; j < F::NO; ++j) X[(8 + a * F::NO + j) * kThreads + ltid] = o[a][j];
+      for (int j = 0; j < F::NO; ++j) X[(2 * RT + a * F::NO + j) * kFx2Group + ltid] = o[a][j];
     }
   }
   __syncthreads();
   if (grp == 1) return;
 #pragma unroll
-  for (int a = 0; a < 4; ++a) {
-    const int row = q0 + ty * 4 + a;
-    const float m1 = X[a * kThreads + ltid], l1 = X[(4 + a) * kThreads + ltid];
+  for (int a = 0; a < RT; ++a) {
+    const int lr = ty + 8 * a, row = q0 + lr;
+    const float m1 = X[a * kFx2Group + ltid], l1 = X[(RT + a) * kFx2Group + ltid];
     const float mm = fmaxf(m[a], m1);
     const float s0 = exp2f(m[a] - mm);
     const float s1 = m1 == -INFINITY ? 0.f : exp2f(m1 - mm);
@@ -626,9 +627,8 @@ __global__ void __launch_bounds__(kFlashThreads, 1) flash_f32x2_kernel(const flo
     if (row >= S) continue;
     float val[F::NO];
 #pragma unroll
-    for (int j = 0; j < F::NO; ++j) val[j] = o[a][j] * s0 + X[(8 + a * F::NO + j) * kThreads + ltid] * s1;
+    for (int j = 0; j < F::NO; ++j) val[j] = o[a][j] * s0 + X[(2 * RT + a * F::NO + j) * kFx2Group + ltid] * s1;
     if (pt >= 0) {  // a part of a split tile: its state, for flash_merge_kernel
-      const int lr = ty * 4 + a;
       float* st = part + ((n * nsplit + (ntiles - 1 - qt)) * 2 + pt) * (int64_t)(kBR * (D + 2));
       if (tx == 0) {
         st[lr] = mm;
@@ -1060,14 +1060,14 @@ cudaError_t set_smem(F* kernel, size_t bytes) {
 // d <= 64: the paired-FMA kernel; d = 128: flash_f32_kernel (its two groups'
 // single-buffered K/V tiles and the re-laid V would not fit beside each other).
 template <int D, typename Kernel>
-cudaError_t flash_launch(Kernel kernel, const AttnProblem& p, cudaStream_t st) {
+cudaError_t flash_launch(Kernel kernel, int threads, const AttnProblem& p, cudaStream_t st) {
   const size_t smem = flash_smem(D);
   cudaError_t e = set_smem(kernel, smem);
   if (e != cudaSuccess) return e;
   const int tiles = (p.S + kBR - 1) / kBR;
   const int split_from = p.work ? (tiles + 1) / 2 : tiles;
   const int nsplit = tiles - split_from;
-  kernel<<<(unsigned)((tiles + nsplit) * p.N), kFlashThreads, smem, st>>>(
+  kernel<<<(unsigned)((tiles + nsplit) * p.N), threads, smem, st>>>(
       (const float*)p.q, (const float*)p.k, (const float*)p.v, (float*)p.o, p.lse, p.N, p.S, p.causal,
       p.scale * kLog2e, p.work, split_from);
   if (nsplit > 0 && (e = cudaGetLastError()) == cudaSuccess)
@@ -1078,9 +1078,9 @@ cudaError_t flash_launch(Kernel kernel, const AttnProblem& p, cudaStream_t st) {
 template <int D>
 cudaError_t flash_launch(const AttnProblem& p, cudaStream_t st) {
   if constexpr (D <= 64)
-    return flash_launch<D>(flash_f32x2_kernel<D>, p, st);
+    return flash_launch<D>(flash_f32x2_kernel<D>, kFx2Threads, p, st);
   else
-    return flash_launch<D>(flash_f32_kernel<D>, p, st);
+    return flash_launch<D>(flash_f32_kernel<D>, kFlashThreads, p, st);
 }
 
 template <int D>
