@@ -513,20 +513,25 @@ __global__ void __launch_bounds__(kFx2Threads, 1) flash_f32x2_kernel(const float
       for (int a = 0; a < RT; ++a)
 #pragma unroll
         for (int b = 0; b < 4; ++b) s2[a][b] = make_float2(0.f, 0.f);
+      // per 4 features: all 32 products of features (k, k+1), then those of
+      // (k+2, k+3), so that the two FMAs into one accumulator are 32 apart
 #pragma unroll
       for (int k = 0; k < D; k += 4) {
-        float4 kv[4];
+        float4 kv[4], qv[RT];
 #pragma unroll
         for (int b = 0; b < 4; ++b) kv[b] = ld4(Ks + (tx + 16 * b) * F::LDQ + k);
 #pragma unroll
-        for (int a = 0; a < RT; ++a) {
-          const float4 qv = ld4(Qs + (ty + 8 * a) * F::LDQ + k);
+        for (int a = 0; a < RT; ++a) qv[a] = ld4(Qs + (ty + 8 * a) * F::LDQ + k);
 #pragma unroll
-          for (int b = 0; b < 4; ++b) {
-            s2[a][b] = __ffma2_rn(make_float2(qv.x, qv.y), make_float2(kv[b].x, kv[b].y), s2[a][b]);
-            s2[a][b] = __ffma2_rn(make_float2(qv.z, qv.w), make_float2(kv[b].z, kv[b].w), s2[a][b]);
-          }
-        }
+        for (int a = 0; a < RT; ++a)
+#pragma unroll
+          for (int b = 0; b < 4; ++b)
+            s2[a][b] = __ffma2_rn(make_float2(qv[a].x, qv[a].y), make_float2(kv[b].x, kv[b].y), s2[a][b]);
+#pragma unroll
+        for (int a = 0; a < RT; ++a)
+#pragma unroll
+          for (int b = 0; b < 4; ++b)
+            s2[a][b] = __ffma2_rn(make_float2(qv[a].z, qv[a].w), make_float2(kv[b].z, kv[b].w), s2[a][b]);
       }
 #pragma unroll
       for (int a = 0; a < RT; ++a)
@@ -579,19 +584,20 @@ __global__ void __launch_bounds__(kFx2Threads, 1) flash_f32x2_kernel(const float
       for (int kk = 0; kk < 2; ++kk)
 #pragma unroll
         for (int g = 0; g < F::G; ++g) v[kk][g] = ld4(Vp + (2 * c4 + kk) * 2 * D + 64 * g + 4 * tx);
+      float4 p[RT];
 #pragma unroll
-      for (int a = 0; a < RT; ++a) {
-        const float4 p = ld4(Pr + (ty + 8 * a) * F::LDP + 4 * c4);
+      for (int a = 0; a < RT; ++a) p[a] = ld4(Pr + (ty + 8 * a) * F::LDP + 4 * c4);
 #pragma unroll
-        for (int kk = 0; kk < 2; ++kk) {
-          const float2 pp = kk == 0 ? make_float2(p.x, p.y) : make_float2(p.z, p.w);
+      for (int kk = 0; kk < 2; ++kk)  // key pair 2 c4 + kk for every row, then the next
+#pragma unroll
+        for (int a = 0; a < RT; ++a) {
+          const float2 pp = kk == 0 ? make_float2(p[a].x, p[a].y) : make_float2(p[a].z, p[a].w);
 #pragma unroll
           for (int g = 0; g < F::G; ++g) {
             acc[a][2 * g] = __ffma2_rn(pp, make_float2(v[kk][g].x, v[kk][g].y), acc[a][2 * g]);
             acc[a][2 * g + 1] = __ffma2_rn(pp, make_float2(v[kk][g].z, v[kk][g].w), acc[a][2 * g + 1]);
           }
         }
-      }
     }
 #pragma unroll
     for (int a = 0; a < RT; ++a)
