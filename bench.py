@@ -192,7 +192,7 @@ def kernel_for(w, sms: int) -> dict:
                               "measured bf16 burst (cuBLAS 8192^3) x 1, the nominal fp16:bf16 dense ratio")}
     if w.dtype == "q15":
         return {"kernel": "q15_attn_kernel", "bound": "alu", "launches_per_step": 1, "peak_key": None,
-                "peak_note": "integer multiply-add lanes (see DESIGN.md)"}
+                "peak_note": "integer multiply-add lanes: SMs x 64 dp2a lanes x 2 x max SM clock"}
     # the library splits the heavier causal query tiles over two blocks on small grids
     # (N * ceil(S / 64) <= 2 x SMs, S >= 256) and merges them in a second launch
     tiles = (w.S + 63) // 64
