@@ -898,10 +898,14 @@ __global__ void __launch_bounds__(kFlashThreads, 1) naive_pv_kernel(const float*
 // O(S)). A block takes R consecutive query rows of one head (R = 4 where their
 // R score rows fit in shared memory and the grid keeps two blocks per SM, else
 // 2 or 1 -- R = 1 is the page's layout and sets the same S cap), so every K and
-// V element read from L2 serves R rows. Key tiles of 64 keys are staged in shared memory with coalesced
-// loads; each dot product is split over 4 threads, thread q of a key taking
-// float4 q, q + 4, ...; rows are padded by 16 floats so that the 8 threads of
-// one 128-bit load phase (2 keys x 4 parts) touch 8 distinct bank groups.
+// V element read from L2 serves R rows. Key tiles of 64 keys, of K in the score
+// pass and of V in the P V pass, are staged in two shared-memory buffers by
+// cp.async, the next tile's copies in flight while the current one is used;
+// each dot product is split over 4 threads, thread q of a key taking float4 q,
+// q + 4, ...; K rows are padded by 16 floats so that the 8 threads of one
+// 128-bit load phase (2 keys x 4 parts) touch 8 distinct bank groups. In the
+// P V pass a thread takes one output column and every G-th quad of keys, the
+// four weights of a quad read with one 16-byte load per row.
 // Masked keys (past a row's causal limit) hold -inf, so every row of the block
 // runs over the same key range and gets probability 0 there.
 // ---------------------------------------------------------------------------
@@ -943,12 +947,15 @@ __global__ void __launch_bounds__(kFusedThreads) fused_row_f32_kernel(const floa
                                                                       float scale_log2) {
   constexpr int LDK = D + 16;
   constexpr int G = kFusedThreads / D;  // key groups of the P V pass
+  constexpr int QUADS = kFusedKeys / 4;  // key quads of a tile
+  static_assert(QUADS % G == 0, "the key quads of a tile split evenly over the key groups");
   extern __shared__ float4 smem4[];
-  float* Ks = reinterpret_cast<float*>(smem4);  // [kFusedKeys][LDK]
-  float* qs = Ks + kFusedKeys * LDK;             // [R][D]
+  float* buf = reinterpret_cast<float*>(smem4);  // two tile buffers: K [kFusedKeys][LDK], later V [kFusedKeys][D]
+  float* qs = buf + 2 * kFusedKeys * LDK;        // [R][D]
   float* red = qs + R * D;                       // [kFusedWarps * R]
   float* part = red + kFusedWarps * R;           // [R][kFusedThreads]
-  float* sc = part + R * kFusedThreads;          // [R][S]
+  float* sc = part + R * kFusedThreads;          // [R][SP]
+  const int SP = (S + 3) & ~3;                   // score row stride: 16-byte aligned rows
   const int tiles = (S + R - 1) / R;
   // heads interleaved, the last (causal: heaviest) row tiles first
   const int64_t nheads = gridDim.x / tiles;
@@ -956,28 +963,39 @@ __global__ void __launch_bounds__(kFusedThreads) fused_row_f32_kernel(const floa
   const int i0 = (tiles - 1 - (int)(blockIdx.x / nheads)) * R;
   const int tid = threadIdx.x;
   const int last_block = causal ? min(i0 + R - 1, S - 1) : S - 1;  // keys any row of the block sees
+  const int nt = last_block / kFusedKeys + 1;                       // key tiles
   const float* Kh = K + n * S * D;
   const float* Vh = V + n * S * D;
+  auto tile_buf = [&](int b) { return buf + (b & 1) * kFusedKeys * LDK; };
+  // cp.async copies of key tile t of K or V (row stride ld) into dst; rows past
+  // last_block are zero-filled and read nothing
+  auto issue = [&](const float* src, int ld, int t, float* dst) {
+    const int k0 = t * kFusedKeys;
+    for (int f = tid; f < kFusedKeys * (D / 4); f += kFusedThreads) {
+      const int r = f / (D / 4), c4 = f % (D / 4);
+      const bool ok = k0 + r <= last_block;
+      cp_async<16>(dst + r * ld + 4 * c4, src + (int64_t)(ok ? k0 + r : 0) * D + 4 * c4, ok);
+    }
+    cp_async_commit();
+  };
 
+  issue(Kh, LDK, 0, tile_buf(0));
   for (int f = tid; f < R * D; f += kFusedThreads) {
     const int r = f / D, c = f % D;
     qs[f] = i0 + r < S ? Q[(n * S + i0 + r) * D + c] * scale_log2 : 0.f;
   }
 
-  // scores: thread tid works on key tid / 4 of the tile, float4 (tid % 4) + 4 t, for all R rows
+  // scores: thread tid works on key tid / 4 of the tile, float4 (tid % 4) + 4 t, for all R rows;
+  // the next K tile's copies are in flight while the current one is used
   const int kl = tid >> 2, qp = tid & 3;
   float tmax[R];
 #pragma unroll
   for (int r = 0; r < R; ++r) tmax[r] = -INFINITY;
-  for (int k0 = 0; k0 <= last_block; k0 += kFusedKeys) {
-    __syncthreads();  // the previous tile is no longer read (and qs is written)
-    for (int f = tid; f < kFusedKeys * (D / 4); f += kFusedThreads) {
-      const int r = f / (D / 4), c4 = f % (D / 4);
-      float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (k0 + r <= last_block) x = ld4(Kh + (int64_t)(k0 + r) * D + 4 * c4);
-      *reinterpret_cast<float4*>(Ks + r * LDK + 4 * c4) = x;
-    }
-    __syncthreads();
+  for (int t = 0; t < nt; ++t) {
+    cp_async_wait<0>();  // this thread's copies of tile t have landed
+    __syncthreads();     // everyone's have (and qs is written); tile t - 1 is no longer read
+    if (t + 1 < nt) issue(Kh, LDK, t + 1, tile_buf(t + 1));
+    const float* Ks = tile_buf(t);
     float dot[R];
 #pragma unroll
     for (int r = 0; r < R; ++r) dot[r] = 0.f;
@@ -993,7 +1011,7 @@ __global__ void __launch_bounds__(kFusedThreads) fused_row_f32_kernel(const floa
         dot[r] = fmaf(qv.w, kv.w, dot[r]);
       }
     }
-    const int key = k0 + kl;
+    const int key = t * kFusedKeys + kl;
 #pragma unroll
     for (int r = 0; r < R; ++r) {
       float x = dot[r];
@@ -1002,32 +1020,58 @@ __global__ void __launch_bounds__(kFusedThreads) fused_row_f32_kernel(const floa
       const int last_r = causal ? min(i0 + r, S - 1) : S - 1;
       if (qp == 0 && key <= last_block) {
         const float sv = key <= last_r ? x : -INFINITY;
-        sc[r * S + key] = sv;
+        sc[r * SP + key] = sv;
         tmax[r] = fmaxf(tmax[r], sv);
       }
     }
   }
+  // the first V tile into the buffer the last K tile does not occupy (every
+  // thread passed the barrier after its last read of that buffer)
+  issue(Vh, D, 0, tile_buf(nt));
   block_rows<R, true>(tmax, red);  // its barriers also publish sc[]
+  // weights; the up to three entries past last_block that its last key quad
+  // spans are set to 0 (never written above, and their V rows are zero-filled)
+  const int jend = (last_block + 4) & ~3;  // <= SP
   float tsum[R];
 #pragma unroll
   for (int r = 0; r < R; ++r) {
     tsum[r] = 0.f;
-    for (int j = tid; j <= last_block; j += kFusedThreads) {
-      const float p = exp2f(sc[r * S + j] - tmax[r]);
-      sc[r * S + j] = p;
+    for (int j = tid; j < jend; j += kFusedThreads) {
+      const float p = j <= last_block ? exp2f(sc[r * SP + j] - tmax[r]) : 0.f;
+      sc[r * SP + j] = p;
       tsum[r] += p;
     }
   }
   block_rows<R, false>(tsum, red);  // its barriers also publish the new sc[]
 
+  // O = P V: thread (c, g) takes column c and the key quads g, g + G, ... of every
+  // tile (a warp shares g, so its weight loads are broadcasts); V tiles are
+  // double-buffered like K
   const int c = tid % D, g = tid / D;
   float acc[R];
 #pragma unroll
   for (int r = 0; r < R; ++r) acc[r] = 0.f;
-  for (int j = g; j <= last_block; j += G) {
-    const float v = Vh[(int64_t)j * D + c];
+  for (int t = 0; t < nt; ++t) {
+    cp_async_wait<0>();
+    __syncthreads();
+    if (t + 1 < nt) issue(Vh, D, t + 1, tile_buf(nt + t + 1));
+    const float* Vs = tile_buf(nt + t);
+    const int k0 = t * kFusedKeys;
 #pragma unroll
-    for (int r = 0; r < R; ++r) acc[r] = fmaf(sc[r * S + j], v, acc[r]);
+    for (int qd = g; qd < QUADS; qd += G) {
+      if (k0 + 4 * qd > last_block) break;
+      float v[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) v[i] = Vs[(4 * qd + i) * D + c];
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const float4 p = ld4(sc + r * SP + k0 + 4 * qd);
+        acc[r] = fmaf(p.x, v[0], acc[r]);
+        acc[r] = fmaf(p.y, v[1], acc[r]);
+        acc[r] = fmaf(p.z, v[2], acc[r]);
+        acc[r] = fmaf(p.w, v[3], acc[r]);
+      }
+    }
   }
 #pragma unroll
   for (int r = 0; r < R; ++r) part[r * kFusedThreads + tid] = acc[r];
@@ -1054,8 +1098,8 @@ size_t flash_smem(int d) {
 size_t naive_scores_smem(int d) { return sizeof(float) * (size_t)(d * kLD + kBC * (d + 4)); }
 size_t naive_pv_smem(int d) { return sizeof(float) * (size_t)(2 * 2 * (kBR * kLDP + kBC * d)); }
 size_t fused_smem(int S, int d, int rows = 1) {
-  return sizeof(float) * (size_t)(kFusedKeys * (d + 16) + rows * d + kFusedWarps * rows + rows * kFusedThreads +
-                                  (size_t)rows * S);
+  return sizeof(float) * (size_t)(2 * kFusedKeys * (d + 16) + rows * d + kFusedWarps * rows + rows * kFusedThreads +
+                                  (size_t)rows * (size_t)((S + 3) & ~3));
 }
 
 template <typename F>
