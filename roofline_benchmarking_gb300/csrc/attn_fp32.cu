@@ -102,12 +102,14 @@ __device__ __forceinline__ void pv_accumulate(float (&acc)[4][D / 16], const flo
 }
 
 // ---------------------------------------------------------------------------
-// flash: one block per (head, 64-row query tile); grid.x = tiles * N with the
-// heaviest causal tiles scheduled first. The block's 512 threads form two
-// groups of 256 (each synchronised by its own named barrier) that take the
-// even and the odd key tiles with their own K/V/P buffers and their own
-// running max, sum and O, and are merged at the end -- twice the warps per
-// query tile, so that small grids still hide the latency of shared memory.
+// flash at d = 128 (d <= 64 runs flash_f32x2_kernel below): one block per
+// (head, 64-row query tile); grid.x = tiles * N with the heaviest causal tiles
+// scheduled first. The block's 512 threads form two groups of 256 (each
+// synchronised by its own named barrier) that take the even and the odd key
+// tiles with their own K/V/P buffers and their own running max, sum and O, and
+// are merged at the end -- twice the warps per query tile, so that small grids
+// still hide the latency of shared memory. Two K/V buffers per group do not fit
+// in shared memory at d = 128, so each group loads its tile, then computes.
 // ---------------------------------------------------------------------------
 constexpr int kFlashThreads = 2 * kThreads;
 
@@ -156,14 +158,10 @@ __device__ __forceinline__ void flash_issue_kv(float* Kr, float* Vr, const float
   }
 }
 
-// At d <= 64 each group double-buffers its K and V tiles: the copies of its next
-// tile (cp.async) are in flight while it computes the current one. At d = 128
-// two buffers per group do not fit in shared memory; the loads stay synchronous.
-template <int D>
-constexpr bool flash_double_buffer() { return D <= 64; }
+// Floats of one group's K, V and P buffers in flash_f32_kernel.
 template <int D>
 constexpr int flash_group_floats() {
-  return (flash_double_buffer<D>() ? 2 : 1) * (kBC * flash_ldk<D>() + kBC * D) + kBC * kLD;
+  return kBC * flash_ldk<D>() + kBC * D + kBC * kLD;
 }
 
 // s[a][b] = sum_k Qs[k][ty*4+a] * K[tx+16b][k]: Q transposed (Qs[k * kLD + r]), K
@@ -215,15 +213,16 @@ __global__ void __launch_bounds__(kFlashThreads, 1) flash_f32_kernel(const float
   // blocks, over key tiles [0, h) and [h, qt] with h = ceil((qt + 1) / 2); each
   // writes its merged online-softmax state (m, l and the unnormalised O rows) to
   // `part` and flash_merge_kernel combines the two. split_from = tiles: no split.
+  static_assert(D == 128, "d <= 64 runs flash_f32x2_kernel");
   using C = Cols<D>;
-  constexpr bool DB = flash_double_buffer<D>();
-  constexpr int GROUP = flash_group_floats<D>();  // floats of one group's K, V and P buffers
-  constexpr int KV = kBC * flash_ldk<D>() + kBC * D;  // one K + V buffer pair
+  constexpr int GROUP = flash_group_floats<D>();      // floats of one group's K, V and P buffers
+  constexpr int KV = kBC * flash_ldk<D>() + kBC * D;  // the K + V buffer pair
   extern __shared__ float4 smem4[];
   float* Qs = reinterpret_cast<float*>(smem4);  // [D][kLD], both groups
   const int grp = threadIdx.x / kThreads, ltid = threadIdx.x % kThreads;
-  float* KV0 = Qs + D * kLD + grp * GROUP;       // buffer b: K [kBC][D + 4] at KV0 + b KV, V [kBC][D] after it
-  float* Ps = KV0 + (DB ? 2 : 1) * KV;           // [kBC][kLD]
+  float* Ks = Qs + D * kLD + grp * GROUP;       // [kBC][D + 4]
+  float* Vs = Ks + kBC * flash_ldk<D>();        // [kBC][D]
+  float* Ps = Ks + KV;                          // [kBC][kLD]
 
   const int ntiles = (S + kBR - 1) / kBR;
   const int nsplit = ntiles - split_from;  // split query tiles per head
@@ -259,28 +258,12 @@ __global__ void __launch_bounds__(kFlashThreads, 1) flash_f32_kernel(const float
     for (int c = 0; c < D / 16; ++c) acc[a][c] = 0.f;
   }
 
-  const int kt_last = ke;
-  if constexpr (DB) {
-    if (kb + grp <= kt_last) flash_issue_kv<D>(KV0, KV0 + kBC * flash_ldk<D>(), Kh, Vh, (kb + grp) * kBC, S, ltid);
-    cp_async_commit();
-  }
-  for (int kt = kb + grp, it = 0; kt <= kt_last; kt += 2, ++it) {
+  for (int kt = kb + grp; kt <= ke; kt += 2) {
     const int k0 = kt * kBC;
-    float* Ks = KV0 + (DB ? (it & 1) * KV : 0);  // [kBC][D + 4]
-    float* Vs = Ks + kBC * flash_ldk<D>();        // [kBC][D]
-    group_bar(grp);  // the group's previous K, V (other buffer) and P are no longer read
-    if constexpr (DB) {
-      if (kt + 2 <= kt_last) {
-        float* Kn = KV0 + ((it + 1) & 1) * KV;
-        flash_issue_kv<D>(Kn, Kn + kBC * flash_ldk<D>(), Kh, Vh, k0 + 2 * kBC, S, ltid);
-      }
-      cp_async_commit();
-      cp_async_wait<1>();  // this thread's copies of tile kt have landed
-    } else {
-      flash_issue_kv<D>(Ks, Vs, Kh, Vh, k0, S, ltid);
-      cp_async_commit();
-      cp_async_wait<0>();
-    }
+    group_bar(grp);  // the group's previous K, V and P are no longer read
+    flash_issue_kv<D>(Ks, Vs, Kh, Vh, k0, S, ltid);
+    cp_async_commit();
+    cp_async_wait<0>();
     group_bar(grp);
 
     float s[4][4];

@@ -132,12 +132,17 @@ def test_graph_replay_matches_oracle(oracle, variant):
 
 
 @pytest.mark.parametrize("shape", [(1, 8, 1023, 64, False), (1, 8, 1021, 64, True), (2, 4, 777, 32, True),
-                                   (1, 4, 513, 128, False), (1, 3, 1030, 128, True)],
+                                   (1, 4, 513, 128, False), (1, 3, 1030, 128, True), (1, 4, 2047, 64, True),
+                                   (1, 2, 2046, 32, False)],
                          ids=lambda s: "b{}h{}s{}d{}{}".format(*s[:4], "c" if s[4] else ""))
-def test_fused_four_rows_per_block_with_ragged_tails(oracle, shape):
-    """Grids large enough that the fused-row kernel takes four query rows per
-    block, with S not a multiple of four (the last block of each head is
-    partial) and causal rows whose key ranges differ within a block."""
+def test_fused_multi_row_blocks_with_ragged_tails(oracle, shape):
+    """Grids large enough that the fused-row kernel takes several query rows
+    per block: eight where two such blocks fit in one SM's shared memory (the
+    S ~ 1000 shapes at d <= 64 and S = 2046 at d = 32), else four (S = 2047 at
+    d = 64, and d = 128). S is not a
+    multiple of the rows per block (the last block of each head is partial) nor
+    of the 64-key tile or the 4-key quad, and causal rows' key ranges differ
+    within a block."""
     B, H, S, d, causal = shape
     w = inputs.Workload("t", B, H, S, d, causal, "f32", 500 + S, "uniform")
     got = run(w, Variant.FUSED)
