@@ -6,9 +6,11 @@ written as CSV, Markdown and JSON lines.
   python -m roofline_benchmarking_gb300.harness [--only SUBSTR] [--out DIR]
                                                 [--seconds S] [--quick] [--sweep]
 
-``--sweep`` runs only the kbench page's sequence sweep (section "Running") and
-writes its table (speed-up of each variant over the naive one per S) to
-``sweep.md`` beside the other outputs.
+``--sweep`` runs only the kbench page's sequence sweep (section "Running") with
+the three fp32 variants, and the same sweep widened to S = 16384 on the
+tensor-core path (bf16, d = 64 and 128), and writes their tables (the fp32
+variants' speed-up over the naive one per S; the tensor-core kernels' fraction
+of the measured bf16 peak per S) to ``sweep.md`` beside the other outputs.
 
 Sources (web pages): the kbench page, "Implementation details" (events around
 the kernel only, configurable warm-up, mean / p50 / p99 / min, achieved GFLOP/s
@@ -190,6 +192,23 @@ def write_outputs(rows, out_dir, meta):
     return "\n".join(md)
 
 
+def tc_sweep_table(rows) -> str | None:
+    """The tensor-core sweep (16 heads, bf16, d = 64 and 128, S = 128 ... 16384):
+    per d and S the median time, TFLOP/s, the fraction of the measured bf16
+    peak and the algorithmic GB/s (Q, K, V and O once)."""
+    names = {w.name: w for w in inputs.TC_SWEEP}
+    by = {r["workload"]: r for r in rows if r["workload"] in names and r["kernel"] == "attention"}
+    if not by:
+        return None
+    md = ["| d | S | p50 ms | TFLOP/s | frac of measured bf16 peak | GB/s | SM MHz |", "|---|---|---|---|---|---|---|"]
+    for w in inputs.TC_SWEEP:
+        r = by.get(w.name)
+        if r is not None:
+            md.append(f"| {w.d} | {w.S} | {r['p50_ms']:.4f} | {r['tflops']:.1f} | {r['roofline_frac']:.3f} | "
+                      f"{r['gbs']:.0f} | {r['sm_mhz']} |")
+    return "\n".join(md)
+
+
 def sweep_table(rows) -> str | None:
     """The kbench page's sequence sweep (16 heads, d = 64, fp32) as the page
     reports it: per S and variant the median time, GFLOP/s, effective GB/s
@@ -223,8 +242,9 @@ def main(argv=None) -> int:
     p.add_argument("--no-hbm", action="store_true")
     p.add_argument("--no-attention", action="store_true")
     p.add_argument("--sweep", action="store_true",
-                   help="only the kbench page's sequence sweep (fp32, 16 heads, d = 64, S = 128 ... 2048; "
-                        "no HBM rows unless --with-hbm)")
+                   help="only the kbench page's sequence sweep (fp32, 16 heads, d = 64, S = 128 ... 2048) and its "
+                        "tensor-core widening (bf16, d = 64 and 128, S = 128 ... 16384); no HBM rows unless "
+                        "--with-hbm")
     p.add_argument("--with-hbm", action="store_true", help="with --sweep: run the HBM kernels too")
     args = p.parse_args(argv)
     if args.sweep and not args.with_hbm:
@@ -253,7 +273,7 @@ def main(argv=None) -> int:
         triad = [r["gbs"] for r in hbm if r["kernel"] == "triad"]
         bandwidth = max(triad) if triad else peaks["hbm_gbs"]
         bw_source = "best STREAM Triad of this run" if triad else "measured copy bandwidth (no Triad run)"
-        todo = inputs.KBENCH_SWEEP if args.sweep else inputs.WORKLOADS.values()
+        todo = inputs.KBENCH_SWEEP + inputs.TC_SWEEP if args.sweep else inputs.WORKLOADS.values()
         for w in ([] if args.no_attention else todo):
             for variant in ATTN_VARIANTS[w.dtype]:
                 if only and only not in w.name.lower() and only not in variant.name.lower():
@@ -271,7 +291,7 @@ def main(argv=None) -> int:
             "theoretical_hbm_gbs": rf.theoretical_dram_gbs(info["mem_clock_khz"] / 1e3, info["mem_bus_width_bits"]),
             "fp32_peak_tflops": rf.fp32_peak_gflops(info["sm_count"], info["sm_clock_khz"] / 1e3) / 1e3}
     print(write_outputs(rows, args.out, meta))
-    sweep = sweep_table(rows)
+    sweep = "\n\n".join(s for s in (sweep_table(rows), tc_sweep_table(rows)) if s)
     if sweep:
         with open(os.path.join(args.out, "sweep.md"), "w") as f:
             f.write(sweep + "\n")

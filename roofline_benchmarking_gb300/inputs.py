@@ -92,10 +92,17 @@ KBENCH_SWEEP_S = (128, 256, 512, 1024, 2048)
 KBENCH_SWEEP = tuple(Workload(f"f32_b1h16s{S}d64", 1, 16, S, 64, False, "f32", 5, "uniform")
                      for S in KBENCH_SWEEP_S)
 
+# The same sweep on the tensor-core path: 16 heads, bf16 with fp32 accumulation,
+# d = 64 and 128, non-causal, S from 128 to 16384 (from a handful of CTAs to a
+# full persistent grid), N(0, 1) draws rounded to bf16, seed 5.
+TC_SWEEP_S = (128, 256, 512, 1024, 2048, 4096, 8192, 16384)
+TC_SWEEP = tuple(Workload(f"bf16_b1h16s{S}d{d}", 1, 16, S, d, False, "bf16", 5, "normal")
+                 for d in (64, 128) for S in TC_SWEEP_S)
+
 WORKLOADS = {w.name: w for w in (SINGLE_HEAD_F32, F32_S1024, F32_S1024_CAUSAL,
                                  BF16_CAUSAL_S4096, BF16_S2048_D64, BF16_CAUSAL_S16384, BF16_CAUSAL_D256,
                                  F16_CAUSAL_S4096, F16_S2048_D64,
-                                 Q15_SINGLE_HEAD, Q15_S1024, Q15_S1024_CAUSAL, *KBENCH_SWEEP)}
+                                 Q15_SINGLE_HEAD, Q15_S1024, Q15_S1024_CAUSAL, *KBENCH_SWEEP, *TC_SWEEP)}
 
 # STREAM Triad working set: three fp32 arrays of 2 GiB each.
 TRIAD_ARRAY_BYTES = 2 << 30

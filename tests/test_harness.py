@@ -48,6 +48,19 @@ def test_kbench_sequence_sweep_table():
     assert harness.sweep_table([rows[-1]]) is None
 
 
+def test_tensor_core_sweep_table():
+    assert [w.S for w in inputs.TC_SWEEP] == [128, 256, 512, 1024, 2048, 4096, 8192, 16384] * 2
+    assert [w.d for w in inputs.TC_SWEEP] == [64] * 8 + [128] * 8
+    assert all((w.B, w.H, w.dtype, w.causal) == (1, 16, "bf16", False) for w in inputs.TC_SWEEP)
+    assert all(inputs.WORKLOADS[w.name] is w for w in inputs.TC_SWEEP)
+    w = inputs.TC_SWEEP[-1]
+    row = {"kernel": "attention", "workload": w.name, "variant": "TC", "p50_ms": 1.5, "tflops": 1466.0,
+           "gbs": 179.0, "roofline_frac": 0.747, "sm_mhz": 1950.0}
+    lines = harness.tc_sweep_table([row, dict(row, workload=inputs.F32_S1024.name)]).splitlines()
+    assert len(lines) == 3 and lines[2] == "| 128 | 16384 | 1.5000 | 1466.0 | 0.747 | 179 | 1950.0 |"
+    assert harness.tc_sweep_table([dict(row, workload="other")]) is None
+
+
 @pytest.mark.gpu
 def test_harness_runs_a_quick_sweep(tmp_path):
     assert harness.main(["--only", "f32_b1h1s64d32", "--no-hbm", "--seconds", "0.02",
