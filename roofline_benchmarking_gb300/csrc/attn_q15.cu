@@ -19,15 +19,16 @@
 //   output  acc_c / l rounded to nearest, halves away from zero, saturated.
 // Every step is integer arithmetic, so the result is defined bit for bit.
 //
-// GPU layout: one block per ROWS query rows of one head (32 rows; 16 under
-// the causal mask, where short blocks balance the triangle), 8 threads per
-// row. Per 32-key tile the block stages K (split into low and high bytes) and
-// V (split and transposed to channel-major) in shared memory; thread g of a
-// row computes the scores of keys g, g+8, g+16, g+24 with dp2a, the row's 8
-// threads combine the tile maximum and the weight sum with shuffles, and each
-// thread accumulates channels g, g+8, ... in 64-bit registers. The tiles
-// are the model's tiles, and the block's rows all use the same tile bounds, so
-// the sequence of rescales is exactly the model's.
+// GPU layout: one block per ROWS = 16 query rows of one head (short blocks
+// balance the causal triangle; 32-row blocks measured no faster without the
+// mask), 8 threads per row. Per 32-key tile the block stages K (split into low and high bytes) and
+// V (split and transposed to channel-major) in shared memory, one tile ahead in
+// three rotating buffers, with one barrier per tile; thread g of a row keeps
+// the row's query in registers, computes the scores of keys g, g+8, g+16, g+24
+// with dp2a, the row's 8 threads combine the tile maximum and the weight sum
+// with shuffles, and each thread accumulates channels g, g+8, ... in 64-bit
+// registers. The tiles are the model's tiles, and the block's rows all use the
+// same tile bounds, so the sequence of rescales is exactly the model's.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -113,24 +114,48 @@ __device__ __forceinline__ void split4(int2 x, unsigned& lo, unsigned& hi) {
 // a signed high byte and an unsigned low byte, so q . k = 256 (q . kh) + q . kl
 // with both partial sums exact in 32 bits (|q kh| <= 2^22, 0 <= ... q kl < 2^23,
 // at most 128 terms); likewise each tile's sum over 32 keys of p v (p <= 2^15).
+//
+// Per block: three staging buffers for the model's 32-key tiles (K split into
+// low and high bytes, key-major; V split and channel-major, read straight from
+// global memory in that order), two buffers of packed weights, one barrier per
+// tile. Iteration t issues the global loads of tile t + 1 into registers, scores
+// tile t, then stores tile t + 1 into buffer (t + 1) % 3; the barrier publishes
+// tile t's weights and tile t + 1's staging; P V of tile t follows. A buffer is
+// restaged only after the barrier that follows its last use two iterations
+// earlier. Each thread keeps its row's query words in registers.
+template <int D, int ROWS>
+struct Q15Smem {
+  static constexpr int KW = D / 4;            // words (byte quads) of a split key row
+  static constexpr int KLD = KW + 4;          // padded: the 8 rows read by one load phase fall in distinct banks
+  static constexpr int VLD = kTile / 4 + 4;   // words of a split value column (32 keys), padded likewise
+  static constexpr int KBUF = kTile * KLD;    // one K half (low or high bytes) of a buffer
+  static constexpr int VBUF = D * VLD;        // one V half of a buffer
+  static constexpr int PBUF = ROWS * (kTile / 2);
+  static constexpr int WORDS = 3 * (2 * KBUF + 2 * VBUF) + 2 * PBUF + 32;  // + the exp table (64 x 16 bits)
+  static constexpr size_t BYTES = sizeof(unsigned) * (size_t)WORDS;
+};
+
 template <int D, int ROWS>
 __global__ void __launch_bounds__(8 * ROWS) q15_attn_kernel(const short* __restrict__ Q,
                                                            const short* __restrict__ K,
                                                            const short* __restrict__ V, short* __restrict__ O,
                                                            int S, int tiles_per_head, int causal,
                                                            const Q15Params prm) {
+  using L = Q15Smem<D, ROWS>;
   constexpr int QW = D / 2;       // words (int16 pairs) of a query row
-  constexpr int KW = D / 4;       // words (byte quads) of a split key row
-  constexpr int KLD = KW + 4;     // padded: the 8 rows read by one load phase fall in distinct banks
-  constexpr int VLD = kTile / 4 + 4;  // words of a split value column (32 keys), padded likewise
+  constexpr int KW = L::KW;
+  constexpr int KLD = L::KLD;
+  constexpr int VLD = L::VLD;
   constexpr int CH = D / 8;       // output channels per thread: g, g + 8, ...
   constexpr int kThreads = 8 * ROWS;
-  __shared__ __align__(16) int Qw[ROWS][QW];
-  __shared__ __align__(16) unsigned Kl[kTile][KLD], Kh[kTile][KLD];
-  __shared__ __align__(16) short Vs[kTile][D];
-  __shared__ __align__(16) unsigned Vl[D][VLD], Vh[D][VLD];
-  __shared__ __align__(16) unsigned Pw[ROWS][kTile / 2];
-  __shared__ unsigned short tab[64];
+  extern __shared__ uint4 q15_smem[];
+  unsigned* sm = reinterpret_cast<unsigned*>(q15_smem);
+  unsigned* Kl = sm;                          // [3][kTile][KLD]
+  unsigned* Kh = Kl + 3 * L::KBUF;            // [3][kTile][KLD]
+  unsigned* Vl = Kh + 3 * L::KBUF;            // [3][D][VLD]
+  unsigned* Vh = Vl + 3 * L::VBUF;            // [3][D][VLD]
+  unsigned* Pw = Vh + 3 * L::VBUF;            // [2][ROWS][kTile / 2]
+  unsigned short* tab = reinterpret_cast<unsigned short*>(Pw + 2 * L::PBUF);
 
   const int tid = threadIdx.x;
   const int r = tid >> 3, g = tid & 7;
@@ -140,58 +165,97 @@ __global__ void __launch_bounds__(8 * ROWS) q15_attn_kernel(const short* __restr
   const long long n = blockIdx.x % nheads;
   const int i0 = (tiles_per_head - 1 - (int)(blockIdx.x / nheads)) * ROWS;
   const int i = i0 + r;
-  const short* Qh = Q + n * S * D;
   const short* Kg = K + n * S * D;
   const short* Vg = V + n * S * D;
 
   if (tid < 64) tab[tid] = prm.t[tid];
-  for (int f = tid; f < ROWS * (D / 8); f += kThreads) {
-    const int rr = f / (D / 8), c8 = f % (D / 8);
-    int4 x = make_int4(0, 0, 0, 0);
-    if (i0 + rr < S) x = *reinterpret_cast<const int4*>(Qh + (long long)(i0 + rr) * D + 8 * c8);
-    *reinterpret_cast<int4*>(&Qw[rr][4 * c8]) = x;
+  int qreg[QW];  // the row's query values as int16 pairs
+  {
+    const int* qrow = reinterpret_cast<const int*>(Q + (n * S + (i < S ? i : 0)) * D);
+#pragma unroll
+    for (int w = 0; w < QW; w += 4) {
+      int4 x = make_int4(0, 0, 0, 0);
+      if (i < S) x = *reinterpret_cast<const int4*>(qrow + w);
+      qreg[w] = x.x; qreg[w + 1] = x.y; qreg[w + 2] = x.z; qreg[w + 3] = x.w;
+    }
   }
+
+  // Staging of a tile in two halves, so that the global loads of tile t + 1
+  // are in flight while tile t is scored: stage_load reads this thread's
+  // share into registers (K as int16 quads, V as four keys of one channel),
+  // stage_store splits it into low and high byte quads (V transposed to
+  // channel-major) in buffer b. Keys >= S read as 0.
+  constexpr int KT = (kTile * KW + kThreads - 1) / kThreads;        // K quads per thread
+  constexpr int VT = (D * (kTile / 4) + kThreads - 1) / kThreads;  // V quads per thread
+  int2 kreg[KT], vreg[VT];
+  auto stage_load = [&](int tt) {
+    const int t0 = tt * kTile;
+#pragma unroll
+    for (int x = 0; x < KT; ++x) {
+      const int f = tid + x * kThreads;
+      const int j = f / KW, w = f % KW;
+      kreg[x] = make_int2(0, 0);
+      if (f < kTile * KW && t0 + j < S) kreg[x] = *reinterpret_cast<const int2*>(Kg + (long long)(t0 + j) * D + 4 * w);
+    }
+#pragma unroll
+    for (int x = 0; x < VT; ++x) {
+      const int f = tid + x * kThreads;
+      const int c = f / (kTile / 4), kq = f % (kTile / 4);
+      unsigned e[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int key = t0 + 4 * kq + u;
+        e[u] = (f < D * (kTile / 4) && key < S) ? (unsigned)(unsigned short)Vg[(long long)key * D + c] : 0u;
+      }
+      vreg[x] = make_int2((int)(e[0] | (e[1] << 16)), (int)(e[2] | (e[3] << 16)));
+    }
+  };
+  auto stage_store = [&](int b) {
+    unsigned* kl = Kl + b * L::KBUF;
+    unsigned* kh = Kh + b * L::KBUF;
+#pragma unroll
+    for (int x = 0; x < KT; ++x) {
+      const int f = tid + x * kThreads;
+      if (f >= kTile * KW) continue;
+      const int j = f / KW, w = f % KW;
+      unsigned lo, hi;
+      split4(kreg[x], lo, hi);
+      kl[j * KLD + w] = lo;
+      kh[j * KLD + w] = hi;
+    }
+    unsigned* vl = Vl + b * L::VBUF;
+    unsigned* vh = Vh + b * L::VBUF;
+#pragma unroll
+    for (int x = 0; x < VT; ++x) {
+      const int f = tid + x * kThreads;
+      if (f >= D * (kTile / 4)) continue;
+      const int c = f / (kTile / 4), kq = f % (kTile / 4);
+      unsigned lo, hi;
+      split4(vreg[x], lo, hi);
+      vl[c * VLD + kq] = lo;
+      vh[c * VLD + kq] = hi;
+    }
+  };
 
   const int my_last = causal ? min(i, S - 1) : S - 1;
   const int block_last = causal ? min(i0 + ROWS - 1, S - 1) : S - 1;
+  const int nt = block_last / kTile + 1;
   long long m = 0, l = 0, acc[CH];
   bool have_m = false;
 #pragma unroll
   for (int c = 0; c < CH; ++c) acc[c] = 0;
 
-  for (int t0 = 0; t0 <= block_last; t0 += kTile) {
-    __syncthreads();  // the previous tile is no longer read (and Qw is written)
-    // K: split each quad of features into low and high bytes
-    for (int f = tid; f < kTile * KW; f += kThreads) {
-      const int j = f / KW, w = f % KW;
-      int2 x = make_int2(0, 0);
-      if (t0 + j < S) x = *reinterpret_cast<const int2*>(Kg + (long long)(t0 + j) * D + 4 * w);
-      unsigned lo, hi;
-      split4(x, lo, hi);
-      Kl[j][w] = lo;
-      Kh[j][w] = hi;
-    }
-    // V: staged as is (coalesced), then split and transposed below
-    for (int f = tid; f < kTile * (D / 8); f += kThreads) {
-      const int j = f / (D / 8), c8 = f % (D / 8);
-      int4 x = make_int4(0, 0, 0, 0);
-      if (t0 + j < S) x = *reinterpret_cast<const int4*>(Vg + (long long)(t0 + j) * D + 8 * c8);
-      *reinterpret_cast<int4*>(&Vs[j][8 * c8]) = x;
-    }
-    __syncthreads();
-    for (int f = tid; f < D * (kTile / 4); f += kThreads) {
-      const int c = f / (kTile / 4), kq = f % (kTile / 4);
-      const int2 x = make_int2((int)((unsigned)(unsigned short)Vs[4 * kq][c] |
-                                     ((unsigned)(unsigned short)Vs[4 * kq + 1][c] << 16)),
-                               (int)((unsigned)(unsigned short)Vs[4 * kq + 2][c] |
-                                     ((unsigned)(unsigned short)Vs[4 * kq + 3][c] << 16)));
-      unsigned lo, hi;
-      split4(x, lo, hi);
-      Vl[c][kq] = lo;
-      Vh[c][kq] = hi;
-    }
+  stage_load(0);
+  stage_store(0);
+  __syncthreads();
+  for (int tt = 0; tt < nt; ++tt) {
+    const int t0 = tt * kTile;
+    const int b = tt % 3;
+    if (tt + 1 < nt) stage_load(tt + 1);  // consumed by stage_store after the scores
 
     // scores of keys g, g+8, g+16, g+24 of the tile
+    const unsigned* kl = Kl + b * L::KBUF;
+    const unsigned* kh = Kh + b * L::KBUF;
     long long z[4];
     bool ok[4];
     long long mt = 0;
@@ -202,18 +266,18 @@ __global__ void __launch_bounds__(8 * ROWS) q15_attn_kernel(const short* __restr
       int accl = 0, acch = 0;
 #pragma unroll
       for (int w = 0; w < KW; w += 4) {
-        const uint4 kl = *reinterpret_cast<const uint4*>(&Kl[kk][w]);
-        const uint4 kh = *reinterpret_cast<const uint4*>(&Kh[kk][w]);
-        const int4 qa = *reinterpret_cast<const int4*>(&Qw[r][2 * w]);
-        const int4 qb = *reinterpret_cast<const int4*>(&Qw[r][2 * w + 4]);
-        accl = dp2a_lo_su(qa.x, kl.x, accl); accl = dp2a_hi_su(qa.y, kl.x, accl);
-        acch = dp2a_lo_ss(qa.x, kh.x, acch); acch = dp2a_hi_ss(qa.y, kh.x, acch);
-        accl = dp2a_lo_su(qa.z, kl.y, accl); accl = dp2a_hi_su(qa.w, kl.y, accl);
-        acch = dp2a_lo_ss(qa.z, kh.y, acch); acch = dp2a_hi_ss(qa.w, kh.y, acch);
-        accl = dp2a_lo_su(qb.x, kl.z, accl); accl = dp2a_hi_su(qb.y, kl.z, accl);
-        acch = dp2a_lo_ss(qb.x, kh.z, acch); acch = dp2a_hi_ss(qb.y, kh.z, acch);
-        accl = dp2a_lo_su(qb.z, kl.w, accl); accl = dp2a_hi_su(qb.w, kl.w, accl);
-        acch = dp2a_lo_ss(qb.z, kh.w, acch); acch = dp2a_hi_ss(qb.w, kh.w, acch);
+        const uint4 l4 = *reinterpret_cast<const uint4*>(&kl[kk * KLD + w]);
+        const uint4 h4 = *reinterpret_cast<const uint4*>(&kh[kk * KLD + w]);
+        const int qa0 = qreg[2 * w], qa1 = qreg[2 * w + 1], qa2 = qreg[2 * w + 2], qa3 = qreg[2 * w + 3];
+        const int qb0 = qreg[2 * w + 4], qb1 = qreg[2 * w + 5], qb2 = qreg[2 * w + 6], qb3 = qreg[2 * w + 7];
+        accl = dp2a_lo_su(qa0, l4.x, accl); accl = dp2a_hi_su(qa1, l4.x, accl);
+        acch = dp2a_lo_ss(qa0, h4.x, acch); acch = dp2a_hi_ss(qa1, h4.x, acch);
+        accl = dp2a_lo_su(qa2, l4.y, accl); accl = dp2a_hi_su(qa3, l4.y, accl);
+        acch = dp2a_lo_ss(qa2, h4.y, acch); acch = dp2a_hi_ss(qa3, h4.y, acch);
+        accl = dp2a_lo_su(qb0, l4.z, accl); accl = dp2a_hi_su(qb1, l4.z, accl);
+        acch = dp2a_lo_ss(qb0, h4.z, acch); acch = dp2a_hi_ss(qb1, h4.z, acch);
+        accl = dp2a_lo_su(qb2, l4.w, accl); accl = dp2a_hi_su(qb3, l4.w, accl);
+        acch = dp2a_lo_ss(qb2, h4.w, acch); acch = dp2a_hi_ss(qb3, h4.w, acch);
       }
       const long long dot = (long long)acch * 256 + accl;  // the exact sum of the d products
       z[u] = ((dot >> 14) * prm.C) >> 16;                   // arithmetic shifts: floor
@@ -241,6 +305,7 @@ __global__ void __launch_bounds__(8 * ROWS) q15_attn_kernel(const short* __restr
         m = mt;
       }
     }
+    unsigned* pw_tile = Pw + (tt & 1) * L::PBUF;
     long long psum = 0;
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
@@ -248,17 +313,20 @@ __global__ void __launch_bounds__(8 * ROWS) q15_attn_kernel(const short* __restr
       psum += p;
       // weights of keys 2m and 2m+1 share a word: even threads take their odd neighbour's
       const unsigned pn = __shfl_down_sync(0xffffffffu, p, 1);
-      if ((g & 1) == 0) Pw[r][(g + 8 * u) >> 1] = p | (pn << 16);
+      if ((g & 1) == 0) pw_tile[r * (kTile / 2) + ((g + 8 * u) >> 1)] = p | (pn << 16);
     }
 #pragma unroll
     for (int s = 1; s < 8; s <<= 1) psum += __shfl_xor_sync(0xffffffffu, psum, s);
     l += psum;
-    __syncthreads();  // Vl / Vh complete; the row's weights written
+    if (tt + 1 < nt) stage_store((tt + 1) % 3);
+    __syncthreads();  // the tile's weights written; tile tt + 1 staged
 
     // acc_c += sum_j p_j v_jc over the tile for channels c = g + 8 i
+    const unsigned* vl = Vl + b * L::VBUF;
+    const unsigned* vh = Vh + b * L::VBUF;
     uint4 pw[kTile / 8];
 #pragma unroll
-    for (int q4 = 0; q4 < kTile / 8; ++q4) pw[q4] = *reinterpret_cast<const uint4*>(&Pw[r][4 * q4]);
+    for (int q4 = 0; q4 < kTile / 8; ++q4) pw[q4] = *reinterpret_cast<const uint4*>(&pw_tile[r * (kTile / 2) + 4 * q4]);
 #pragma unroll
     for (int ci = 0; ci < CH; ++ci) {
       const int c = g + 8 * ci;
@@ -266,17 +334,17 @@ __global__ void __launch_bounds__(8 * ROWS) q15_attn_kernel(const short* __restr
       int ah = 0;
 #pragma unroll
       for (int q4 = 0; q4 < kTile / 16; ++q4) {
-        const uint4 vl = *reinterpret_cast<const uint4*>(&Vl[c][4 * q4]);
-        const uint4 vh = *reinterpret_cast<const uint4*>(&Vh[c][4 * q4]);
+        const uint4 l4 = *reinterpret_cast<const uint4*>(&vl[c * VLD + 4 * q4]);
+        const uint4 h4 = *reinterpret_cast<const uint4*>(&vh[c * VLD + 4 * q4]);
         const uint4 pa = pw[2 * q4], pb = pw[2 * q4 + 1];  // keys 16 q4 .. 16 q4 + 15 as 8 pairs
-        al = dp2a_lo_uu(pa.x, vl.x, al); al = dp2a_hi_uu(pa.y, vl.x, al);
-        ah = dp2a_lo_us(pa.x, vh.x, ah); ah = dp2a_hi_us(pa.y, vh.x, ah);
-        al = dp2a_lo_uu(pa.z, vl.y, al); al = dp2a_hi_uu(pa.w, vl.y, al);
-        ah = dp2a_lo_us(pa.z, vh.y, ah); ah = dp2a_hi_us(pa.w, vh.y, ah);
-        al = dp2a_lo_uu(pb.x, vl.z, al); al = dp2a_hi_uu(pb.y, vl.z, al);
-        ah = dp2a_lo_us(pb.x, vh.z, ah); ah = dp2a_hi_us(pb.y, vh.z, ah);
-        al = dp2a_lo_uu(pb.z, vl.w, al); al = dp2a_hi_uu(pb.w, vl.w, al);
-        ah = dp2a_lo_us(pb.z, vh.w, ah); ah = dp2a_hi_us(pb.w, vh.w, ah);
+        al = dp2a_lo_uu(pa.x, l4.x, al); al = dp2a_hi_uu(pa.y, l4.x, al);
+        ah = dp2a_lo_us(pa.x, h4.x, ah); ah = dp2a_hi_us(pa.y, h4.x, ah);
+        al = dp2a_lo_uu(pa.z, l4.y, al); al = dp2a_hi_uu(pa.w, l4.y, al);
+        ah = dp2a_lo_us(pa.z, h4.y, ah); ah = dp2a_hi_us(pa.w, h4.y, ah);
+        al = dp2a_lo_uu(pb.x, l4.z, al); al = dp2a_hi_uu(pb.y, l4.z, al);
+        ah = dp2a_lo_us(pb.x, h4.z, ah); ah = dp2a_hi_us(pb.y, h4.z, ah);
+        al = dp2a_lo_uu(pb.z, l4.w, al); al = dp2a_hi_uu(pb.w, l4.w, al);
+        ah = dp2a_lo_us(pb.z, h4.w, ah); ah = dp2a_hi_us(pb.w, h4.w, ah);
       }
       acc[ci] += (long long)ah * 256 + (long long)al;
     }
@@ -295,8 +363,11 @@ __global__ void __launch_bounds__(8 * ROWS) q15_attn_kernel(const short* __restr
 
 template <int D, int ROWS>
 cudaError_t q15_launch_rows(const AttnProblem& p, const Q15Params& prm, cudaStream_t st) {
+  constexpr size_t smem = Q15Smem<D, ROWS>::BYTES;
+  cudaError_t e = cudaFuncSetAttribute(q15_attn_kernel<D, ROWS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
   const int tiles = (p.S + ROWS - 1) / ROWS;
-  q15_attn_kernel<D, ROWS><<<(unsigned)(p.N * tiles), 8 * ROWS, 0, st>>>(
+  q15_attn_kernel<D, ROWS><<<(unsigned)(p.N * tiles), 8 * ROWS, smem, st>>>(
       static_cast<const short*>(p.q), static_cast<const short*>(p.k), static_cast<const short*>(p.v),
       static_cast<short*>(p.o), p.S, tiles, p.causal, prm);
   return cudaGetLastError();
@@ -304,7 +375,7 @@ cudaError_t q15_launch_rows(const AttnProblem& p, const Q15Params& prm, cudaStre
 
 template <int D>
 cudaError_t q15_launch(const AttnProblem& p, const Q15Params& prm, cudaStream_t st) {
-  return p.causal ? q15_launch_rows<D, 16>(p, prm, st) : q15_launch_rows<D, 32>(p, prm, st);
+  return q15_launch_rows<D, 16>(p, prm, st);
 }
 
 }  // namespace
