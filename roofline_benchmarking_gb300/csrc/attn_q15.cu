@@ -101,13 +101,13 @@ __device__ __forceinline__ int dp2a_hi_us(unsigned a, unsigned b, int c) {
   return d;
 }
 
-// Four int16 values (packed as two words) split into their low bytes
-// (unsigned, x & 255) and high bytes (signed, x >> 8): x = 256 * hi + lo.
+// Four int16 values (packed little-endian as two words) split into their low
+// bytes (unsigned, x & 255) and high bytes (signed, x >> 8): x = 256 * hi + lo.
+// Bytes 0, 2 of x.x and of x.y are the low bytes, 1, 3 the high ones: one byte
+// permute each.
 __device__ __forceinline__ void split4(int2 x, unsigned& lo, unsigned& hi) {
-  const int a = (int)(short)(x.x & 0xffff), b = x.x >> 16, c = (int)(short)(x.y & 0xffff), d = x.y >> 16;
-  lo = (unsigned)(a & 255) | ((unsigned)(b & 255) << 8) | ((unsigned)(c & 255) << 16) | ((unsigned)(d & 255) << 24);
-  hi = (unsigned)((a >> 8) & 255) | ((unsigned)((b >> 8) & 255) << 8) | ((unsigned)((c >> 8) & 255) << 16) |
-       ((unsigned)((d >> 8) & 255) << 24);
+  lo = __byte_perm((unsigned)x.x, (unsigned)x.y, 0x6420);
+  hi = __byte_perm((unsigned)x.x, (unsigned)x.y, 0x7531);
 }
 
 // The integer products are formed with dp2a: a key k = 256 kh + kl splits into
@@ -280,7 +280,9 @@ __global__ void __launch_bounds__(8 * ROWS) q15_attn_kernel(const short* __restr
         acch = dp2a_lo_ss(qb2, h4.w, acch); acch = dp2a_hi_ss(qb3, h4.w, acch);
       }
       const long long dot = (long long)acch * 256 + accl;  // the exact sum of the d products
-      z[u] = ((dot >> 14) * prm.C) >> 16;                   // arithmetic shifts: floor
+      // arithmetic shifts: floor; |dot| < 2^38, so dot >> 14 fits in 32 bits, as C does
+      // (scale checked on the host), and the product is one 32 x 32 -> 64-bit multiply
+      z[u] = ((long long)(int)(dot >> 14) * (long long)(int)prm.C) >> 16;
       ok[u] = t0 + kk <= my_last;
       if (ok[u] && (!any || z[u] > mt)) mt = z[u];
       any = any || ok[u];
