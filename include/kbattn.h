@@ -77,9 +77,12 @@ typedef enum { KB_F32 = 0, KB_BF16 = 1, KB_F16 = 2, KB_Q15 = 3 } kb_dtype;
  * this library's sm_103a kernel):
  *  KB_NAIVE : three passes, the N*S*S fp32 score matrix goes through global
  *             memory (score GEMM, row softmax in place, P*V GEMM). fp32 only.
- *  KB_FUSED : one block per query row, the S-length score row kept in shared
- *             memory. fp32 only; UNSUPPORTED when S*4 bytes exceed the shared
- *             memory a block may use.
+ *  KB_FUSED : a block per query row (or per 2, 4 or 8 consecutive rows where
+ *             they fit), the S-length score rows kept in shared memory beside
+ *             two 64-key staging buffers. fp32 only; UNSUPPORTED when one row's
+ *             S*4 bytes and the buffers exceed the shared memory a block may
+ *             use (on GB300: S up to about 39,000 at d = 128, 47,000 at d = 64,
+ *             51,000 at d = 32).
  *  KB_FLASH : tiled, online softmax (running max and denominator), the score
  *             matrix never materialised; CUDA cores. fp32 only.
  *  KB_TC    : tiled, online softmax on the 5th-generation tensor cores
