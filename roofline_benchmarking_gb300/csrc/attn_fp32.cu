@@ -876,6 +876,231 @@ __global__ void __launch_bounds__(kFlashThreads, 1) naive_pv_kernel(const float*
 }
 
 // ---------------------------------------------------------------------------
+// naive passes 1 and 3 at d <= 64 with paired FMAs and 8 x 4 register tiles,
+// the tile products of flash_f32x2_kernel (the softmax pass is shared):
+//  * scores: a block of 128 threads per 64 x 64 score tile, Q (scaled) and K
+//    row-major in shared memory, features paired; thread (tx, ty) owns rows
+//    ty + 8 a and keys tx + 16 b;
+//  * P V: per 64-row query tile two groups of 128 threads take the even and the
+//    odd key tiles; each double-buffers its P tile (row-major, as pass 2 left
+//    it) and V tile with cp.async (the next tile's copies issued once every
+//    thread of the group is past the tile that last read that buffer), re-lays
+//    V as key pairs and accumulates rows ty + 8 a, columns 32 g + 2 tx + e over
+//    key pairs; group 0 adds group 1's sums at the end.
+// ---------------------------------------------------------------------------
+constexpr int kNx2Threads = 128;
+
+template <int D>
+__global__ void __launch_bounds__(kNx2Threads) naive_scores_x2_kernel(const float* __restrict__ Q,
+                                                                       const float* __restrict__ K,
+                                                                       float* __restrict__ Sc, int64_t N, int S,
+                                                                       int causal, float scale) {
+  static_assert(D == 32 || D == 64, "paired-FMA naive score pass: d = 32 and 64");
+  constexpr int RT = 8;
+  constexpr int LDQ = D + 4;
+  extern __shared__ float4 smem4[];
+  float* Qs = reinterpret_cast<float*>(smem4);  // [kBR][LDQ], scaled
+  float* Ks = Qs + kBR * LDQ;                    // [kBC][LDQ]
+  const int kt = blockIdx.x, qt = blockIdx.y;
+  const int64_t n = blockIdx.z;
+  if (causal && kt > qt) return;
+  const int q0 = qt * kBR, k0 = kt * kBC;
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  const float* Qh = Q + n * S * D;
+  const float* Kh = K + n * S * D;
+  for (int f = tid; f < kBR * (D / 4); f += kNx2Threads) {  // coalesced 16-byte loads; rows >= S read as 0
+    const int r = f / (D / 4), c4 = f % (D / 4);
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f), y = x;
+    if (q0 + r < S) x = ld4(Qh + (int64_t)(q0 + r) * D + 4 * c4);
+    if (k0 + r < S) y = ld4(Kh + (int64_t)(k0 + r) * D + 4 * c4);
+    *reinterpret_cast<float4*>(Qs + r * LDQ + 4 * c4) = make_float4(x.x * scale, x.y * scale, x.z * scale, x.w * scale);
+    *reinterpret_cast<float4*>(Ks + r * LDQ + 4 * c4) = y;
+  }
+  __syncthreads();
+  float2 s2[RT][4];
+#pragma unroll
+  for (int a = 0; a < RT; ++a)
+#pragma unroll
+    for (int b = 0; b < 4; ++b) s2[a][b] = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int k = 0; k < D; k += 4) {
+    float4 kv[4], qv[RT];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) kv[b] = ld4(Ks + (tx + 16 * b) * LDQ + k);
+#pragma unroll
+    for (int a = 0; a < RT; ++a) qv[a] = ld4(Qs + (ty + 8 * a) * LDQ + k);
+#pragma unroll
+    for (int a = 0; a < RT; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b)
+        s2[a][b] = __ffma2_rn(make_float2(qv[a].x, qv[a].y), make_float2(kv[b].x, kv[b].y), s2[a][b]);
+#pragma unroll
+    for (int a = 0; a < RT; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b)
+        s2[a][b] = __ffma2_rn(make_float2(qv[a].z, qv[a].w), make_float2(kv[b].z, kv[b].w), s2[a][b]);
+  }
+  float* Sh = Sc + n * (int64_t)S * S;
+#pragma unroll
+  for (int a = 0; a < RT; ++a) {
+    const int row = q0 + ty + 8 * a;
+    if (row >= S) continue;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const int key = k0 + tx + 16 * b;
+      if (key >= S) continue;
+      Sh[(int64_t)row * S + key] = (causal && key > row) ? -INFINITY : s2[a][b].x + s2[a][b].y;
+    }
+  }
+}
+
+template <int D>
+struct Nx2 {
+  static constexpr int LDP = kBC + 16;   // P rows ty and ty + 1 16 banks apart
+  static constexpr int G = D / 32;
+  static constexpr int NO = 2 * G;
+  static constexpr int PBUF = kBR * LDP;
+  static constexpr int VBUF = kBC * D;
+  static constexpr int GROUP = 2 * (PBUF + VBUF) + kBC * D;  // P + V x 2, Vp
+  static constexpr int SMEM_FLOATS = 2 * GROUP;
+};
+
+template <int D>
+__global__ void __launch_bounds__(2 * kNx2Threads, 1) naive_pv_x2_kernel(const float* __restrict__ Sc,
+                                                                      const float* __restrict__ V,
+                                                                      float* __restrict__ O, int64_t N, int S,
+                                                                      int causal) {
+  static_assert(D == 32 || D == 64, "paired-FMA naive P V pass: d = 32 and 64");
+  using F = Nx2<D>;
+  constexpr int RT = 8;
+  extern __shared__ float4 smem4[];
+  const int grp = threadIdx.x / kNx2Threads, ltid = threadIdx.x % kNx2Threads;
+  float* B0 = reinterpret_cast<float*>(smem4) + grp * F::GROUP;  // buffer b: P at B0 + b (PBUF + VBUF), V after it
+  float* Vp = B0 + 2 * (F::PBUF + F::VBUF);                      // [kBC / 2][2 D]
+  const int ntiles = (S + kBR - 1) / kBR;
+  const int64_t n = blockIdx.x % N;
+  const int qt = ntiles - 1 - (int)(blockIdx.x / N);
+  const int q0 = qt * kBR;
+  const int tx = ltid & 15, ty = ltid >> 4;
+  const float* Sh = Sc + n * (int64_t)S * S;
+  const float* Vh = V + n * S * D;
+  const bool vec16 = (S & 3) == 0;
+  // cp.async copies of key tile kt: the P rows q0 .. q0 + 63 (row-major, keys
+  // kt*64 ..) and the V rows; entries past S are zero-filled
+  auto issue = [&](int kt, float* Pr, float* Vr) {
+    const int k0 = kt * kBC;
+    if (vec16) {
+      for (int f = ltid; f < kBR * (kBC / 4); f += kNx2Threads) {
+        const int r = f / (kBC / 4), c4 = f % (kBC / 4);
+        const int row = q0 + r, col = k0 + 4 * c4;
+        const bool ok = row < S && col < S;  // S % 4 == 0: a 4-key chunk is wholly in or out
+        cp_async<16>(Pr + r * F::LDP + 4 * c4, Sh + (ok ? (int64_t)row * S + col : 0), ok);
+      }
+    } else {
+      for (int f = ltid; f < kBR * kBC; f += kNx2Threads) {
+        const int r = f / kBC, c = f % kBC;
+        const int row = q0 + r, col = k0 + c;
+        const bool ok = row < S && col < S;
+        cp_async<4>(Pr + r * F::LDP + c, Sh + (ok ? (int64_t)row * S + col : 0), ok);
+      }
+    }
+    for (int f = ltid; f < kBC * (D / 4); f += kNx2Threads) {
+      const int r = f / (D / 4), c4 = f % (D / 4);
+      const bool ok = k0 + r < S;
+      cp_async<16>(Vr + r * D + 4 * c4, Vh + (int64_t)(ok ? k0 + r : 0) * D + 4 * c4, ok);
+    }
+    cp_async_commit();
+  };
+  auto pbuf = [&](int it) { return B0 + (it & 1) * (F::PBUF + F::VBUF); };
+
+  float o[RT][F::NO];
+#pragma unroll
+  for (int a = 0; a < RT; ++a)
+#pragma unroll
+    for (int j = 0; j < F::NO; ++j) o[a][j] = 0.f;
+
+  const int kt_last = causal ? qt : ntiles - 1;
+  if (grp <= kt_last) issue(grp, pbuf(0), pbuf(0) + F::PBUF);
+  for (int kt = grp, it = 0; kt <= kt_last; kt += 2, ++it) {
+    float* Pr = pbuf(it);
+    const float* Vs = Pr + F::PBUF;
+    cp_async_wait<0>();  // this thread's copies of tile kt have landed
+    fx2_group_bar(grp);  // everyone's have, and everyone finished the previous tile (its P, V and Vp)
+    // tile kt + 2 into the other buffer pair, whose P the previous tile's P V read
+    if (kt + 2 <= kt_last) issue(kt + 2, pbuf(it + 1), pbuf(it + 1) + F::PBUF);
+    if (causal && kt == qt)  // the diagonal tile: keys after the row are masked (-inf from pass 1)
+      for (int f = ltid; f < kBR * kBC; f += kNx2Threads) {
+        const int r = f / kBC, c = f % kBC;
+        if (c > r) Pr[r * F::LDP + c] = 0.f;
+      }
+    for (int w = ltid; w < (kBC / 2) * (D / 4); w += kNx2Threads) {  // V as key pairs
+      const int kp = w / (D / 4), c4 = w % (D / 4);
+      const float4 a = ld4(Vs + (2 * kp) * D + 4 * c4), b = ld4(Vs + (2 * kp + 1) * D + 4 * c4);
+      const float4 lo = make_float4(a.x, b.x, a.y, b.y), hi = make_float4(a.z, b.z, a.w, b.w);
+      float* dst = Vp + kp * 2 * D + 8 * c4;
+      const int sw = ((c4 >> 2) & 1) * 4;
+      st4(dst + sw, sw ? hi : lo);
+      st4(dst + 4 - sw, sw ? lo : hi);
+    }
+    fx2_group_bar(grp);  // Vp and the masked P are visible to the group
+    float2 acc[RT][F::NO];
+#pragma unroll
+    for (int a = 0; a < RT; ++a)
+#pragma unroll
+      for (int j = 0; j < F::NO; ++j) acc[a][j] = make_float2(0.f, 0.f);
+#pragma unroll 2
+    for (int c4 = 0; c4 < kBC / 4; ++c4) {
+      float4 v[2][F::G];
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+        for (int g = 0; g < F::G; ++g) v[kk][g] = ld4(Vp + (2 * c4 + kk) * 2 * D + 64 * g + 4 * tx);
+      float4 pv[RT];
+#pragma unroll
+      for (int a = 0; a < RT; ++a) pv[a] = ld4(Pr + (ty + 8 * a) * F::LDP + 4 * c4);
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+        for (int a = 0; a < RT; ++a) {
+          const float2 pp = kk == 0 ? make_float2(pv[a].x, pv[a].y) : make_float2(pv[a].z, pv[a].w);
+#pragma unroll
+          for (int g = 0; g < F::G; ++g) {
+            acc[a][2 * g] = __ffma2_rn(pp, make_float2(v[kk][g].x, v[kk][g].y), acc[a][2 * g]);
+            acc[a][2 * g + 1] = __ffma2_rn(pp, make_float2(v[kk][g].z, v[kk][g].w), acc[a][2 * g + 1]);
+          }
+        }
+    }
+#pragma unroll
+    for (int a = 0; a < RT; ++a)
+#pragma unroll
+      for (int j = 0; j < F::NO; ++j) o[a][j] += acc[a][j].x + acc[a][j].y;
+  }
+  // group 0 adds group 1's sums (group 1's buffers hold them)
+  float* X = reinterpret_cast<float*>(smem4) + F::GROUP;
+  static_assert(RT * F::NO * kNx2Threads <= F::GROUP, "partial sums fit in one group's buffers");
+  __syncthreads();
+  if (grp == 1) {
+#pragma unroll
+    for (int a = 0; a < RT; ++a)
+#pragma unroll
+      for (int j = 0; j < F::NO; ++j) X[(a * F::NO + j) * kNx2Threads + ltid] = o[a][j];
+  }
+  __syncthreads();
+  if (grp == 1) return;
+#pragma unroll
+  for (int a = 0; a < RT; ++a) {
+    const int row = q0 + ty + 8 * a;
+    if (row >= S) continue;
+    float* orow = O + (n * S + row) * D;
+#pragma unroll
+    for (int g = 0; g < F::G; ++g)
+      *reinterpret_cast<float2*>(orow + 32 * g + 2 * tx) =
+          make_float2(o[a][2 * g] + X[(a * F::NO + 2 * g) * kNx2Threads + ltid],
+                      o[a][2 * g + 1] + X[(a * F::NO + 2 * g + 1) * kNx2Threads + ltid]);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // fused: the S-length score rows live in shared memory, one pass over the keys
 // (kbench, "The three GPU kernels": one block per query row, shared memory
 // O(S)). A block takes R consecutive query rows of one head (R = 4 where their
@@ -1116,21 +1341,35 @@ cudaError_t flash_launch(const AttnProblem& p, cudaStream_t st) {
     return flash_launch<D>(flash_f32_kernel<D>, kFlashThreads, p, st);
 }
 
+// d <= 64: the paired-FMA score and P V passes; d = 128: the scalar ones.
 template <int D>
 cudaError_t naive_launch(const AttnProblem& p, float* scores, cudaStream_t st) {
-  cudaError_t e = set_smem(naive_scores_kernel<D>, naive_scores_smem(D));
-  if (e == cudaSuccess) e = set_smem(naive_pv_kernel<D>, naive_pv_smem(D));
+  constexpr bool X2 = D <= 64;
+  constexpr int XD = X2 ? D : 64;  // keeps the paired kernels' templates instantiable at d = 128
+  const size_t sc_smem = X2 ? sizeof(float) * (size_t)(2 * kBR * (D + 4)) : naive_scores_smem(D);
+  const size_t pv_smem = X2 ? sizeof(float) * (size_t)Nx2<XD>::SMEM_FLOATS : naive_pv_smem(D);
+  cudaError_t e = X2 ? set_smem(naive_scores_x2_kernel<XD>, sc_smem) : set_smem(naive_scores_kernel<D>, sc_smem);
+  if (e == cudaSuccess)
+    e = X2 ? set_smem(naive_pv_x2_kernel<XD>, pv_smem) : set_smem(naive_pv_kernel<D>, pv_smem);
   if (e != cudaSuccess) return e;
   const int tiles = (p.S + kBR - 1) / kBR;
-  naive_scores_kernel<D><<<dim3(tiles, tiles, (unsigned)p.N), kThreads, naive_scores_smem(D), st>>>(
-      (const float*)p.q, (const float*)p.k, scores, p.N, p.S, p.causal, p.scale);
+  if constexpr (X2)
+    naive_scores_x2_kernel<XD><<<dim3(tiles, tiles, (unsigned)p.N), kNx2Threads, sc_smem, st>>>(
+        (const float*)p.q, (const float*)p.k, scores, p.N, p.S, p.causal, p.scale);
+  else
+    naive_scores_kernel<D><<<dim3(tiles, tiles, (unsigned)p.N), kThreads, sc_smem, st>>>(
+        (const float*)p.q, (const float*)p.k, scores, p.N, p.S, p.causal, p.scale);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int64_t rows = p.N * p.S;
   naive_softmax_kernel<<<(unsigned)((rows + kThreads / 32 - 1) / (kThreads / 32)), kThreads, 0, st>>>(
       scores, rows, p.S, p.causal);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  naive_pv_kernel<D><<<(unsigned)(tiles * p.N), kFlashThreads, naive_pv_smem(D), st>>>(
-      scores, (const float*)p.v, (float*)p.o, p.N, p.S, p.causal);
+  if constexpr (X2)
+    naive_pv_x2_kernel<XD><<<(unsigned)(tiles * p.N), 2 * kNx2Threads, pv_smem, st>>>(
+        scores, (const float*)p.v, (float*)p.o, p.N, p.S, p.causal);
+  else
+    naive_pv_kernel<D><<<(unsigned)(tiles * p.N), kFlashThreads, pv_smem, st>>>(
+        scores, (const float*)p.v, (float*)p.o, p.N, p.S, p.causal);
   return cudaGetLastError();
 }
 
