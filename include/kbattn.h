@@ -141,8 +141,10 @@ typedef struct {
  * kb_attn_workspace_bytes): this call takes them from a per-device cache that
  * it grows with cudaMalloc, synchronising the device first when it replaces a
  * smaller buffer (so it may allocate and block); calls on different streams
- * share that cache and must not overlap. kb_attn_fwd_ws lets the caller supply
- * the workspace instead.
+ * share that cache and must not overlap on the device. The cache's lock is
+ * held until a call's kernels are enqueued, so a call from another host thread
+ * that grows the cache never frees a buffer under a launch still being made.
+ * kb_attn_fwd_ws lets the caller supply the workspace instead.
  */
 KB_API int kb_attn_fwd(const void* q, const void* k, const void* v, void* o,
                 int B, int H, int S, int d, int causal, float scale,

@@ -114,11 +114,14 @@ struct Workspace {
 };
 Workspace g_ws;
 
-int cached_workspace(size_t need, void** out) {
+// The caller holds g_ws.mu, and keeps holding it until the kernels that use
+// the returned buffer are enqueued: a concurrent call that replaces the buffer
+// synchronises the device before freeing it, which covers only work already
+// enqueued.
+int cached_workspace_locked(size_t need, void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e);
-  std::lock_guard<std::mutex> lk(g_ws.mu);
   if ((int)g_ws.ptr.size() <= dev) {
     g_ws.ptr.resize(dev + 1, nullptr);
     g_ws.bytes.resize(dev + 1, 0);
@@ -152,6 +155,7 @@ int run_attention(const void* q, const void* k, const void* v, void* o, int B, i
   AttnProblem p{q, k, v, o, (int64_t)B * H, S, d, causal, scale, dtype};
   p.lse = lse;
   float* scores = nullptr;
+  std::unique_lock<std::mutex> ws_lock(g_ws.mu, std::defer_lock);  // held through the launch below
   if (var == KB_NAIVE) {
     const size_t need = naive_workspace_bytes(p.N, S);
     if (caller_ws) {
@@ -162,7 +166,8 @@ int run_attention(const void* q, const void* k, const void* v, void* o, int B, i
     } else {
       if ((st = check_device()) != KB_OK) return st;
       void* w = nullptr;
-      if ((st = cached_workspace(need, &w)) != KB_OK) return st;
+      ws_lock.lock();
+      if ((st = cached_workspace_locked(need, &w)) != KB_OK) return st;
       scores = static_cast<float*>(w);
     }
   } else if ((st = check_device()) != KB_OK) {
@@ -176,7 +181,8 @@ int run_attention(const void* q, const void* k, const void* v, void* o, int B, i
       if (workspace && ws_bytes >= need && aligned16(workspace)) p.work = static_cast<float*>(workspace);
     } else {
       void* w = nullptr;
-      if ((st = cached_workspace(need, &w)) != KB_OK) return st;
+      ws_lock.lock();
+      if ((st = cached_workspace_locked(need, &w)) != KB_OK) return st;
       p.work = static_cast<float*>(w);
     }
   }
