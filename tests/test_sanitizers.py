@@ -1,4 +1,4 @@
-"""AddressSanitizer and UndefinedBehaviorSanitizer builds (CPU, no GPU).
+"""AddressSanitizer, UndefinedBehaviorSanitizer and ThreadSanitizer builds (CPU, no GPU).
 
 The oracle's C source and the library's host-side code (every translation unit
 of libkbattn, with its device code compiled as usual) are rebuilt with
@@ -9,8 +9,11 @@ validation of every entry point, the workspace sizing, the tensor-core path's
 work lists over a grid of shapes, and the small host-only calls. Any invalid
 access, overflow or undefined operation aborts the driver. Nothing here
 launches a kernel (every attention call is rejected by validation first), so
-a GPU is neither needed nor touched. This is the substitute for the sanitizer
-runs of the GPU code, which are not available here.
+a GPU is neither needed nor touched. A third build under ``-fsanitize=thread``
+runs the host-only calls from eight threads at once (``thread_driver.cpp``): the
+work lists' shared per-shape cache, validation, the status strings and the
+per-thread last error. This is the substitute for the sanitizer runs of the GPU
+code, which are not available here.
 """
 import concurrent.futures as cf
 import os
@@ -74,4 +77,26 @@ def test_library_host_code_under_address_and_undefined_sanitizers(gcc, tmp_path)
     run(["g++", *SAN, "-O1", "-std=c++17", "-I", kb_build.INCLUDE, os.path.join(HERE, "host_driver.cpp"), *objs,
          "-L", cudalib, "-lcudart_static", "-ldl", "-lpthread", "-lrt", "-o", exe])
     r = run([exe], env=ENV, timeout=600)
+    assert "all checks passed" in r.stdout
+
+
+def test_library_host_code_under_thread_sanitizer(gcc, tmp_path):
+    cudalib = cuda_lib_dir()
+    nvcc = kb_build.nvcc()
+    tsan = ["-fsanitize=thread", "-fno-omit-frame-pointer", "-g"]
+    xsan = [x for f in tsan for x in ("-Xcompiler", f)]
+
+    def compile_one(src):
+        obj = str(tmp_path / (os.path.splitext(src)[0] + ".o"))
+        run([nvcc, *kb_build.ARCH, *kb_build.NVCC_FLAGS, *xsan, "-I", kb_build.INCLUDE, "-c",
+             os.path.join(kb_build.CSRC, src), "-o", obj])
+        return obj
+
+    with cf.ThreadPoolExecutor(max_workers=len(kb_build.SOURCES)) as ex:
+        objs = list(ex.map(compile_one, kb_build.SOURCES))
+    exe = str(tmp_path / "host_tsan")
+    run(["g++", *tsan, "-O1", "-std=c++17", "-I", kb_build.INCLUDE, os.path.join(HERE, "thread_driver.cpp"), *objs,
+         "-L", cudalib, "-lcudart_static", "-ldl", "-lpthread", "-lrt", "-o", exe])
+    env = dict(os.environ, TSAN_OPTIONS="halt_on_error=1:second_deadlock_stack=1")
+    r = run([exe], env=env, timeout=600)
     assert "all checks passed" in r.stdout
