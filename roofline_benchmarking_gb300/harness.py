@@ -6,6 +6,11 @@ written as CSV, Markdown and JSON lines.
   python -m roofline_benchmarking_gb300.harness [--only SUBSTR] [--out DIR]
                                                 [--seconds S] [--quick] [--sweep]
 
+Every row is appended to ``checkpoint.jsonl`` in the output directory as soon as
+it is measured; ``--resume`` reuses the rows found there (a run that was cut off
+keeps what it finished) and measures only the missing ones, then writes the
+outputs from all of them.
+
 ``--sweep`` runs only the kbench page's sequence sweep (section "Running") with
 the three fp32 variants, and the same sweep widened to S = 16384 on the
 tensor-core path (bf16, d = 64 and 128), and writes their tables (the fp32
@@ -166,6 +171,42 @@ def hbm_rows(peaks, dev_info, quick, sampler, only) -> list[dict]:
     return rows
 
 
+CHECKPOINT = "checkpoint.jsonl"
+
+
+def row_key(row: dict) -> tuple:
+    """What identifies a row across runs: kernel, workload, variant, block."""
+    return (row.get("kernel"), row.get("workload"), row.get("variant"), str(row.get("block", "")))
+
+
+def append_checkpoint(out_dir: str, row: dict) -> None:
+    """Append one finished row to the checkpoint file (one JSON object per line)."""
+    os.makedirs(out_dir, exist_ok=True)
+    with open(os.path.join(out_dir, CHECKPOINT), "a") as f:
+        f.write(json.dumps(row) + "\n")
+        f.flush()
+        os.fsync(f.fileno())
+
+
+def load_checkpoint(out_dir: str) -> dict:
+    """Rows of an earlier run's checkpoint by row_key (the last copy of a key
+    wins); a line cut short by an interrupted write, or any other line that is
+    not a complete row, is ignored."""
+    rows = {}
+    try:
+        with open(os.path.join(out_dir, CHECKPOINT)) as f:
+            for line in f:
+                try:
+                    r = json.loads(line)
+                except ValueError:
+                    continue
+                if isinstance(r, dict) and "kernel" in r and "workload" in r and "variant" in r:
+                    rows[row_key(r)] = r
+    except OSError:
+        pass
+    return rows
+
+
 def write_outputs(rows, out_dir, meta):
     os.makedirs(out_dir, exist_ok=True)
     with open(os.path.join(out_dir, "results.jsonl"), "w") as f:
@@ -246,6 +287,8 @@ def main(argv=None) -> int:
                         "tensor-core widening (bf16, d = 64 and 128, S = 128 ... 16384); no HBM rows unless "
                         "--with-hbm")
     p.add_argument("--with-hbm", action="store_true", help="with --sweep: run the HBM kernels too")
+    p.add_argument("--resume", action="store_true",
+                   help="reuse the rows in OUT/checkpoint.jsonl and measure only the missing ones")
     args = p.parse_args(argv)
     if args.sweep and not args.with_hbm:
         args.no_hbm = True
@@ -263,13 +306,21 @@ def main(argv=None) -> int:
     time.sleep(0.3)
     rows, hbm = [], []
     only = args.only.lower()
+    done = load_checkpoint(args.out) if args.resume else {}
+    if not args.resume and os.path.exists(os.path.join(args.out, CHECKPOINT)):
+        os.remove(os.path.join(args.out, CHECKPOINT))
     try:
         # the HBM kernels first: the best STREAM Triad of this run is the attention rows'
         # bandwidth roof (the measured copy figure when the HBM rows are not run)
         if not args.no_hbm:
-            for r in hbm_rows(peaks, info, args.quick, sampler, only):
-                hbm.append(r)
-                print(json.dumps(r), flush=True)
+            earlier = [r for r in done.values() if r["kernel"] != "attention"]
+            if any(r["kernel"] == "triad" for r in earlier):
+                hbm = earlier  # the HBM rows of the interrupted run, Triad included
+            else:
+                for r in hbm_rows(peaks, info, args.quick, sampler, only):
+                    hbm.append(r)
+                    append_checkpoint(args.out, r)
+                    print(json.dumps(r), flush=True)
         triad = [r["gbs"] for r in hbm if r["kernel"] == "triad"]
         bandwidth = max(triad) if triad else peaks["hbm_gbs"]
         bw_source = "best STREAM Triad of this run" if triad else "measured copy bandwidth (no Triad run)"
@@ -278,11 +329,19 @@ def main(argv=None) -> int:
             for variant in ATTN_VARIANTS[w.dtype]:
                 if only and only not in w.name.lower() and only not in variant.name.lower():
                     continue
-                rows.append(attention_row(w, variant, peaks, info, args.seconds, sampler, bandwidth))
-                print(json.dumps(rows[-1]), flush=True)
+                base = done.get(("attention", w.name, variant.name, ""))
+                if base is None:
+                    base = attention_row(w, variant, peaks, info, args.seconds, sampler, bandwidth)
+                    append_checkpoint(args.out, base)
+                    print(json.dumps(base), flush=True)
+                rows.append(base)
                 if w.flops < 1e8:  # launch-bound sizes: also timed as a CUDA graph
-                    rows.append(graph_row(w, variant, rows[-1], sampler))
-                    print(json.dumps(rows[-1]), flush=True)
+                    g = done.get(("attention", w.name, f"{variant.name}+graph{GRAPH_LAUNCHES}", ""))
+                    if g is None:
+                        g = graph_row(w, variant, base, sampler)
+                        append_checkpoint(args.out, g)
+                        print(json.dumps(g), flush=True)
+                    rows.append(g)
         rows += hbm
     finally:
         sampler.stop()

@@ -1,5 +1,6 @@
 """Host logic of the measurement harness (no GPU): the naive variant's score
-traffic model and the one-schema CSV / Markdown / JSON output."""
+traffic model, the one-schema CSV / Markdown / JSON output and the row
+checkpoint that ``--resume`` reads."""
 import csv
 import json
 
@@ -69,3 +70,23 @@ def test_harness_runs_a_quick_sweep(tmp_path):
     assert {r["variant"] for r in rows} == {"NAIVE", "FUSED", "FLASH", "NAIVE+graph200", "FUSED+graph200",
                                             "FLASH+graph200"}
     assert all(r["p50_ms"] > 0 and 0 < r["roofline_frac"] < 2 for r in rows)
+
+
+def test_checkpoint_keeps_finished_rows_and_ignores_a_cut_line(tmp_path):
+    out = str(tmp_path)
+    a = {"kernel": "attention", "workload": "w1", "variant": "TC", "block": "", "p50_ms": 0.2}
+    g = dict(a, variant="TC+graph200", p50_ms=0.1)
+    t1 = {"kernel": "triad", "workload": "2048 MiB arrays", "variant": "triad", "block": 256, "gbs": 7000.0}
+    t2 = dict(t1, block=512, gbs=7100.0)
+    for r in (a, g, t1, t2):
+        harness.append_checkpoint(out, r)
+    harness.append_checkpoint(out, dict(a, p50_ms=0.25))          # a later copy of the same row wins
+    with open(tmp_path / harness.CHECKPOINT, "a") as f:
+        f.write('{"kernel": "attention", "workload": "w2", "vari')  # a write cut off by an interruption
+        f.write("\n[1, 2, 3]\n")                                   # not a row
+    done = harness.load_checkpoint(out)
+    assert set(done) == {("attention", "w1", "TC", ""), ("attention", "w1", "TC+graph200", ""),
+                         ("triad", "2048 MiB arrays", "triad", "256"), ("triad", "2048 MiB arrays", "triad", "512")}
+    assert done[("attention", "w1", "TC", "")]["p50_ms"] == 0.25
+    assert harness.row_key(t1) == ("triad", "2048 MiB arrays", "triad", "256")
+    assert harness.load_checkpoint(str(tmp_path / "missing")) == {}
