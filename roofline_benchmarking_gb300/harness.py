@@ -4,7 +4,9 @@ roofline, with SM clocks sampled during each row. One schema for all rows,
 written as CSV, Markdown and JSON lines.
 
   python -m roofline_benchmarking_gb300.harness [--only SUBSTR] [--out DIR]
-                                                [--seconds S] [--quick] [--sweep]
+                                                [--seconds S] [--quick] [--sweep] [--resume]
+                                                [--config NAMES] [--variant NAMES]
+                                                [--warmup W] [--iters N] [--size-mb MB]
 
 Every row is appended to ``checkpoint.jsonl`` in the output directory as soon as
 it is measured; ``--resume`` reuses the rows found there (a run that was cut off
@@ -65,17 +67,28 @@ def naive_score_bytes(w: inputs.Workload) -> float:
     return 5.0 * 4.0 * w.N * visible
 
 
-def attention_row(w, variant, peaks, dev_info, seconds, sampler, bandwidth_gbs: float) -> dict:
+def row_clock(clocks: dict) -> tuple:
+    """The SM clock and throttle reasons of a row: the median of the samples
+    taken while the row ran; a row shorter than one sampling period has none
+    (its neighbours' samples would mostly show the idle clock between rows)."""
+    if clocks.get("window") != "timed region":
+        return None, "no sample (row shorter than one clock sample)"
+    return clocks["sm_mhz"], "+".join(clocks["reasons"]) or "none"
+
+
+def attention_row(w, variant, peaks, dev_info, seconds, sampler, bandwidth_gbs: float, warmup: int = 10,
+                  iters: int = 0) -> dict:
     q, k, v = (t.cuda() for t in inputs.make_qkv(w))
     o = torch.empty_like(q)
     ws = None
     if variant == kbattn.Variant.NAIVE:
         nbytes = kbattn.kb_attn_workspace_bytes(w.B, w.H, w.S, w.d, kbattn.DType.F32, variant)
         ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
-    probe = kbattn.kb_attn_bench(q, k, v, o, w.causal, w.scale, variant, warmup=3, iters=3, workspace=ws)
-    iters = max(10, min(5000, int(seconds / max(statistics.median(probe) * 1e-3, 1e-6))))
+    if iters <= 0:  # as many launches as fill `seconds`
+        probe = kbattn.kb_attn_bench(q, k, v, o, w.causal, w.scale, variant, warmup=3, iters=3, workspace=ws)
+        iters = max(10, min(5000, int(seconds / max(statistics.median(probe) * 1e-3, 1e-6))))
     t0 = time.time()
-    ms = kbattn.kb_attn_bench(q, k, v, o, w.causal, w.scale, variant, warmup=10, iters=iters, workspace=ws)
+    ms = kbattn.kb_attn_bench(q, k, v, o, w.causal, w.scale, variant, warmup=warmup, iters=iters, workspace=ws)
     t1 = time.time()
     if kbattn.kb_check_device_error() != kbattn.Status.OK:
         raise RuntimeError(f"device error in {w.name} {variant.name}")
@@ -103,8 +116,8 @@ def attention_row(w, variant, peaks, dev_info, seconds, sampler, bandwidth_gbs: 
         bound = "hbm"
     return {"kernel": "attention", "workload": w.name, "variant": variant.name, "dtype": w.dtype, "block": "",
             **st, "tflops": tflops, "gbs": traffic / sec / 1e9, "bound": bound, "attainable": attainable,
-            "roofline_unit": "TFLOP/s", "roofline_frac": tflops / attainable, "sm_mhz": clocks["sm_mhz"],
-            "clock_reasons": "+".join(clocks["reasons"]) or "none"}
+            "roofline_unit": "TFLOP/s", "roofline_frac": tflops / attainable, "sm_mhz": row_clock(clocks)[0],
+            "clock_reasons": row_clock(clocks)[1]}
 
 
 GRAPH_LAUNCHES = 200
@@ -130,13 +143,15 @@ def graph_row(w, variant, base: dict, sampler) -> dict:
     row = dict(base)
     row.update({**st, "variant": f"{variant.name}+graph{GRAPH_LAUNCHES}", "tflops": tflops,
                 "gbs": base["gbs"] * base["p50_ms"] / st["p50_ms"],
-                "roofline_frac": tflops / base["attainable"], "sm_mhz": clocks["sm_mhz"],
-                "clock_reasons": "+".join(clocks["reasons"]) or "none"})
+                "roofline_frac": tflops / base["attainable"], "sm_mhz": row_clock(clocks)[0],
+                "clock_reasons": row_clock(clocks)[1]})
     return row
 
 
-def hbm_rows(peaks, dev_info, quick, sampler, only) -> list[dict]:
+def hbm_rows(peaks, dev_info, quick, sampler, only, size_mb: int = 0) -> list[dict]:
     n = inputs.TRIAD_N if not quick else inputs.TRIAD_N // 8
+    if size_mb > 0:
+        n = size_mb * (1 << 20) // 4
     a = torch.empty(n, dtype=torch.float32, device="cuda")
     b = torch.ones(n, dtype=torch.float32, device="cuda")
     c = torch.full((n,), 2.0, dtype=torch.float32, device="cuda")
@@ -163,12 +178,16 @@ def hbm_rows(peaks, dev_info, quick, sampler, only) -> list[dict]:
             rows.append({"kernel": name, "workload": f"{n * 4 >> 20} MiB arrays", "variant": name,
                          "dtype": "f32", "block": block, **st, "tflops": 0.0, "gbs": best, "bound": "hbm",
                          "attainable": theo, "roofline_unit": "GB/s", "roofline_frac": best / theo,
-                         "sm_mhz": clocks["sm_mhz"], "clock_reasons": "+".join(clocks["reasons"]) or "none",
+                         "sm_mhz": row_clock(clocks)[0], "clock_reasons": row_clock(clocks)[1],
                          "gbs_median_of_runs": statistics.median(gbs_runs),
                          "frac_of_measured_copy": best / peaks["hbm_gbs"]})
     del a, b, c
     torch.cuda.empty_cache()
     return rows
+
+
+def _mhz(x) -> str:
+    return "n/a" if x is None else f"{x}"
 
 
 CHECKPOINT = "checkpoint.jsonl"
@@ -227,7 +246,7 @@ def write_outputs(rows, out_dir, meta):
     for r in rows:
         md.append(f"| {r['kernel']} | {r['workload']} | {r['variant']} | {r['block']} | {r['p50_ms']:.4f} | "
                   f"{r['min_ms']:.4f} | {r['p99_ms']:.4f} | {r['tflops']:.2f} | {r['gbs']:.0f} | {r['bound']} | "
-                  f"{r['attainable']:.1f} {r['roofline_unit']} | {r['roofline_frac']:.3f} | {r['sm_mhz']} |")
+                  f"{r['attainable']:.1f} {r['roofline_unit']} | {r['roofline_frac']:.3f} | {_mhz(r['sm_mhz'])} |")
     with open(os.path.join(out_dir, "results.md"), "w") as f:
         f.write("\n".join(md) + "\n")
     return "\n".join(md)
@@ -246,7 +265,7 @@ def tc_sweep_table(rows) -> str | None:
         r = by.get(w.name)
         if r is not None:
             md.append(f"| {w.d} | {w.S} | {r['p50_ms']:.4f} | {r['tflops']:.1f} | {r['roofline_frac']:.3f} | "
-                      f"{r['gbs']:.0f} | {r['sm_mhz']} |")
+                      f"{r['gbs']:.0f} | {_mhz(r['sm_mhz'])} |")
     return "\n".join(md)
 
 
@@ -274,7 +293,7 @@ def sweep_table(rows) -> str | None:
     return "\n".join(md)
 
 
-def main(argv=None) -> int:
+def parse_args(argv=None):
     p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     p.add_argument("--only", default="", help="run only rows whose workload, variant or kernel contains this")
     p.add_argument("--out", default="harness_out")
@@ -289,9 +308,52 @@ def main(argv=None) -> int:
     p.add_argument("--with-hbm", action="store_true", help="with --sweep: run the HBM kernels too")
     p.add_argument("--resume", action="store_true",
                    help="reuse the rows in OUT/checkpoint.jsonl and measure only the missing ones")
+    p.add_argument("--config", default="", help="comma-separated workload names (default: all, or the sweep's)")
+    p.add_argument("--variant", default="",
+                   help="comma-separated variants: NAIVE, FUSED, FLASH, TC, FIXEDPOINT (default: each workload's all)")
+    p.add_argument("--warmup", type=int, default=10, help="untimed launches before each attention row")
+    p.add_argument("--iters", type=int, default=0,
+                   help="timed launches per attention row (default: as many as fill --seconds)")
+    p.add_argument("--size-mb", type=int, default=0, help="MiB per HBM-kernel array (default 2048; --quick 256)")
     args = p.parse_args(argv)
     if args.sweep and not args.with_hbm:
         args.no_hbm = True
+    return args
+
+
+def attention_plan(args) -> list:
+    """The (workload, variant) pairs a run measures, in order; raises on an
+    unknown workload or variant name."""
+    if args.no_attention:
+        return []
+    todo = list(inputs.KBENCH_SWEEP + inputs.TC_SWEEP) if args.sweep else list(inputs.WORKLOADS.values())
+    if args.config:
+        names = [n.strip() for n in args.config.split(",") if n.strip()]
+        unknown = [n for n in names if n not in inputs.WORKLOADS]
+        if unknown:
+            raise SystemExit(f"unknown workload(s) {unknown}; known: {sorted(inputs.WORKLOADS)}")
+        todo = [inputs.WORKLOADS[n] for n in names]
+    wanted = None
+    if args.variant:
+        wanted = [n.strip().upper() for n in args.variant.split(",") if n.strip()]
+        bad = [n for n in wanted if n not in kbattn.Variant.__members__ or n == "AUTO"]
+        if bad:
+            raise SystemExit(f"unknown variant(s) {bad}")
+    only = args.only.lower()
+    plan = []
+    for w in todo:
+        for variant in ATTN_VARIANTS[w.dtype]:
+            if wanted is not None and variant.name not in wanted:
+                continue
+            if only and only not in w.name.lower() and only not in variant.name.lower():
+                continue
+            plan.append((w, variant))
+    return plan
+
+
+def main(argv=None) -> int:
+    args = parse_args(argv)
+    plan = attention_plan(args)  # unknown names fail here, before anything is measured
     if not torch.cuda.is_available():
         print("the harness needs a CUDA GPU", file=sys.stderr)
         return 2
@@ -317,31 +379,28 @@ def main(argv=None) -> int:
             if any(r["kernel"] == "triad" for r in earlier):
                 hbm = earlier  # the HBM rows of the interrupted run, Triad included
             else:
-                for r in hbm_rows(peaks, info, args.quick, sampler, only):
+                for r in hbm_rows(peaks, info, args.quick, sampler, only, args.size_mb):
                     hbm.append(r)
                     append_checkpoint(args.out, r)
                     print(json.dumps(r), flush=True)
         triad = [r["gbs"] for r in hbm if r["kernel"] == "triad"]
         bandwidth = max(triad) if triad else peaks["hbm_gbs"]
         bw_source = "best STREAM Triad of this run" if triad else "measured copy bandwidth (no Triad run)"
-        todo = inputs.KBENCH_SWEEP + inputs.TC_SWEEP if args.sweep else inputs.WORKLOADS.values()
-        for w in ([] if args.no_attention else todo):
-            for variant in ATTN_VARIANTS[w.dtype]:
-                if only and only not in w.name.lower() and only not in variant.name.lower():
-                    continue
-                base = done.get(("attention", w.name, variant.name, ""))
-                if base is None:
-                    base = attention_row(w, variant, peaks, info, args.seconds, sampler, bandwidth)
-                    append_checkpoint(args.out, base)
-                    print(json.dumps(base), flush=True)
-                rows.append(base)
-                if w.flops < 1e8:  # launch-bound sizes: also timed as a CUDA graph
-                    g = done.get(("attention", w.name, f"{variant.name}+graph{GRAPH_LAUNCHES}", ""))
-                    if g is None:
-                        g = graph_row(w, variant, base, sampler)
-                        append_checkpoint(args.out, g)
-                        print(json.dumps(g), flush=True)
-                    rows.append(g)
+        for w, variant in plan:
+            base = done.get(("attention", w.name, variant.name, ""))
+            if base is None:
+                base = attention_row(w, variant, peaks, info, args.seconds, sampler, bandwidth, args.warmup,
+                                     args.iters)
+                append_checkpoint(args.out, base)
+                print(json.dumps(base), flush=True)
+            rows.append(base)
+            if w.flops < 1e8:  # launch-bound sizes: also timed as a CUDA graph
+                g = done.get(("attention", w.name, f"{variant.name}+graph{GRAPH_LAUNCHES}", ""))
+                if g is None:
+                    g = graph_row(w, variant, base, sampler)
+                    append_checkpoint(args.out, g)
+                    print(json.dumps(g), flush=True)
+                rows.append(g)
         rows += hbm
     finally:
         sampler.stop()

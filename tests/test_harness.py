@@ -90,3 +90,32 @@ def test_checkpoint_keeps_finished_rows_and_ignores_a_cut_line(tmp_path):
     assert done[("attention", "w1", "TC", "")]["p50_ms"] == 0.25
     assert harness.row_key(t1) == ("triad", "2048 MiB arrays", "triad", "256")
     assert harness.load_checkpoint(str(tmp_path / "missing")) == {}
+
+
+def test_run_plan_from_the_flags():
+    plan = harness.attention_plan(harness.parse_args([]))
+    every = [(w.name, v.name) for w in inputs.WORKLOADS.values() for v in harness.ATTN_VARIANTS[w.dtype]]
+    assert [(w.name, v.name) for w, v in plan] == every
+    plan = harness.attention_plan(harness.parse_args(["--config", "f32_b1h8s1024d64,bf16_b16h12s2048d64",
+                                                      "--variant", "flash,TC"]))
+    assert [(w.name, v.name) for w, v in plan] == [("f32_b1h8s1024d64", "FLASH"), ("bf16_b16h12s2048d64", "TC")]
+    plan = harness.attention_plan(harness.parse_args(["--config", "f32_b1h8s1024d64", "--only", "naive"]))
+    assert [v.name for _, v in plan] == ["NAIVE"]
+    sweep = harness.attention_plan(harness.parse_args(["--sweep", "--variant", "FUSED"]))
+    assert [w.S for w, _ in sweep] == [128, 256, 512, 1024, 2048]
+    assert harness.attention_plan(harness.parse_args(["--no-attention"])) == []
+    args = harness.parse_args(["--warmup", "3", "--iters", "50", "--size-mb", "64"])
+    assert (args.warmup, args.iters, args.size_mb) == (3, 50, 64)
+    with pytest.raises(SystemExit):
+        harness.attention_plan(harness.parse_args(["--config", "no_such_workload"]))
+    with pytest.raises(SystemExit):
+        harness.attention_plan(harness.parse_args(["--variant", "AUTO"]))
+
+
+def test_row_clock_needs_a_sample_inside_the_row():
+    inside = {"window": "timed region", "sm_mhz": 2070.0, "reasons": ["sw_power_cap"]}
+    assert harness.row_clock(inside) == (2070.0, "sw_power_cap")
+    assert harness.row_clock(dict(inside, reasons=[])) == (2070.0, "none")
+    near = {"window": "timed region +- 0.3 s", "sm_mhz": 120.0, "reasons": []}
+    mhz, why = harness.row_clock(near)
+    assert mhz is None and "no sample" in why
