@@ -131,16 +131,17 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(expected_hash: str):
+def profiled_traffic(expected_hash: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel source; else None."""
+    the current kernel source and on this workload; else None."""
     try:
         text = open(PROFILE_SUMMARY).read()
     except OSError:
         return None
     mh = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
     mt = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not mh or not mt or mh.group(1) != expected_hash:
+    mw = re.search(r"profiled_workload:\s*(\S+)", text)
+    if not mh or not mt or not mw or mh.group(1) != expected_hash or mw.group(1) != workload:
         return None
     return float(mt.group(1))
 
@@ -186,7 +187,7 @@ def kernel_for(w, sms: int) -> dict:
     noted), what bounds it, and the peak it is measured against."""
     if w.dtype in ("bf16", "f16"):
         name = (f"attn_tc256_kernel<{w.dtype}>" if w.d == 256 else
-                f"attn_tc_kernel<{64 if w.d <= 64 else 128},{w.dtype}>")
+                f"attn_tc64_kernel<{w.dtype}>" if w.d <= 64 else f"attn_tc_kernel<128,{w.dtype}>")
         return {"kernel": name, "bound": "tensor", "launches_per_step": 1, "peak_key": "bf16_tflops",
                 "peak_note": ("measured bf16 burst (cuBLAS 8192^3)" if w.dtype == "bf16" else
                               "measured bf16 burst (cuBLAS 8192^3) x 1, the nominal fp16:bf16 dense ratio")}
@@ -506,7 +507,7 @@ def run_ours(args, d: Dist):
         "timing": "CUDA events around each launch on the launching stream",
     }
     if kinfo["kernel"].startswith("attn_tc_kernel<128,bf16>"):
-        traffic = profiled_traffic(kernel_source_hash())
+        traffic = profiled_traffic(kernel_source_hash(), w.name)
         if traffic is not None:
             roof["traffic"] = traffic
     if sus is not None:

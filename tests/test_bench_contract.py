@@ -51,8 +51,8 @@ def test_roofline_kernel_follows_the_workload():
     import bench
     from roofline_benchmarking_gb300 import inputs
     want = {"bf16_causal_b4h16s4096d128": ("attn_tc_kernel<128,bf16>", "tensor"),
-            "bf16_b16h12s2048d64": ("attn_tc_kernel<64,bf16>", "tensor"),
-            "f16_b16h12s2048d64": ("attn_tc_kernel<64,f16>", "tensor"),
+            "bf16_b16h12s2048d64": ("attn_tc64_kernel<bf16>", "tensor"),
+            "f16_b16h12s2048d64": ("attn_tc64_kernel<f16>", "tensor"),
             "bf16_causal_b2h16s4096d256": ("attn_tc256_kernel<bf16>", "tensor"),
             "f32_b1h8s1024d64": ("flash_f32x2_kernel", "alu"),
             "f32_b1h8s1024d64_causal": ("flash_f32x2_kernel + flash_merge_kernel", "alu")}
@@ -93,4 +93,14 @@ def test_library_arm_line_names_the_d64_kernel():
     line = run_bench("--workload", "bf16_b16h12s2048d64", "--steps", "3", "--warmup", "3", "--no-e2e",
                      "--no-cpu-baseline", "--no-triad", "--soak-seconds", "0")
     assert line["config"]["workload"] == "bf16_b16h12s2048d64"
-    assert line["roofline"]["kernel"] == "attn_tc_kernel<64,bf16>"
+    assert line["roofline"]["kernel"] == "attn_tc64_kernel<bf16>"
+    assert line["roofline"]["traffic"] is None  # the committed capture is of another workload
+
+
+def test_profiled_traffic_only_for_the_captured_workload_and_source():
+    import bench
+    h = bench.kernel_source_hash()
+    traffic = bench.profiled_traffic(h, bench.HEADLINE)
+    assert traffic is not None and traffic > 0  # the committed capture is of the current source
+    assert bench.profiled_traffic(h, "bf16_causal_b1h32s16384d128_sharp") is None
+    assert bench.profiled_traffic("0" * 16, bench.HEADLINE) is None
