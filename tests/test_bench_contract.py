@@ -104,3 +104,12 @@ def test_profiled_traffic_only_for_the_captured_workload_and_source():
     assert traffic is not None and traffic > 0  # the committed capture is of the current source
     assert bench.profiled_traffic(h, "bf16_causal_b1h32s16384d128_sharp") is None
     assert bench.profiled_traffic("0" * 16, bench.HEADLINE) is None
+
+
+def test_l2_policy_in_the_config():
+    import bench
+    from roofline_benchmarking_gb300 import inputs
+    big = bench.bench_config(inputs.BF16_CAUSAL_S4096, 1)["l2"]
+    assert big.startswith("no flush") and "256 MiB" in big and not bench.flushes_l2(inputs.BF16_CAUSAL_S4096)
+    small = bench.bench_config(inputs.F32_S1024, 1)["l2"]
+    assert small.startswith("flushed") and bench.flushes_l2(inputs.F32_S1024)
