@@ -1,6 +1,6 @@
-"""The benchmark's one-line JSON contract: every key the driver reads, with
-the types and units it expects, for the reference arm (the oracle on the host
-cores; runs on CPU) and for the library's own arm (GPU)."""
+"""The benchmark's one-line JSON contract: every key the line carries, with
+its type and unit, for the reference arm (the oracle on the host cores; runs
+on CPU) and for the library's own arm (GPU)."""
 import json
 import os
 import subprocess
