@@ -711,6 +711,9 @@ __global__ void __launch_bounds__(kThreads) naive_scores_kernel(const float* __r
 }
 
 // naive pass 2: in-place row softmax, one warp per row over its visible keys.
+// When S is a multiple of 4 every row starts 16 bytes aligned and the row is
+// read and written as float4 (the running max rescales the sum once per four
+// scores); the remaining keys, and every key otherwise, one float at a time.
 __global__ void __launch_bounds__(kThreads) naive_softmax_kernel(float* __restrict__ Sc, int64_t rows, int S,
                                                                  int causal) {
   const int64_t r = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
@@ -719,9 +722,18 @@ __global__ void __launch_bounds__(kThreads) naive_softmax_kernel(float* __restri
   const int i = (int)(r % S);
   const int len = causal ? i + 1 : S;
   float* row = Sc + r * S;
+  const int n4 = (S & 3) == 0 ? len >> 2 : 0;  // whole float4s of the visible keys
+  float4* row4 = reinterpret_cast<float4*>(row);
   // one read pass: lane-local running max and sum, then combined across lanes
   float m = -INFINITY, l = 0.f;
-  for (int j = lane; j < len; j += 32) {
+  for (int q = lane; q < n4; q += 32) {
+    const float4 v = row4[q];
+    const float x0 = v.x * kLog2e, x1 = v.y * kLog2e, x2 = v.z * kLog2e, x3 = v.w * kLog2e;
+    const float m_new = fmaxf(m, fmaxf(fmaxf(x0, x1), fmaxf(x2, x3)));
+    l = l * exp2f(m - m_new) + ((exp2f(x0 - m_new) + exp2f(x1 - m_new)) + (exp2f(x2 - m_new) + exp2f(x3 - m_new)));
+    m = m_new;
+  }
+  for (int j = 4 * n4 + lane; j < len; j += 32) {
     const float x = row[j] * kLog2e;
     const float m_new = fmaxf(m, x);
     l = l * exp2f(m - m_new) + exp2f(x - m_new);
@@ -730,7 +742,12 @@ __global__ void __launch_bounds__(kThreads) naive_softmax_kernel(float* __restri
   const float mw = warp_max(m);
   l = warp_sum(m == -INFINITY ? 0.f : l * exp2f(m - mw));
   const float inv = 1.0f / l;
-  for (int j = lane; j < len; j += 32) row[j] = exp2f(row[j] * kLog2e - mw) * inv;
+  for (int q = lane; q < n4; q += 32) {
+    const float4 v = row4[q];
+    row4[q] = make_float4(exp2f(v.x * kLog2e - mw) * inv, exp2f(v.y * kLog2e - mw) * inv,
+                          exp2f(v.z * kLog2e - mw) * inv, exp2f(v.w * kLog2e - mw) * inv);
+  }
+  for (int j = 4 * n4 + lane; j < len; j += 32) row[j] = exp2f(row[j] * kLog2e - mw) * inv;
 }
 
 // naive pass 3: O = P V as a tiled GEMM over the visible key tiles. As in the
